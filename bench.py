@@ -1,0 +1,478 @@
+"""SGEMM throughput on GB300: C = alpha*A*B + beta*C, fp32, through the C ABI.
+
+One "step" is one SGEMM of the benchmark workload (default: M = N = K = 8192,
+A and B uniform[-1,1) from seed 4, alpha = 1, beta = 0) with its inputs already
+resident in HBM.  The inputs (768 MiB) are larger than the 129 MB L2, so no
+flush is needed between steps.
+
+Prints ONE JSON line (rank 0):
+  value      TFLOP/s (2*M*N*K per GEMM) over all ranks, device-timed
+  e2e        the same metric with host buffers: pinned host->device copies of
+             A and B, the GEMM and the device->host copy of C inside the timed
+             region, every step
+  roofline   the dominant kernel against the fp32 FMA peak of the chip
+             (SMs x 128 FMA/clk x 2 FLOP x max SM clock)
+  cpu_baseline  the CPU oracle timed on a bounded sample of the same workload
+
+`--impl reference` times the CPU oracle (the only reference this method has)
+on the same workload, metric and unit, each step a bounded sample of rows.
+
+Launch: python bench.py [--gpus N --steps K --warmup W]; for N > 1 under
+torch.distributed.run, each rank runs an independent replica of the
+workload (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "SGEMM TFLOP/s (2MNK/t) at M=N=K=8192 fp32; % of GB300 FP32 FFMA peak"
+UNIT = "TFLOP/s"
+FMA_PER_SM_PER_CLK = 128      # fp32 FMA lanes per SM (4 sub-partitions x 32)
+L2_BYTES = 129 * 1000 * 1000
+KERNEL_SOURCE = os.path.join(ROOT, "dense_fp32_matrix_06_gb300", "csrc", "ffma_gemm.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def describe(p: workloads.Problem) -> str:
+    d = p.meta.get("dist")
+    return (f"{p.name}: SGEMM M={p.M} N={p.N} K={p.K} fp32 row-major, lda={p.lda} ldb={p.ldb} "
+            f"ldc={p.ldc}, A,B {d} seed {p.meta.get('seed')}, alpha={p.alpha:g}, beta={p.beta:g}")
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (host logic; tested on CPU with gloo)
+# --------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """Max of a float over all ranks (the slowest rank's time)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64,
+                     device=device if (device is not None and dist.get_backend() == "nccl")
+                     else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput(flops_per_step: float, steps: int, world: int, seconds: float) -> float:
+    """Whole-job TFLOP/s: every rank did `steps` GEMMs in at most `seconds`."""
+    if seconds <= 0:
+        return float("nan")
+    return flops_per_step * steps * world / seconds / 1e12
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+
+CLOCK_FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, interval_ms: int = 200):
+        self.interval_ms = interval_ms
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(self.interval_ms)], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self, uuid: str | None):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        return summarize_clocks(rows, uuid)
+
+
+def summarize_clocks(rows, uuid):
+    if uuid:
+        mine = [r for r in rows if r[0].replace("GPU-", "") == uuid.replace("GPU-", "")]
+        rows = mine or rows
+    sm, smax, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for r in rows:
+        try:
+            sm.append(float(r[1]))
+            smax.append(float(r[2]))
+        except ValueError:
+            continue
+        for name, v in zip(names, r[5:9]):
+            if v.strip().lower() == "active":
+                reasons.add(name)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+    # samples under load: within the top half of the observed range
+    lo = max(sm) * 0.5
+    loaded = [x for x in sm if x >= lo] or sm
+    return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+            "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# the CPU oracle as a timed baseline (bounded sample of rows)
+# --------------------------------------------------------------------------
+
+def oracle_rows_rate(p: workloads.Problem, rows: int, seed: int = 0):
+    """Time the oracle on `rows` seeded rows of C; returns (seconds, flops, threads)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    idx = rng.choice(p.M, size=min(rows, p.M), replace=False).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.sgemm_rows(p.M, p.N, p.K, p.alpha, p.A, p.B, p.beta, p.C0, idx, lda=p.lda,
+                      ldb=p.ldb, ldc0=p.ldc)
+    dt = time.perf_counter() - t0
+    return dt, 2.0 * len(idx) * p.N * p.K, oracle.max_threads()
+
+
+def calibrate_rows(p: workloads.Problem, target_s: float) -> int:
+    """Rows of C the oracle finishes in about `target_s` seconds on all cores."""
+    import oracle
+    threads = oracle.max_threads()
+    dt, _, _ = oracle_rows_rate(p, threads, seed=99)
+    per_batch = max(dt, 1e-3)
+    batches = max(1, int(target_s / per_batch))
+    return min(p.M, batches * threads)
+
+
+def cpu_baseline(p: workloads.Problem, target_s: float = 15.0) -> dict:
+    rows = calibrate_rows(p, target_s)
+    dt, flops, threads = oracle_rows_rate(p, rows, seed=1)
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{rows} of {p.M} rows of C ({rows}x{p.N}x{p.K} fp64-accumulated "
+                      f"multiply-adds, {dt:.1f} s on {threads} OpenMP threads)"}
+
+
+# --------------------------------------------------------------------------
+# arms
+# --------------------------------------------------------------------------
+
+def source_hash() -> str:
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def committed_traffic(kernel_id: int, workload: str, flops_per_launch: float):
+    """DRAM bytes per launch from the committed ncu capture, if it was taken on
+    the current kernel source (else None)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = t.get(f"{workload}/kernel{kernel_id}")
+    if not entry or entry.get("source_sha") != source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+def peak_fp32_tflops(sms: int) -> tuple[float, float, str]:
+    """fp32 FMA peak = SMs x 128 x 2 x max SM clock."""
+    mhz, src = None, None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f)["sm_max_mhz"])
+            src = "MEASURED_PEAKS.json sm_max_mhz"
+    except (OSError, ValueError, KeyError):
+        pass
+    if mhz is None:
+        try:
+            out = subprocess.run(["nvidia-smi", "--query-gpu=clocks.max.sm",
+                                  "--format=csv,noheader,nounits"], capture_output=True,
+                                 text=True, timeout=30).stdout.split()
+            mhz = float(out[0])
+            src = "nvidia-smi clocks.max.sm"
+        except Exception:
+            mhz, src = 2070.0, "nominal 2070 MHz"
+    return sms * FMA_PER_SM_PER_CLK * 2 * mhz * 1e6 / 1e12, mhz, src
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+
+    import dense_fp32_matrix_06_gb300 as sg
+    sg.build()
+    sg.load_library()
+
+    p = workloads.workload(args.workload)
+    flops = float(p.flops)
+    A_h = torch.from_numpy(p.A).pin_memory()
+    B_h = torch.from_numpy(p.B).pin_memory()
+    A = A_h.to(device)
+    B = B_h.to(device)
+    C = torch.from_numpy(p.C0).to(device)
+    stream = torch.cuda.current_stream(device)
+    sh = stream.cuda_stream
+    plan = sg.gemm_plan(p.M, p.N, p.K, p.lda, p.ldb, p.ldc, A.data_ptr(), B.data_ptr(),
+                        C.data_ptr())
+    launches_per_gemm = 1
+
+    def step():
+        sg.sgemm_ptr(p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
+                     C.data_ptr(), p.ldc, sh)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+
+    # ---- device-timed region ----
+    sampler = ClockSampler()
+    sampler.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(dist, device)
+    clocks = sampler.stop(str(getattr(torch.cuda.get_device_properties(device), "uuid", "")) or None)
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    per_launch = [a.elapsed_time(b) / 1e3 for a, b in ev]
+    elapsed_max = max_over_ranks(elapsed, dist, device)
+    value = throughput(flops, args.steps, world, elapsed_max)
+
+    # ---- end-to-end: host buffers, copies inside the timed region ----
+    e2e = None
+    if not args.no_e2e:
+        C_h = torch.empty((p.M, p.ldc), dtype=torch.float32).pin_memory()
+        e_steps = max(3, min(args.steps, args.e2e_steps))
+
+        def e2e_step():
+            A.copy_(A_h, non_blocking=True)
+            B.copy_(B_h, non_blocking=True)
+            sg.sgemm_ptr(p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb,
+                         p.beta, C.data_ptr(), p.ldc, sh)
+            C_h.copy_(C, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(device)
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        barrier(dist, device)
+        s0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize(device)
+        e_el = max_over_ranks(s0.elapsed_time(s1) / 1e3, dist, device)
+        h2d = (p.A.nbytes + p.B.nbytes) + (p.C0.nbytes if p.beta != 0 else 0)
+        if p.beta != 0:
+            pass  # C0 would be uploaded too; the default workload has beta = 0
+        e2e = {"value": throughput(flops, e_steps, world, e_el), "unit": UNIT,
+               "h2d_bytes_per_step": int(p.A.nbytes + p.B.nbytes), "d2h_bytes_per_step":
+               int(C_h.numel() * 4), "steps": e_steps}
+
+    props = torch.cuda.get_device_properties(device)
+    sms = props.multi_processor_count
+    peak, mhz, peak_src = peak_fp32_tflops(sms)
+    avg_launch = statistics.mean(per_launch)
+    achieved = flops / avg_launch / 1e12
+    traffic = committed_traffic(plan.kernel, p.name, flops)
+    roofline = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 3),
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                "kernel": f"ffma_gemm_kernel (plan kernel {plan.kernel})",
+                "peak_source": f"{sms} SMs x {FMA_PER_SM_PER_CLK} FMA/clk x 2 x {mhz:.0f} MHz "
+                               f"({peak_src})",
+                "algorithmic_flops_per_launch": flops,
+                "avg_launch_ms": round(avg_launch * 1e3, 4)}
+    if clocks.get("sm_mhz"):
+        peak_at_clock = sms * FMA_PER_SM_PER_CLK * 2 * clocks["sm_mhz"] * 1e6 / 1e12
+        roofline["frac_at_measured_clock"] = round(achieved / peak_at_clock, 4)
+
+    probe = None
+    if args.probe:
+        probe = ffma_probe(sg, device, sms)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(p, target_s=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(elapsed_max / args.steps * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic (seeded uniform[-1,1) inputs, no dataset)",
+            "config": {"workload": describe(p), "M": p.M, "N": p.N, "K": p.K,
+                       "l2": f"inputs larger than L2 ({(p.A.nbytes + p.B.nbytes) >> 20} MiB of "
+                             f"A+B > 129 MB L2); no flush between steps",
+                       "plan": {k: v for k, v in plan.as_dict().items() if k != "reserved"},
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "e2e": e2e, "gpu_launches": args.steps * launches_per_gemm,
+            "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks,
+        }
+        if probe:
+            line["ffma_probe"] = probe
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def ffma_probe(sg, device, sms):
+    """Attainable fp32 FMA rate (packed and scalar issue), CUDA-event timed."""
+    import torch
+    out = {}
+    ctas = sms * 8
+    buf = torch.empty(ctas * 256, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device).cuda_stream
+    iters = 20000
+    for packed in (True, False):
+        sg.ffma_probe(ctas, 100, buf.data_ptr(), packed, stream)
+        torch.cuda.synchronize(device)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        sg.ffma_probe(ctas, iters, buf.data_ptr(), packed, stream)
+        e1.record()
+        torch.cuda.synchronize(device)
+        dt = e0.elapsed_time(e1) / 1e3
+        out["packed" if packed else "scalar"] = round(ctas * 256 * iters * 128 / dt / 1e12, 3)
+    return out
+
+
+def run_reference(args):
+    """The CPU oracle on the same workload: each step a bounded sample of rows."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    p = workloads.workload(args.workload)
+    total_steps = args.steps + args.warmup
+    budget = float(args.ref_seconds)
+    import oracle
+    threads = oracle.max_threads()
+    dt1, _, _ = oracle_rows_rate(p, threads, seed=99)
+    per_step = budget / max(total_steps, 1)
+    rows = max(1, min(p.M, int(per_step / max(dt1, 1e-3)) * threads)) if per_step > dt1 else \
+        max(1, min(threads, int(threads * per_step / max(dt1, 1e-3))))
+    for i in range(args.warmup):
+        oracle_rows_rate(p, rows, seed=1000 + i)
+    times, flops = [], 0.0
+    for i in range(args.steps):
+        dt, f, _ = oracle_rows_rate(p, rows, seed=i)
+        times.append(dt)
+        flops = f
+    el = sum(times)
+    value = flops * args.steps / el / 1e12
+    sample = (f"{rows} of {p.M} rows of C per step ({rows}x{p.N}x{p.K} fp64-accumulated "
+              f"multiply-adds), {threads} OpenMP threads")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded uniform[-1,1) inputs, no dataset)",
+        "config": {"workload": describe(p), "M": p.M, "N": p.N, "K": p.K},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def parse(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="square8192", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-seconds", type=float, default=90.0)
+    ap.add_argument("--probe", action="store_true", help="also time the fp32 FMA probe")
+    return ap.parse_args(argv)
+
+
+def main(argv=None):
+    args = parse(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,294 @@
+"""GB300 (sm_103a) single-precision GEMM: Python binding of libsgemm.so.
+
+The binding only marshals arguments: it turns torch CUDA tensors (or raw
+device addresses) and torch's current stream into the plain pointers, sizes
+and leading dimensions the C ABI in ``include/sgemm.h`` takes, and turns a
+status code into an exception.  Every step of the GEMM runs in the library's
+CUDA kernels.  There is no fallback: if ``libsgemm.so`` is missing or cannot
+run on the current device, the calls raise.
+
+    C = alpha * A @ B + beta * C        (row-major fp32, any M, N, K)
+
+Shape errors raise ValueError before anything is launched, mirroring the
+Python-facing matmul of velog @levelstage "AutoMinepp7" (section
+"직사각형 타일링"), which rejects operands that are not 2-D or whose inner
+dimensions differ.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libsgemm.so")
+
+SGEMM_OK = 0
+STATUS_NAMES = {
+    0: "SGEMM_OK",
+    1: "SGEMM_ERR_INVALID_ARG",
+    2: "SGEMM_ERR_MISALIGNED",
+    3: "SGEMM_ERR_UNSUPPORTED_DEVICE",
+    4: "SGEMM_ERR_LAUNCH",
+    5: "SGEMM_ERR_TIMEOUT",
+    6: "SGEMM_ERR_ALLOC",
+    7: "SGEMM_ERR_WORKSPACE",
+}
+WORKSPACE_COUNTER_BYTES = 16384
+
+# Every symbol include/sgemm.h declares (checked by the tests).
+EXPORTED_SYMBOLS = (
+    "gemm_plan",
+    "gemm_plan_for_sms",
+    "sgemm",
+    "sgemm_with_plan",
+    "sgemm_status_string",
+    "sgemm_last_cuda_error",
+    "sgemm_ffma_probe",
+)
+
+
+class SgemmError(RuntimeError):
+    """A non-OK status from the C ABI."""
+
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = int(status)
+        name = STATUS_NAMES.get(self.status, f"status {status}")
+        msg = f"{where}: {name}"
+        if detail:
+            msg += f" ({detail})"
+        super().__init__(msg)
+
+
+class GemmPlan(ctypes.Structure):
+    """Mirror of gemm_plan_t."""
+
+    _fields_ = [
+        ("mode", ctypes.c_int32),
+        ("kernel", ctypes.c_int32),
+        ("bm", ctypes.c_int32),
+        ("bn", ctypes.c_int32),
+        ("bk", ctypes.c_int32),
+        ("threads", ctypes.c_int32),
+        ("split_k", ctypes.c_int32),
+        ("vec", ctypes.c_int32),
+        ("edge", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("k_per_split", ctypes.c_int64),
+        ("tiles_m", ctypes.c_int64),
+        ("tiles_n", ctypes.c_int64),
+        ("grid_ctas", ctypes.c_int64),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_lock = threading.Lock()
+_lib = None
+
+_i64 = ctypes.c_int64
+_vp = ctypes.c_void_p
+_f32 = ctypes.c_float
+
+
+def build() -> str:
+    """Compile libsgemm.so in-tree (nvcc, sm_103a)."""
+    from . import _build
+    return _build.build()
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libsgemm.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'` "
+                "(there is no CPU fallback)")
+        lib = ctypes.CDLL(LIB_PATH)
+        lib.gemm_plan.argtypes = [_i64, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _vp,
+                                  ctypes.POINTER(GemmPlan)]
+        lib.gemm_plan.restype = ctypes.c_int
+        lib.gemm_plan_for_sms.argtypes = [_i64, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _vp,
+                                          ctypes.c_int32, ctypes.POINTER(GemmPlan)]
+        lib.gemm_plan_for_sms.restype = ctypes.c_int
+        lib.sgemm.argtypes = [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _vp]
+        lib.sgemm.restype = ctypes.c_int
+        lib.sgemm_with_plan.argtypes = [ctypes.POINTER(GemmPlan), _i64, _i64, _i64, _f32, _vp,
+                                        _i64, _vp, _i64, _f32, _vp, _i64, _vp, ctypes.c_size_t,
+                                        _vp]
+        lib.sgemm_with_plan.restype = ctypes.c_int
+        lib.sgemm_status_string.argtypes = [ctypes.c_int]
+        lib.sgemm_status_string.restype = ctypes.c_char_p
+        lib.sgemm_last_cuda_error.argtypes = []
+        lib.sgemm_last_cuda_error.restype = ctypes.c_int
+        lib.sgemm_ffma_probe.argtypes = [_i64, _i64, ctypes.c_int32, _vp, _vp]
+        lib.sgemm_ffma_probe.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != SGEMM_OK:
+        lib = load_library()
+        detail = lib.sgemm_status_string(status).decode()
+        cuda_err = lib.sgemm_last_cuda_error()
+        if cuda_err:
+            detail += f"; cudaError {cuda_err}"
+        raise SgemmError(status, where, detail)
+
+
+def status_string(status: int) -> str:
+    return load_library().sgemm_status_string(int(status)).decode()
+
+
+# --------------------------------------------------------------------------
+# pointer-level calls (same names and argument order as the C ABI)
+# --------------------------------------------------------------------------
+
+def gemm_plan(M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
+              A: int = 0, B: int = 0, C: int = 0) -> GemmPlan:
+    """gemm_plan(): the launch configuration the library picks for a shape."""
+    plan = GemmPlan()
+    _check(load_library().gemm_plan(M, N, K, lda, ldb, ldc, A or None, B or None, C or None,
+                                    ctypes.byref(plan)), "gemm_plan")
+    return plan
+
+
+def gemm_plan_for_sms(M: int, N: int, K: int, lda: int, ldb: int, ldc: int, A: int = 0,
+                      B: int = 0, C: int = 0, sm_count: int = 152) -> GemmPlan:
+    """gemm_plan_for_sms(): plan for a GPU with `sm_count` SMs, no device needed."""
+    plan = GemmPlan()
+    _check(load_library().gemm_plan_for_sms(M, N, K, lda, ldb, ldc, A or None, B or None,
+                                            C or None, sm_count, ctypes.byref(plan)),
+           "gemm_plan_for_sms")
+    return plan
+
+
+def sgemm_ptr(M: int, N: int, K: int, alpha: float, A: int, lda: int, B: int, ldb: int,
+              beta: float, C: int, ldc: int, stream: int = 0) -> None:
+    """sgemm() on raw device addresses; `stream` is a cudaStream_t value."""
+    _check(load_library().sgemm(M, N, K, alpha, A or None, lda, B or None, ldb, beta,
+                                C or None, ldc, stream or None), "sgemm")
+
+
+def sgemm_with_plan_ptr(plan: GemmPlan, M: int, N: int, K: int, alpha: float, A: int, lda: int,
+                        B: int, ldb: int, beta: float, C: int, ldc: int, workspace: int,
+                        workspace_bytes: int, stream: int = 0) -> None:
+    """sgemm_with_plan() on raw device addresses."""
+    _check(load_library().sgemm_with_plan(ctypes.byref(plan), M, N, K, alpha, A or None, lda,
+                                          B or None, ldb, beta, C or None, ldc,
+                                          workspace or None, workspace_bytes, stream or None),
+           "sgemm_with_plan")
+
+
+def ffma_probe(ctas: int, iters: int, out_ptr: int, packed: bool = True, stream: int = 0) -> None:
+    """sgemm_ffma_probe(): FLOPs = ctas * 256 * iters * 128."""
+    _check(load_library().sgemm_ffma_probe(ctas, iters, 1 if packed else 0, out_ptr or None,
+                                           stream or None), "sgemm_ffma_probe")
+
+
+# --------------------------------------------------------------------------
+# torch-tensor convenience layer
+# --------------------------------------------------------------------------
+
+def _row_major_view(t, name: str):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D (got {t.dim()}-D)")
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32 (got {t.dtype})")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    rows, cols = t.shape
+    if cols > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} rows must be contiguous (stride(1) == 1)")
+    ld = t.stride(0) if rows > 1 else max(cols, 1)
+    if ld < max(cols, 1):
+        raise ValueError(f"{name} has a row stride smaller than its width")
+    return t.data_ptr(), int(ld)
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def sgemm(A, B, C=None, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """C = alpha * A @ B + beta * C on torch CUDA float32 tensors.
+
+    A (M, K) and B (K, N) may be row-strided views (stride(1) == 1, any
+    stride(0) >= width).  C (M, N) is written in place; when C is None a new
+    tensor is allocated (and beta must be 0).  Runs asynchronously on `stream`
+    (default: torch's current stream) and returns C.
+    """
+    import torch
+    if not isinstance(A, torch.Tensor) or not isinstance(B, torch.Tensor):
+        raise TypeError("A and B must be torch tensors")
+    if A.dim() != 2 or B.dim() != 2:
+        raise ValueError("sgemm works on 2-D matrices only")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: A is {tuple(A.shape)}, B is {tuple(B.shape)}")
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs an input C")
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    elif tuple(C.shape) != (M, N):
+        raise ValueError(f"C must be ({M}, {N}), got {tuple(C.shape)}")
+    a_ptr, lda = _row_major_view(A, "A")
+    b_ptr, ldb = _row_major_view(B, "B")
+    c_ptr, ldc = _row_major_view(C, "C")
+    if not (A.device == B.device == C.device):
+        raise ValueError("A, B and C must be on the same device")
+    lda = max(lda, K, 1)
+    ldb = max(ldb, N, 1)
+    ldc = max(ldc, N, 1)
+    with torch.cuda.device(A.device):
+        sgemm_ptr(M, N, K, float(alpha), a_ptr, lda, b_ptr, ldb, float(beta), c_ptr, ldc,
+                  _stream_handle(stream))
+    return C
+
+
+def plan_for(A, B, C) -> GemmPlan:
+    """gemm_plan() for torch tensors A (M,K), B (K,N), C (M,N)."""
+    import torch
+    M, K = A.shape
+    N = B.shape[1]
+    a_ptr, lda = _row_major_view(A, "A")
+    b_ptr, ldb = _row_major_view(B, "B")
+    c_ptr, ldc = _row_major_view(C, "C")
+    with torch.cuda.device(A.device):
+        return gemm_plan(M, N, K, max(lda, K, 1), max(ldb, N, 1), max(ldc, N, 1),
+                         a_ptr, b_ptr, c_ptr)
+
+
+def sgemm_with_plan(plan: GemmPlan, A, B, C, alpha: float = 1.0, beta: float = 0.0,
+                    workspace=None, stream=None):
+    """sgemm_with_plan() on torch tensors; `workspace` is a CUDA uint8 tensor
+    (or None when plan.workspace_bytes == 0) whose first
+    WORKSPACE_COUNTER_BYTES bytes are zero before its first use."""
+    import torch
+    M, K = A.shape
+    N = B.shape[1]
+    a_ptr, lda = _row_major_view(A, "A")
+    b_ptr, ldb = _row_major_view(B, "B")
+    c_ptr, ldc = _row_major_view(C, "C")
+    ws_ptr, ws_bytes = 0, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    with torch.cuda.device(A.device):
+        sgemm_with_plan_ptr(plan, M, N, K, float(alpha), a_ptr, max(lda, K, 1), b_ptr,
+                            max(ldb, N, 1), float(beta), c_ptr, max(ldc, N, 1), ws_ptr,
+                            ws_bytes, _stream_handle(stream))
+    return C

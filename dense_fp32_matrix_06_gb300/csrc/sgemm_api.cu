@@ -1,0 +1,357 @@
+// sgemm_api.cu -- the C ABI: argument checks, the per-shape planner, the
+// library-owned split-K workspace and the launches.
+//
+// The boundary follows the Python-facing matmul of velog @levelstage
+// "AutoMinepp7" (section "직사각형 타일링"): check ranks and the inner
+// dimension before any work and report a mismatch as an error; here the
+// caller passes device pointers and leading dimensions instead of arrays, and
+// errors are status codes.  The tile constants the pages tune by hand
+// ("AutoMinepp7", section "세부 조정") become a per-shape choice in gemm_plan.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/sgemm.h"
+#include "sgemm_internal.h"
+
+using namespace sgemm_impl;
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+sgemm_status cuda_fail(cudaError_t e, sgemm_status s) {
+    g_last_cuda_error = int(e);
+    return s;
+}
+
+struct DeviceInfo {
+    bool probed = false;
+    bool supported = false;
+    int sms = 0;
+};
+
+std::mutex g_dev_mu;
+std::vector<DeviceInfo> g_devices;
+
+// SM count of the current device, or 0 when the device cannot run the kernels.
+sgemm_status current_device(int *dev_out, int *sms_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_UNSUPPORTED_DEVICE);
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (int(g_devices.size()) <= dev) g_devices.resize(dev + 1);
+    DeviceInfo &d = g_devices[dev];
+    if (!d.probed) {
+        int major = 0, minor = 0, sms = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaFuncAttributes attr;
+        const bool image_ok = ffma_kernel_attributes(&attr) == cudaSuccess;
+        cudaGetLastError();  // clear a sticky "no kernel image" from the probe
+        d.supported = image_ok && major == 10 && minor == 3 && sms > 0;
+        d.sms = sms;
+        d.probed = true;
+    }
+    if (dev_out) *dev_out = dev;
+    if (sms_out) *sms_out = d.sms;
+    return d.supported ? SGEMM_OK : SGEMM_ERR_UNSUPPORTED_DEVICE;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+sgemm_status check_sizes(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                         int64_t ldc) {
+    if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
+    if (lda < (K > 1 ? K : 1)) return SGEMM_ERR_INVALID_ARG;
+    if (ldb < (N > 1 ? N : 1)) return SGEMM_ERR_INVALID_ARG;
+    if (ldc < (N > 1 ? N : 1)) return SGEMM_ERR_INVALID_ARG;
+    // the tile grid is launched as one 1-D grid dimension
+    if (ceil_div(M, kBM) * ceil_div(N, kBN) > int64_t(INT32_MAX)) return SGEMM_ERR_INVALID_ARG;
+    return SGEMM_OK;
+}
+
+// Split-K choice.  Estimated time in units of "one k of one CTA tile":
+// waves * k_per_split, plus a per-CTA cost for writing and re-reading the
+// partial tiles.  Only considered when the tile grid fills less than one wave
+// of resident CTAs.
+int choose_split(int64_t tiles, int64_t K, int sms, int64_t *k_per_split) {
+    const int64_t slots = int64_t(sms) * kCtasPerSm;
+    const int64_t kslices = ceil_div(K, kBK);
+    int best = 1;
+    int64_t best_kps = kslices * kBK;
+    if (const char *force = std::getenv("SGEMM_FORCE_SPLIT")) {
+        int s = std::atoi(force);
+        if (s >= 1) {
+            if (s > kMaxSplit) s = kMaxSplit;
+            int64_t kps = ceil_div(kslices, s) * kBK;
+            int eff = int(ceil_div(K, kps > 0 ? kps : 1));
+            if (eff < 1) eff = 1;
+            if (eff > 1 && tiles > kMaxSplitTiles) eff = 1, kps = kslices * kBK;
+            *k_per_split = eff > 1 ? kps : kslices * kBK;
+            return eff;
+        }
+    }
+    if (tiles < slots && tiles <= kMaxSplitTiles && K >= 2 * 128) {
+        double best_cost = double(ceil_div(tiles, slots)) * double(best_kps);
+        for (int s = 2; s <= kMaxSplit; ++s) {
+            const int64_t kps = ceil_div(kslices, s) * kBK;
+            if (kps < 128) break;  // keep at least 8 K slices per partition
+            const int eff = int(ceil_div(K, kps));
+            const int64_t ctas = tiles * eff;
+            const double cost = double(ceil_div(ctas, slots)) * (double(kps) + 8.0 * eff + 32.0);
+            if (cost < best_cost * 0.97) {
+                best_cost = cost;
+                best = eff;
+                best_kps = kps;
+            }
+        }
+    }
+    *k_per_split = best_kps;
+    return best;
+}
+
+// Kernel the planner names: the packed-FMA kernel unless SGEMM_FORCE_KERNEL
+// (0 = scalar, 1 = packed) asks otherwise; the override exists for sweeps.
+int32_t default_kernel() {
+    if (const char *force = std::getenv("SGEMM_FORCE_KERNEL")) {
+        const int k = std::atoi(force);
+        if (k == kKernelFfma128 || k == kKernelFfma2x128) return k;
+    }
+    return kKernelFfma2x128;
+}
+
+sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                       int64_t ldc, const void *A, const void *B, const void *C,
+                       int sms, gemm_plan_t *out) {
+    gemm_plan_t p;
+    std::memset(&p, 0, sizeof(p));
+    p.mode = SGEMM_MODE_FFMA;
+    p.kernel = default_kernel();
+    p.bm = kBM;
+    p.bn = kBN;
+    p.bk = kBK;
+    p.threads = kThreads;
+    p.vec = (lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0 && aligned16(A) && aligned16(B) &&
+             aligned16(C))
+                ? 1
+                : 0;
+    p.tiles_m = ceil_div(M, kBM);
+    p.tiles_n = ceil_div(N, kBN);
+    const int64_t tiles = p.tiles_m * p.tiles_n;
+    int64_t kps = 0;
+    p.split_k = (M > 0 && N > 0 && K > 0) ? choose_split(tiles, K, sms, &kps) : 1;
+    p.k_per_split = kps;
+    const bool full = (M % kBM == 0) && (N % kBN == 0) && (K % kBK == 0) &&
+                      (p.split_k == 1 || K % p.k_per_split == 0);
+    p.edge = (p.vec && full) ? 0 : 1;
+    p.grid_ctas = tiles * p.split_k;
+    p.workspace_bytes =
+        p.split_k > 1 ? kCounterBytes + size_t(tiles) * p.split_k * kBM * kBN * sizeof(float)
+                      : 0;
+    *out = p;
+    return SGEMM_OK;
+}
+
+// ---- library-owned workspace: one buffer per (device, stream) ----
+struct Workspace {
+    int dev;
+    void *stream;
+    void *ptr;
+    size_t bytes;
+};
+std::mutex g_ws_mu;
+std::vector<Workspace> g_ws;
+
+sgemm_status library_workspace(int dev, cudaStream_t stream, size_t bytes, void **out) {
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    Workspace *w = nullptr;
+    for (auto &e : g_ws)
+        if (e.dev == dev && e.stream == (void *)stream) w = &e;
+    if (w && w->bytes >= bytes) {
+        *out = w->ptr;
+        return SGEMM_OK;
+    }
+    size_t want = bytes + bytes / 4;
+    want = (want + 0xFFFFF) & ~size_t(0xFFFFF);
+    void *p = nullptr;
+    cudaError_t e = cudaMallocAsync(&p, want, stream);
+    if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_ALLOC);
+    e = cudaMemsetAsync(p, 0, kCounterBytes, stream);
+    if (e != cudaSuccess) {
+        cudaFreeAsync(p, stream);
+        return cuda_fail(e, SGEMM_ERR_ALLOC);
+    }
+    if (w) {
+        cudaFreeAsync(w->ptr, stream);  // stream-ordered: after earlier users
+        w->ptr = p;
+        w->bytes = want;
+    } else {
+        g_ws.push_back(Workspace{dev, (void *)stream, p, want});
+    }
+    *out = p;
+    return SGEMM_OK;
+}
+
+sgemm_status run(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K, float alpha,
+                 const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
+                 float *C, int64_t ldc, void *workspace, cudaStream_t stream) {
+    if (M == 0 || N == 0) return SGEMM_OK;
+    cudaError_t e;
+    if (K == 0 || alpha == 0.0f) {
+        e = launch_scale(C, M, N, ldc, beta, stream);
+        return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
+    }
+    GemmArgs a;
+    a.A = A;
+    a.B = B;
+    a.C = C;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.lda = lda;
+    a.ldb = ldb;
+    a.ldc = ldc;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.k_per_split = plan.k_per_split;
+    a.split_k = plan.split_k;
+    a.tiles_m = int32_t(plan.tiles_m);
+    a.tiles_n = int32_t(plan.tiles_n);
+    a.counters = nullptr;
+    a.partials = nullptr;
+    if (plan.split_k > 1) {
+        a.counters = static_cast<unsigned *>(workspace);
+        a.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + kCounterBytes);
+    }
+    e = launch_ffma(a, plan.kernel, plan.vec != 0, plan.edge != 0, stream);
+    return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
+}
+
+bool plan_matches(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int64_t lda,
+                  int64_t ldb, int64_t ldc, const void *A, const void *B, const void *C) {
+    if (p.mode != SGEMM_MODE_FFMA) return false;
+    if (p.kernel != kKernelFfma128 && p.kernel != kKernelFfma2x128) return false;
+    if (p.bm != kBM || p.bn != kBN || p.bk != kBK || p.threads != kThreads) return false;
+    if (p.tiles_m != ceil_div(M, kBM) || p.tiles_n != ceil_div(N, kBN)) return false;
+    if (p.split_k < 1 || p.split_k > kMaxSplit) return false;
+    if (p.k_per_split <= 0 || p.k_per_split % kBK != 0) return false;
+    if (K > 0 && ceil_div(K, p.k_per_split) != p.split_k) return false;
+    if (p.split_k > 1 && p.tiles_m * p.tiles_n > kMaxSplitTiles) return false;
+    const bool vec_ok = lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0 && aligned16(A) &&
+                        aligned16(B) && aligned16(C);
+    if (p.vec && !vec_ok) return false;
+    if (!p.edge) {
+        if (!p.vec) return false;
+        if (M % kBM || N % kBN || K % kBK || (p.split_k > 1 && K % p.k_per_split)) return false;
+    }
+    const size_t need =
+        p.split_k > 1
+            ? kCounterBytes + size_t(p.tiles_m * p.tiles_n) * p.split_k * kBM * kBN * sizeof(float)
+            : 0;
+    return p.workspace_bytes == need;
+}
+
+}  // namespace
+
+extern "C" {
+
+sgemm_status gemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                       int64_t ldc, const void *A, const void *B, const void *C,
+                       gemm_plan_t *out) {
+    if (!out) return SGEMM_ERR_INVALID_ARG;
+    sgemm_status s = check_sizes(M, N, K, lda, ldb, ldc);
+    if (s != SGEMM_OK) return s;
+    int sms = 0;
+    s = current_device(nullptr, &sms);
+    if (s != SGEMM_OK) return s;
+    return plan_impl(M, N, K, lda, ldb, ldc, A, B, C, sms, out);
+}
+
+sgemm_status gemm_plan_for_sms(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                               int64_t ldc, const void *A, const void *B, const void *C,
+                               int32_t sm_count, gemm_plan_t *out) {
+    if (!out || sm_count < 1) return SGEMM_ERR_INVALID_ARG;
+    sgemm_status s = check_sizes(M, N, K, lda, ldb, ldc);
+    if (s != SGEMM_OK) return s;
+    return plan_impl(M, N, K, lda, ldb, ldc, A, B, C, sm_count, out);
+}
+
+sgemm_status sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                   int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                   int64_t ldc, void *stream) {
+    sgemm_status s = check_sizes(M, N, K, lda, ldb, ldc);
+    if (s != SGEMM_OK) return s;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    if (!C) return SGEMM_ERR_INVALID_ARG;
+    if (K > 0 && alpha != 0.0f && (!A || !B)) return SGEMM_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    s = current_device(&dev, &sms);
+    if (s != SGEMM_OK) return s;
+    gemm_plan_t plan;
+    s = plan_impl(M, N, K, lda, ldb, ldc, A, B, C, sms, &plan);
+    if (s != SGEMM_OK) return s;
+    void *ws = nullptr;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (plan.workspace_bytes > 0 && K > 0 && alpha != 0.0f) {
+        s = library_workspace(dev, st, plan.workspace_bytes, &ws);
+        if (s != SGEMM_OK) return s;
+    }
+    return run(plan, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, ws, st);
+}
+
+sgemm_status sgemm_with_plan(const gemm_plan_t *plan, int64_t M, int64_t N, int64_t K,
+                             float alpha, const float *A, int64_t lda, const float *B,
+                             int64_t ldb, float beta, float *C, int64_t ldc, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+    if (!plan) return SGEMM_ERR_INVALID_ARG;
+    sgemm_status s = check_sizes(M, N, K, lda, ldb, ldc);
+    if (s != SGEMM_OK) return s;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    if (!C) return SGEMM_ERR_INVALID_ARG;
+    if (K > 0 && alpha != 0.0f && (!A || !B)) return SGEMM_ERR_INVALID_ARG;
+    if (!plan_matches(*plan, M, N, K, lda, ldb, ldc, A, B, C)) return SGEMM_ERR_INVALID_ARG;
+    if (plan->workspace_bytes > 0) {
+        if (!workspace || workspace_bytes < plan->workspace_bytes) return SGEMM_ERR_WORKSPACE;
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SGEMM_ERR_INVALID_ARG;
+    }
+    s = current_device(nullptr, nullptr);
+    if (s != SGEMM_OK) return s;
+    return run(*plan, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, workspace,
+               static_cast<cudaStream_t>(stream));
+}
+
+const char *sgemm_status_string(sgemm_status status) {
+    switch (status) {
+        case SGEMM_OK: return "SGEMM_OK";
+        case SGEMM_ERR_INVALID_ARG: return "SGEMM_ERR_INVALID_ARG: invalid size, leading dimension, pointer or plan";
+        case SGEMM_ERR_MISALIGNED: return "SGEMM_ERR_MISALIGNED: operand not 16-byte aligned for this mode";
+        case SGEMM_ERR_UNSUPPORTED_DEVICE: return "SGEMM_ERR_UNSUPPORTED_DEVICE: no sm_103 device current";
+        case SGEMM_ERR_LAUNCH: return "SGEMM_ERR_LAUNCH: a CUDA launch or call failed";
+        case SGEMM_ERR_TIMEOUT: return "SGEMM_ERR_TIMEOUT: a bounded device-side wait gave up";
+        case SGEMM_ERR_ALLOC: return "SGEMM_ERR_ALLOC: workspace allocation failed";
+        case SGEMM_ERR_WORKSPACE: return "SGEMM_ERR_WORKSPACE: workspace smaller than the plan needs";
+    }
+    return "SGEMM_ERR_UNKNOWN";
+}
+
+int sgemm_last_cuda_error(void) { return g_last_cuda_error; }
+
+sgemm_status sgemm_ffma_probe(int64_t ctas, int64_t iters, int32_t packed, float *out,
+                              void *stream) {
+    if (ctas <= 0 || ctas > INT32_MAX || iters < 0 || !out) return SGEMM_ERR_INVALID_ARG;
+    sgemm_status s = current_device(nullptr, nullptr);
+    if (s != SGEMM_OK) return s;
+    cudaError_t e =
+        launch_ffma_probe(ctas, iters, packed != 0, out, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
+}
+
+}  // extern "C"

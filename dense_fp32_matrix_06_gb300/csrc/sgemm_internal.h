@@ -1,0 +1,60 @@
+// sgemm_internal.h -- shared between the C ABI layer and the kernel files.
+// Not part of the public interface (that is include/sgemm.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace sgemm_impl {
+
+// CTA tile of the fp32 FFMA kernel: 128 x 128 outputs, K slices of 16,
+// 256 threads, each thread owns an 8 x 8 block of accumulators.
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kBK = 16;
+constexpr int kThreads = 256;
+constexpr int kCtasPerSm = 2;   // resident CTAs per SM the kernel is built for
+constexpr int kGroupM = 8;      // tile rows per raster group (L2 locality)
+
+// Split-K workspace layout: [tile counters: kCounterBytes][partials].  The
+// counter block has a fixed size so a buffer reused across plans never sees
+// stale partial data where a counter is expected.
+constexpr size_t kCounterBytes = 16384;
+constexpr int64_t kMaxSplitTiles = kCounterBytes / sizeof(unsigned);
+constexpr int kMaxSplit = 32;
+
+// Everything a GEMM launch needs, by value.
+struct GemmArgs {
+    const float *A;
+    const float *B;
+    float *C;
+    int64_t M, N, K;
+    int64_t lda, ldb, ldc;
+    float alpha, beta;
+    int64_t k_per_split;   // multiple of kBK
+    int32_t split_k;
+    int32_t tiles_m, tiles_n;
+    unsigned *counters;    // split_k > 1: one per tile, zero on entry and exit
+    float *partials;       // split_k > 1: tiles * split_k * kBM * kBN floats
+};
+
+// Kernel ids a plan can name.
+// Both kernels share the tile, the staging and the arithmetic (one
+// round-to-nearest fp32 FMA per accumulator per k, same order); they differ
+// only in how the FMAs are issued.
+enum KernelId : int32_t {
+    kKernelFfma128 = 0,    // scalar fma.rn.f32
+    kKernelFfma2x128 = 1,  // packed fma.rn.f32x2 (two FMAs per instruction)
+};
+
+cudaError_t launch_ffma(const GemmArgs &a, int kernel, bool vec, bool edge,
+                        cudaStream_t stream);
+cudaError_t launch_scale(float *C, int64_t M, int64_t N, int64_t ldc, float beta,
+                         cudaStream_t stream);
+cudaError_t launch_ffma_probe(int64_t ctas, int64_t iters, bool packed, float *out,
+                              cudaStream_t stream);
+cudaError_t ffma_kernel_attributes(cudaFuncAttributes *attr);
+
+}  // namespace sgemm_impl

@@ -1,0 +1,169 @@
+/*
+ * sgemm.h -- C ABI of the GB300 (sm_103a) single-precision GEMM library.
+ *
+ * Operation (every entry point below computes it, or plans it):
+ *
+ *     C = alpha * A * B + beta * C
+ *
+ * on row-major fp32 matrices: A is M x K with leading dimension lda, B is
+ * K x N with leading dimension ldb, C is M x N with leading dimension ldc.
+ * Element (i, j) of C lives at C[i*ldc + j].
+ *
+ *   - "Micro_gemm_4x4 - cuBLAS micro GEMM skeleton", section 2 (the kernel
+ *     signature: A (M,K), B (K,N), C (M,N), alpha and beta, restrict-qualified,
+ *     so C may not overlap A or B) and section 9 (the final C write: when beta
+ *     is 0 the old C is not read).
+ *   - velog @levelstage "AutoMinepp7", section "직사각형 타일링" (the Python-facing
+ *     matmul boundary: shape checks that throw on a rank or inner-dimension
+ *     mismatch; here they are status codes).
+ *   - "GPU Target" (MLIR tutorial), section "타일링된 행렬 곱셈" (operands are
+ *     strided views; here the stride of a row is the leading dimension).
+ *
+ * Conventions shared by every entry point:
+ *   - A, B and C are DEVICE pointers owned by the caller; the library never
+ *     frees or retains them.  C must not overlap A or B.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Every call is asynchronous on that stream and never
+ *     synchronises the device or the host.
+ *   - Arguments are checked before anything is launched.  M, N, K < 0,
+ *     lda < max(1, K), ldb < max(1, N), ldc < max(1, N), or a NULL pointer
+ *     that the call would dereference -> SGEMM_ERR_INVALID_ARG, nothing
+ *     launched.
+ *   - Quick returns: M == 0 or N == 0 -> SGEMM_OK, no work.  K == 0 or
+ *     alpha == 0 -> C = beta * C without reading A or B (beta == 0 stores
+ *     zeros without reading C).
+ *   - beta == 0: C is write-only; NaN or garbage in C does not propagate.
+ *   - Columns j >= N of C (the padding of a row when ldc > N) are never
+ *     written.
+ *   - The kernels are compiled for sm_103a only; on another device the calls
+ *     return SGEMM_ERR_UNSUPPORTED_DEVICE.
+ *   - Arithmetic: fp32 fused multiply-add, round-to-nearest-even, no
+ *     flush-to-zero.  Each C entry is summed in a fixed order, so repeated
+ *     calls with the same inputs and plan give bit-identical results.
+ */
+#ifndef DENSE_FP32_MATRIX_06_SGEMM_H
+#define DENSE_FP32_MATRIX_06_SGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SGEMM_OK = 0,
+    SGEMM_ERR_INVALID_ARG = 1,        /* bad size, leading dimension, pointer or plan */
+    SGEMM_ERR_MISALIGNED = 2,         /* a mode that needs 16-byte alignment got less */
+    SGEMM_ERR_UNSUPPORTED_DEVICE = 3, /* no device, or not an sm_103 device */
+    SGEMM_ERR_LAUNCH = 4,             /* a CUDA call failed; see sgemm_last_cuda_error */
+    SGEMM_ERR_TIMEOUT = 5,            /* a bounded device-side wait gave up */
+    SGEMM_ERR_ALLOC = 6,              /* the library's workspace could not be grown */
+    SGEMM_ERR_WORKSPACE = 7           /* caller workspace smaller than the plan needs */
+} sgemm_status;
+
+/* Arithmetic mode of a plan. */
+typedef enum {
+    SGEMM_MODE_FFMA = 0     /* fp32 CUDA-core FMA (the default product path) */
+} sgemm_mode;
+
+/* Size of the tile-counter block at the start of a split-K workspace. */
+#define SGEMM_WORKSPACE_COUNTER_BYTES 16384
+
+/* A per-shape launch configuration chosen by gemm_plan.  Plain data: the
+ * caller may inspect it, keep it and pass it back to sgemm_with_plan for any
+ * call with the same (M, N, K, lda, ldb, ldc) and pointers of the same
+ * alignment class. */
+typedef struct {
+    int32_t mode;          /* sgemm_mode */
+    int32_t kernel;        /* 0: scalar fp32 FMA issue, 1: packed fp32x2 FMA issue
+                              (same arithmetic and summation order) */
+    int32_t bm, bn, bk;    /* CTA tile (rows of C, columns of C, K slice) */
+    int32_t threads;       /* threads per CTA */
+    int32_t split_k;       /* number of K partitions (1 = none) */
+    int32_t vec;           /* 1: 16-byte vector loads/stores; 0: 4-byte */
+    int32_t edge;          /* 1: bounds-checked tiles; 0: all tiles full */
+    int32_t reserved;
+    int64_t k_per_split;   /* K extent of one partition (a multiple of bk) */
+    int64_t tiles_m, tiles_n;
+    int64_t grid_ctas;     /* CTAs launched = tiles_m * tiles_n * split_k */
+    size_t workspace_bytes;/* device scratch the plan needs (0 if split_k == 1) */
+} gemm_plan_t;
+
+/*
+ * gemm_plan -- choose the launch configuration for one shape.
+ *   M, N, K, lda, ldb, ldc: as in sgemm.  A, B, C: only their addresses'
+ *   alignment is looked at (they may be NULL, which counts as aligned).
+ *   out: written on success.
+ * Uses the current device's SM count.  Never launches or allocates.
+ * Returns SGEMM_OK, SGEMM_ERR_INVALID_ARG (bad sizes, out == NULL) or
+ * SGEMM_ERR_UNSUPPORTED_DEVICE.
+ */
+sgemm_status gemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                       int64_t ldc, const void *A, const void *B, const void *C,
+                       gemm_plan_t *out);
+
+/*
+ * gemm_plan_for_sms -- gemm_plan for a GPU with `sm_count` SMs, without
+ * querying a device (offline planning, and host-side tests).  The plan is
+ * valid for sgemm_with_plan on a device with that many SMs.
+ * Returns SGEMM_OK or SGEMM_ERR_INVALID_ARG (bad sizes, sm_count < 1,
+ * out == NULL).
+ */
+sgemm_status gemm_plan_for_sms(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                               int64_t ldc, const void *A, const void *B, const void *C,
+                               int32_t sm_count, gemm_plan_t *out);
+
+/*
+ * sgemm -- C = alpha*A*B + beta*C on `stream` (see the conventions above).
+ * Plans the shape with gemm_plan.  When the plan needs workspace (split-K),
+ * the library uses a buffer it owns, one per (device, stream), grown with
+ * stream-ordered allocation and kept until exit; its first use on a stream
+ * therefore allocates.  Returns SGEMM_OK or an error status.
+ */
+sgemm_status sgemm(int64_t M, int64_t N, int64_t K, float alpha,
+                   const float *A, int64_t lda, const float *B, int64_t ldb,
+                   float beta, float *C, int64_t ldc, void *stream);
+
+/*
+ * sgemm_with_plan -- like sgemm, with a plan from gemm_plan and caller-owned
+ * workspace.  `workspace` is a device buffer of at least
+ * plan->workspace_bytes bytes, 256-byte aligned, used only by work queued on
+ * `stream`.  Its first SGEMM_WORKSPACE_COUNTER_BYTES bytes (the tile
+ * counters) must be zero before the first use; every call that completes
+ * leaves them zero again, so one zeroed buffer serves any number of calls and
+ * plans.  Calls that share a workspace must not overlap on the GPU.
+ * workspace may be NULL when plan->workspace_bytes == 0.
+ * Returns SGEMM_ERR_WORKSPACE when workspace_bytes < plan->workspace_bytes,
+ * SGEMM_ERR_INVALID_ARG when the plan does not match the arguments.
+ */
+sgemm_status sgemm_with_plan(const gemm_plan_t *plan, int64_t M, int64_t N, int64_t K,
+                             float alpha, const float *A, int64_t lda,
+                             const float *B, int64_t ldb, float beta, float *C,
+                             int64_t ldc, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char *sgemm_status_string(sgemm_status status);
+
+/* The CUDA error code (a cudaError_t value) behind the last
+ * SGEMM_ERR_LAUNCH / SGEMM_ERR_ALLOC returned on this host thread, 0 if none. */
+int sgemm_last_cuda_error(void);
+
+/*
+ * sgemm_ffma_probe -- a measurement aid, not part of the GEMM: launches
+ * `ctas` CTAs of 256 threads; each thread runs `iters` rounds of 64
+ * independent fp32 FMAs (as 32 packed fma.rn.f32x2 when `packed` != 0, else
+ * 64 scalar fma.rn.f32) and writes one float to `out` (device, ctas*256
+ * floats) so the work cannot be elided.  FLOPs = ctas * 256 * iters * 128.
+ * Timed by the caller, it gives the chip's attainable fp32 FMA rate.
+ * Returns SGEMM_ERR_INVALID_ARG for ctas <= 0, iters < 0 or out == NULL.
+ */
+sgemm_status sgemm_ffma_probe(int64_t ctas, int64_t iters, int32_t packed, float *out,
+                              void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DENSE_FP32_MATRIX_06_SGEMM_H */

@@ -1,0 +1,187 @@
+"""Host-side tests of the C ABI (no GPU work): the library builds, loads and
+exports every symbol include/sgemm.h declares; argument checks reject bad
+input before anything would be launched; the planner's choices."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import dense_fp32_matrix_06_gb300 as sg
+from dense_fp32_matrix_06_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sgemm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return sg.load_library()
+
+
+def declared_functions() -> list[str]:
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([A-Za-z_][A-Za-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_binding_symbols():
+    assert declared_functions() == sorted(sg.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", sg.LIB_PATH], check=True,
+                         capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_build_targets_sm103a_only():
+    flags = _build.ARCH_FLAGS
+    assert flags == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert "--use_fast_math" not in _build.NVCC_FLAGS
+
+
+def test_status_strings(lib):
+    for code, name in sg.STATUS_NAMES.items():
+        assert sg.status_string(code).startswith(name)
+    assert sg.status_string(99) == "SGEMM_ERR_UNKNOWN"
+
+
+BAD_SHAPES = [
+    # M, N, K, lda, ldb, ldc
+    (-1, 4, 4, 4, 4, 4),
+    (4, -1, 4, 4, 4, 4),
+    (4, 4, -1, 4, 4, 4),
+    (4, 4, 8, 7, 4, 4),    # lda < K
+    (4, 8, 4, 4, 7, 8),    # ldb < N
+    (4, 8, 4, 4, 8, 7),    # ldc < N
+    (4, 4, 0, 0, 4, 4),    # lda < 1
+]
+
+
+@pytest.mark.parametrize("shape", BAD_SHAPES)
+def test_invalid_sizes_rejected_before_any_launch(lib, shape):
+    M, N, K, lda, ldb, ldc = shape
+    assert lib.sgemm(M, N, K, 1.0, 16, lda, 16, ldb, 0.0, 16, ldc, None) == 1
+    plan = sg.GemmPlan()
+    assert lib.gemm_plan_for_sms(M, N, K, lda, ldb, ldc, None, None, None, 152,
+                                 ctypes.byref(plan)) == 1
+    assert lib.sgemm_with_plan(ctypes.byref(plan), M, N, K, 1.0, 16, lda, 16, ldb, 0.0, 16,
+                               ldc, None, 0, None) == 1
+
+
+def test_null_pointers_rejected(lib):
+    assert lib.sgemm(4, 4, 4, 1.0, None, 4, 16, 4, 0.0, 16, 4, None) == 1
+    assert lib.sgemm(4, 4, 4, 1.0, 16, 4, None, 4, 0.0, 16, 4, None) == 1
+    assert lib.sgemm(4, 4, 4, 1.0, 16, 4, 16, 4, 0.0, None, 4, None) == 1
+    assert lib.gemm_plan_for_sms(4, 4, 4, 4, 4, 4, None, None, None, 152, None) == 1
+    assert lib.gemm_plan_for_sms(4, 4, 4, 4, 4, 4, None, None, None, 0,
+                                 ctypes.byref(sg.GemmPlan())) == 1
+    assert lib.sgemm_ffma_probe(0, 1, 1, 16, None) == 1
+    assert lib.sgemm_ffma_probe(1, 1, 1, None, None) == 1
+
+
+def test_empty_output_is_a_no_op_without_a_device(lib):
+    # M == 0 or N == 0: nothing to do, succeeds before touching the device
+    assert lib.sgemm(0, 5, 3, 1.0, None, 3, None, 5, 0.0, None, 5, None) == 0
+    assert lib.sgemm(5, 0, 3, 1.0, None, 3, None, 1, 0.0, None, 1, None) == 0
+
+
+def test_device_calls_report_unsupported_without_a_gpu(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    plan = sg.GemmPlan()
+    assert lib.gemm_plan(64, 64, 64, 64, 64, 64, None, None, None, ctypes.byref(plan)) == 3
+
+
+def plan(M, N, K, lda=None, ldb=None, ldc=None, A=0, B=0, C=0, sms=152):
+    return sg.gemm_plan_for_sms(M, N, K, lda or max(K, 1), ldb or max(N, 1), ldc or max(N, 1),
+                                A, B, C, sm_count=sms)
+
+
+def test_plan_full_tiles_take_the_unchecked_vector_path(lib):
+    p = plan(8192, 8192, 8192)
+    assert (p.bm, p.bn, p.bk, p.threads) == (128, 128, 16, 256)
+    assert p.tiles_m == 64 and p.tiles_n == 64
+    assert p.split_k == 1 and p.workspace_bytes == 0
+    assert p.vec == 1 and p.edge == 0
+    assert p.grid_ctas == 4096
+
+
+def test_plan_ragged_shape_takes_the_checked_scalar_path(lib):
+    p = plan(1023, 777, 513, lda=513, ldb=777, ldc=777)
+    assert p.vec == 0 and p.edge == 1
+    assert p.tiles_m == 8 and p.tiles_n == 7
+
+
+def test_plan_misaligned_pointer_disables_vector_loads(lib):
+    assert plan(256, 256, 256, A=4096).vec == 1
+    assert plan(256, 256, 256, A=4100).vec == 0
+    assert plan(256, 256, 256, C=4104).vec == 0
+
+
+def test_plan_split_k_fills_the_gpu_when_tiles_are_few(lib):
+    p = plan(1024, 1024, 16384)          # 64 tiles, long K
+    assert p.split_k > 1
+    assert p.k_per_split % p.bk == 0
+    assert (16384 + p.k_per_split - 1) // p.k_per_split == p.split_k
+    assert p.grid_ctas == 64 * p.split_k
+    assert p.workspace_bytes == sg.WORKSPACE_COUNTER_BYTES + 64 * p.split_k * 128 * 128 * 4
+    # MLP-down: 48 tiles, K = 3072
+    assert plan(1024, 768, 3072).split_k > 1
+    # a full wave of tiles is never split
+    assert plan(8192, 8192, 8192).split_k == 1
+    assert plan(4096, 4096, 4096).split_k == 1
+    # short K is never split below 8 slices per partition
+    q = plan(256, 256, 200)
+    assert q.split_k == 1
+
+
+def test_plan_depends_on_sm_count(lib):
+    small = plan(2048, 2048, 2048, sms=8)
+    big = plan(2048, 2048, 2048, sms=152)
+    assert small.split_k == 1
+    assert big.split_k >= 1
+
+
+def test_sgemm_with_plan_rejects_mismatched_plan_and_small_workspace(lib):
+    p = plan(1024, 1024, 16384)
+    assert p.split_k > 1
+    # workspace too small -> SGEMM_ERR_WORKSPACE (checked before the device)
+    rc = lib.sgemm_with_plan(ctypes.byref(p), 1024, 1024, 16384, 1.0, 4096, 16384, 4096, 1024,
+                             0.0, 4096, 1024, 4096, 16, None)
+    assert rc == 7
+    # plan made for another shape -> SGEMM_ERR_INVALID_ARG
+    rc = lib.sgemm_with_plan(ctypes.byref(p), 1024, 1024, 8192, 1.0, 4096, 8192, 4096, 1024,
+                             0.0, 4096, 1024, 4096, p.workspace_bytes, None)
+    assert rc == 1
+    # a vector plan used with a misaligned pointer -> SGEMM_ERR_INVALID_ARG
+    q = plan(512, 512, 512)
+    rc = lib.sgemm_with_plan(ctypes.byref(q), 512, 512, 512, 1.0, 4100, 512, 4096, 512, 0.0,
+                             4096, 512, None, 0, None)
+    assert rc == 1
+
+
+def test_forced_split_override(lib, monkeypatch):
+    monkeypatch.setenv("SGEMM_FORCE_SPLIT", "4")
+    p = plan(512, 512, 1024)
+    assert p.split_k == 4 and p.k_per_split == 256
+    monkeypatch.setenv("SGEMM_FORCE_SPLIT", "1")
+    assert plan(1024, 1024, 16384).split_k == 1
+
+
+def test_forced_kernel_override(lib, monkeypatch):
+    monkeypatch.setenv("SGEMM_FORCE_KERNEL", "0")
+    assert plan(256, 256, 256).kernel == 0
+    monkeypatch.setenv("SGEMM_FORCE_KERNEL", "1")
+    assert plan(256, 256, 256).kernel == 1

@@ -1,0 +1,322 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Tolerances (the method's own statement of parity):
+  * integer-valued inputs: bit-exact (every partial sum is an integer below
+    2^24, so every summation order gives the same fp32 value);
+  * otherwise: max|C - C_oracle| / (K*max|A|*max|B| + |beta|*max|C0|) <= 1e-6.
+Every test also checks that C's padding and the memory around C are untouched.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL_FFMA = 1e-6
+SENTINEL = np.float32(-12345.5)
+
+
+@pytest.fixture(scope="module")
+def sg():
+    import torch
+    import dense_fp32_matrix_06_gb300 as pkg
+    pkg.build()
+    assert torch.cuda.is_available()
+    pkg.load_library()
+    return pkg
+
+
+def _torch():
+    import torch
+    return torch
+
+
+class DeviceProblem:
+    """A workloads.Problem on the device, with C inside a guard band."""
+
+    def __init__(self, p: workloads.Problem, a_offset: int = 0, b_offset: int = 0,
+                 c_offset: int = 0):
+        torch = _torch()
+        self.p = p
+        dev = torch.device("cuda")
+        self.a_buf = torch.from_numpy(np.concatenate(
+            [np.zeros(a_offset, np.float32), p.A.ravel()])).to(dev)
+        self.b_buf = torch.from_numpy(np.concatenate(
+            [np.zeros(b_offset, np.float32), p.B.ravel()])).to(dev)
+        self.guard = 64 + c_offset
+        c_host = np.full(self.guard + p.C0.size + 64, SENTINEL, np.float32)
+        c_host[self.guard:self.guard + p.C0.size] = p.C0.ravel()
+        # pad columns of C keep their own pad value (from workloads)
+        self.c_host0 = c_host
+        self.c_buf = torch.from_numpy(c_host.copy()).to(dev)
+        self.a_ptr = self.a_buf.data_ptr() + 4 * a_offset
+        self.b_ptr = self.b_buf.data_ptr() + 4 * b_offset
+        self.c_ptr = self.c_buf.data_ptr() + 4 * self.guard
+
+    def run(self, sg, alpha=None, beta=None):
+        p = self.p
+        sg.sgemm_ptr(p.M, p.N, p.K, p.alpha if alpha is None else alpha, self.a_ptr, p.lda,
+                     self.b_ptr, p.ldb, p.beta if beta is None else beta, self.c_ptr, p.ldc,
+                     _torch().cuda.current_stream().cuda_stream)
+
+    def result(self):
+        """(logical C, whole buffer) after a run."""
+        _torch().cuda.synchronize()
+        buf = self.c_buf.cpu().numpy()
+        p = self.p
+        C = buf[self.guard:self.guard + p.C0.size].reshape(p.C0.shape)[:, :p.N]
+        return C.copy(), buf
+
+    def check_untouched(self, buf):
+        p = self.p
+        want = self.c_host0.copy()
+        region = want[self.guard:self.guard + p.C0.size].reshape(p.C0.shape)
+        got_region = buf[self.guard:self.guard + p.C0.size].reshape(p.C0.shape)
+        # everything outside the logical M x N block must be bit-identical
+        mask = np.ones_like(region, dtype=bool)
+        mask[:, :p.N] = False
+        assert np.array_equal(got_region[mask].view(np.uint32), region[mask].view(np.uint32))
+        assert np.array_equal(buf[:self.guard].view(np.uint32), want[:self.guard].view(np.uint32))
+        tail = self.guard + p.C0.size
+        assert np.array_equal(buf[tail:].view(np.uint32), want[tail:].view(np.uint32))
+
+
+def logical(p):
+    return p.A[:, :p.K], p.B[:, :p.N], (p.C0[:, :p.N] if p.beta != 0 else None)
+
+
+def assert_parity(p, C, ref, exact: bool):
+    if exact:
+        assert np.array_equal(C, ref), f"{p.name}: not bit-exact on integer inputs"
+    else:
+        A, B, C0 = logical(p)
+        err = oracle.normalised_error(C, ref, p.K, A, B, p.beta, C0)
+        assert err <= TOL_FFMA, f"{p.name}: normalised error {err:.3e}"
+        assert np.all(np.isfinite(C))
+
+
+def run_and_check(sg, p, exact=False, **offsets):
+    d = DeviceProblem(p, **offsets)
+    d.run(sg)
+    C, buf = d.result()
+    d.check_untouched(buf)
+    ref = oracle.problem(p)
+    assert_parity(p, C, ref, exact)
+    return C
+
+
+SMALL = ["square256", "square256_int", "square1024ab", "ragged", "gpt2_qkv", "gpt2_mlp_up",
+         "gpt2_mlp_down"]
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_workload_full_parity(sg, name):
+    p = workloads.workload(name)
+    run_and_check(sg, p, exact=(p.meta["dist"] == "int4"))
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_workload_integer_copy_bit_exact(sg, name):
+    M, N, K, _, seed, alpha, beta, _ = workloads.WORKLOADS[name]
+    p = workloads.make(M, N, K, dist="int4", seed=seed, alpha=alpha, beta=beta, name=name,
+                       c0_dist="int4")
+    run_and_check(sg, p, exact=True)
+
+
+def test_ragged_leading_dimensions_and_alpha_beta(sg):
+    p = workloads.make(1023, 777, 513, seed=2, lda=515, ldb=781, ldc=779, alpha=-0.75,
+                       beta=1.25, c0_dist="uniform")
+    run_and_check(sg, p)
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_shape_fuzz(sg, seed):
+    rng = np.random.default_rng(1000 + seed)
+    M, N, K = (int(x) for x in rng.integers(1, 301, size=3))
+    lda = K + int(rng.integers(0, 9))
+    ldb = N + int(rng.integers(0, 9))
+    ldc = N + int(rng.integers(0, 9))
+    beta = 0.0 if seed % 2 == 0 else float(rng.uniform(-2, 2))
+    alpha = float(rng.uniform(-2, 2))
+    dist = "int4" if seed % 3 == 0 else "uniform"
+    if dist == "int4":
+        alpha, beta = 1.5, (0.5 if beta else 0.0)
+    p = workloads.make(M, N, K, dist=dist, seed=seed, alpha=alpha, beta=beta, lda=lda,
+                       ldb=ldb, ldc=ldc, c0_dist=dist if beta else None)
+    offs = dict(a_offset=int(seed % 4 == 1), b_offset=int(seed % 5 == 2),
+                c_offset=int(seed % 7 == 3))
+    run_and_check(sg, p, exact=(dist == "int4"), **offs)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (1, 513, 17), (129, 1, 300), (128, 128, 16),
+                                   (127, 129, 15), (256, 384, 1), (3, 5, 4096)])
+def test_edge_shapes(sg, M, N, K):
+    p = workloads.make(M, N, K, seed=M + N + K)
+    run_and_check(sg, p)
+    q = workloads.make(M, N, K, dist="int4", seed=M + N + K)
+    run_and_check(sg, q, exact=True)
+
+
+def test_beta_zero_never_reads_c(sg):
+    p = workloads.make(200, 190, 70, seed=21)   # C0 is NaN where it is logical
+    assert np.isnan(p.C0[:, :p.N]).all()
+    C = run_and_check(sg, p)
+    assert np.all(np.isfinite(C))
+
+
+def test_alpha_zero_and_k_zero_scale_c(sg):
+    p = workloads.make(130, 140, 50, seed=22, beta=0.75, c0_dist="uniform")
+    p.A[:, :p.K] = np.nan
+    p.B[:, :p.N] = np.nan
+    p.alpha = 0.0
+    d = DeviceProblem(p)
+    d.run(sg)
+    C, buf = d.result()
+    d.check_untouched(buf)
+    assert np.array_equal(C, oracle.problem(p))
+    q = workloads.make(130, 140, 0, seed=23, beta=-0.5, c0_dist="uniform")
+    d = DeviceProblem(q)
+    d.run(sg)
+    C, buf = d.result()
+    d.check_untouched(buf)
+    assert np.array_equal(C, oracle.problem(q))
+    r = workloads.make(64, 64, 0, seed=24)   # K = 0, beta = 0: zeros, C not read
+    d = DeviceProblem(r)
+    d.run(sg)
+    C, buf = d.result()
+    assert np.array_equal(C, np.zeros((64, 64), np.float32))
+
+
+def test_empty_shapes_are_no_ops(sg):
+    torch = _torch()
+    c = torch.full((4, 4), 3.0, device="cuda")
+    sg.sgemm_ptr(0, 4, 4, 1.0, c.data_ptr(), 4, c.data_ptr(), 4, 0.0, c.data_ptr(), 4)
+    sg.sgemm_ptr(4, 0, 4, 1.0, c.data_ptr(), 4, c.data_ptr(), 1, 0.0, c.data_ptr(), 1)
+    torch.cuda.synchronize()
+    assert bool((c == 3.0).all())
+
+
+@pytest.mark.parametrize("kernel", ["0", "1"])
+@pytest.mark.parametrize("split", ["1", "2", "3", "7"])
+def test_forced_kernel_and_split(sg, monkeypatch, kernel, split):
+    monkeypatch.setenv("SGEMM_FORCE_KERNEL", kernel)
+    monkeypatch.setenv("SGEMM_FORCE_SPLIT", split)
+    p = workloads.make(300, 260, 1000, seed=31, beta=0.5, c0_dist="uniform")
+    run_and_check(sg, p)
+    q = workloads.make(256, 384, 1024, dist="int4", seed=32, alpha=1.5, beta=0.5,
+                       c0_dist="int4")
+    run_and_check(sg, q, exact=True)
+    r = workloads.make(201, 77, 333, seed=33, lda=335, ldb=79, ldc=81)   # scalar path
+    run_and_check(sg, r)
+
+
+def test_both_kernels_bit_identical(sg, monkeypatch):
+    outs = []
+    for kernel in ("0", "1"):
+        monkeypatch.setenv("SGEMM_FORCE_KERNEL", kernel)
+        for name in ("square1024ab", "ragged", "long_k"):
+            p = workloads.workload(name)
+            d = DeviceProblem(p)
+            d.run(sg)
+            outs.append(d.result()[0])
+    n = len(outs) // 2
+    for a, b in zip(outs[:n], outs[n:]):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_deterministic_run_to_run(sg):
+    for name in ("long_k", "ragged", "gpt2_mlp_down"):
+        p = workloads.workload(name)
+        d = DeviceProblem(p)
+        first = None
+        for _ in range(5):
+            d.run(sg)
+            C, _ = d.result()
+            if first is None:
+                first = C
+            else:
+                assert np.array_equal(C.view(np.uint32), first.view(np.uint32)), name
+
+
+def test_sgemm_with_plan_caller_workspace(sg):
+    torch = _torch()
+    p = workloads.workload("long_k")
+    A = torch.from_numpy(p.A).cuda()
+    B = torch.from_numpy(p.B).cuda()
+    C = torch.empty((p.M, p.N), device="cuda")
+    plan = sg.plan_for(A, B, C)
+    assert plan.split_k > 1 and plan.workspace_bytes > 0
+    ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    ref = oracle.problem(p)
+    for _ in range(3):   # the counters are left zero, so the buffer can be reused
+        C.fill_(float("nan"))
+        sg.sgemm_with_plan(plan, A, B, C, 1.0, 0.0, ws)
+        torch.cuda.synchronize()
+        assert_parity(p, C.cpu().numpy(), ref, exact=False)
+    assert int(ws[:sg.WORKSPACE_COUNTER_BYTES].count_nonzero()) == 0
+    with pytest.raises(sg.SgemmError) as e:
+        sg.sgemm_with_plan(plan, A, B, C, 1.0, 0.0, ws[:16])
+    assert e.value.status == 7
+
+
+def test_torch_api_shapes_and_views(sg):
+    torch = _torch()
+    p = workloads.make(300, 200, 150, seed=41, lda=160, ldb=210)
+    A = torch.from_numpy(p.A).cuda()[:, :p.K]     # row-strided views
+    B = torch.from_numpy(p.B).cuda()[:, :p.N]
+    C = sg.sgemm(A, B)
+    torch.cuda.synchronize()
+    assert_parity(p, C.cpu().numpy(), oracle.problem(p), exact=False)
+    with pytest.raises(ValueError):
+        sg.sgemm(A, B[:-1])
+    with pytest.raises(ValueError):
+        sg.sgemm(A[0], B)
+    with pytest.raises(TypeError):
+        sg.sgemm(A.double(), B)
+    with pytest.raises(ValueError):   # column-strided operand
+        sg.sgemm(A.t().contiguous().t(), B)
+
+
+def test_status_errors_from_device_calls(sg):
+    torch = _torch()
+    x = torch.zeros(64, device="cuda")
+    with pytest.raises(sg.SgemmError) as e:
+        sg.sgemm_ptr(4, 4, 8, 1.0, x.data_ptr(), 7, x.data_ptr(), 4, 0.0, x.data_ptr(), 4)
+    assert e.value.status == 1
+
+
+# ---- full-size workloads: sampled entries against the oracle ----
+
+LARGE = ["square2048", "square4096", "square8192", "skinny_k64", "long_k"]
+
+
+@pytest.mark.parametrize("name", LARGE)
+@pytest.mark.parametrize("dist", ["uniform", "int4"])
+def test_large_workload_sampled(sg, name, dist):
+    p = workloads.workload(name, dist=None if dist == "uniform" else dist)
+    d = DeviceProblem(p)
+    d.run(sg)
+    C, buf = d.result()
+    d.check_untouched(buf)
+    ii, jj = workloads.sample_indices(p.M, p.N, 3000, seed=7)
+    ref = oracle.sgemm_entries(p.M, p.N, p.K, p.alpha, p.A, p.B, p.beta, p.C0, ii, jj,
+                               lda=p.lda, ldb=p.ldb, ldc0=p.ldc)
+    got = C[ii, jj]
+    rows = np.array([0, p.M // 2 + 1, p.M - 1], np.int64)
+    ref_rows = oracle.sgemm_rows(p.M, p.N, p.K, p.alpha, p.A, p.B, p.beta, p.C0, rows,
+                                 lda=p.lda, ldb=p.ldb, ldc0=p.ldc)
+    if dist == "int4":
+        assert np.array_equal(got, ref)
+        assert np.array_equal(C[rows], ref_rows)
+    else:
+        A, B, C0 = logical(p)
+        den = p.K * float(np.abs(A).max()) * float(np.abs(B).max())
+        assert float(np.abs(got.astype(np.float64) - ref).max()) / den <= TOL_FFMA
+        assert float(np.abs(C[rows].astype(np.float64) - ref_rows).max()) / den <= TOL_FFMA
+        assert np.all(np.isfinite(C))

@@ -104,9 +104,9 @@ def make(M: int, N: int, K: int, *, dist: str = "uniform", seed: int = 0,
     ("uniform" U[-1,1), "normal" N(0,1), "int4" integers in {-4..4},
     "gpt2" A ~ N(0,1) and B ~ N(0,0.02)).  C0 is drawn only when beta != 0
     (else it is filled with NaN, which a correct kernel never reads)."""
-    lda = K if lda is None else lda
-    ldb = N if ldb is None else ldb
-    ldc = N if ldc is None else ldc
+    lda = max(K, 1) if lda is None else lda
+    ldb = max(N, 1) if ldb is None else ldb
+    ldc = max(N, 1) if ldc is None else ldc
     rng = np.random.default_rng(seed)
     if dist == "uniform":
         fa = fb = fc = uniform_fill(rng)
