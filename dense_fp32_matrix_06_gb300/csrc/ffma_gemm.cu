@@ -10,11 +10,13 @@
 //    product is a sum of outer products, which keeps the accumulators in
 //    registers; "Micro_gemm_4x4 - cuBLAS micro GEMM skeleton", section 8:
 //    the fully unrolled FMA pattern over the micro tile).
-//  * The 64 FMAs are issued as 32 packed fp32x2 FMAs (fma.rn.f32x2), each a
-//    pair of ordinary round-to-nearest fp32 FMAs, so every accumulator sees
-//    exactly the same sequence of roundings as a scalar fmaf loop.  This
-//    halves the issue slots the FMAs take on Blackwell, leaving room for the
-//    shared-memory loads.
+//  * Two issue forms of the same arithmetic: scalar fma.rn.f32 (the
+//    default) or packed fma.rn.f32x2, each lane of which is an ordinary
+//    round-to-nearest fp32 FMA, so every accumulator sees exactly the same
+//    sequence of roundings either way and the two give bit-identical C.
+//    Measured on GB300 the packed form is slower: it holds the FMA pipe two
+//    cycles, so it saves issue slots but not pipe time, and the broadcast
+//    operand pairs push the kernel past its 128-register budget.
 //  * The 8 x 8 block is split into four 4 x 4 quadrants 64 rows / 64 columns
 //    apart, so one 128-bit shared load serves 4 rows (or columns) and the
 //    loads of a warp are conflict-free: a warp reads 4 distinct 16-byte A
