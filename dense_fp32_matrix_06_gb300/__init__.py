@@ -45,7 +45,9 @@ EXPORTED_SYMBOLS = (
     "sgemm_status_string",
     "sgemm_last_cuda_error",
     "sgemm_ffma_probe",
+    "sgemm_noalloc",
 )
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
 class SgemmError(RuntimeError):
@@ -129,6 +131,8 @@ def load_library() -> ctypes.CDLL:
         lib.sgemm_last_cuda_error.restype = ctypes.c_int
         lib.sgemm_ffma_probe.argtypes = [_i64, _i64, ctypes.c_int32, _vp, _vp]
         lib.sgemm_ffma_probe.restype = ctypes.c_int
+        lib.sgemm_noalloc.argtypes = lib.sgemm.argtypes
+        lib.sgemm_noalloc.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -175,6 +179,17 @@ def sgemm_ptr(M: int, N: int, K: int, alpha: float, A: int, lda: int, B: int, ld
     """sgemm() on raw device addresses; `stream` is a cudaStream_t value."""
     _check(load_library().sgemm(M, N, K, alpha, A or None, lda, B or None, ldb, beta,
                                 C or None, ldc, stream or None), "sgemm")
+
+
+def sgemm_noalloc_ptr(M: int, N: int, K: int, alpha: float, A: int, lda: int, B: int, ldb: int,
+                      beta: float, C: int, ldc: int, stream: int = 0) -> None:
+    """sgemm_noalloc(): the same GEMM as sgemm_ptr without allocating device
+    memory (split-K scratch comes from a fixed 64 MiB buffer inside the
+    library).  For callers that may not allocate, e.g. inside a framework that
+    owns all device memory.  Calls that overlap on the GPU share that buffer
+    and race; keep them ordered."""
+    _check(load_library().sgemm_noalloc(M, N, K, alpha, A or None, lda, B or None, ldb, beta,
+                                        C or None, ldc, stream or None), "sgemm_noalloc")
 
 
 def sgemm_with_plan_ptr(plan: GemmPlan, M: int, N: int, K: int, alpha: float, A: int, lda: int,

@@ -358,3 +358,65 @@ sgemm_status sgemm_ffma_probe(int64_t ctas, int64_t iters, int32_t packed, float
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// sgemm_noalloc: the same GEMM with its split-K scratch in a fixed buffer that
+// lives inside the library, so the call never allocates device memory.
+// ---------------------------------------------------------------------------
+
+// The scratch buffer: tile counters followed by partial tiles, exactly the
+// layout of a split-K workspace.  Every GPU that loads the library holds it
+// until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SGEMM_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+std::vector<void *> g_noalloc_addr;  // device address of the buffer, per device
+
+// Host code cannot use the array's name as a device pointer (on the host it is
+// only a stand-in for the symbol), so the device address is looked up once per
+// device, with that device current, and cached.
+sgemm_status noalloc_scratch(int dev, void **out) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (int(g_noalloc_addr.size()) <= dev) g_noalloc_addr.resize(dev + 1, nullptr);
+    if (!g_noalloc_addr[dev]) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr) return cuda_fail(e, SGEMM_ERR_LAUNCH);
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return SGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" sgemm_status sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
+                                      const float *A, int64_t lda, const float *B, int64_t ldb,
+                                      float beta, float *C, int64_t ldc, void *stream) {
+    sgemm_status s = check_sizes(M, N, K, lda, ldb, ldc);
+    if (s != SGEMM_OK) return s;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    if (!C) return SGEMM_ERR_INVALID_ARG;
+    if (K > 0 && alpha != 0.0f && (!A || !B)) return SGEMM_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    s = current_device(&dev, &sms);
+    if (s != SGEMM_OK) return s;
+    gemm_plan_t plan;
+    s = plan_impl(M, N, K, lda, ldb, ldc, A, B, C, sms, &plan);
+    if (s != SGEMM_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void *ws = nullptr;
+    if (plan.workspace_bytes > 0 && K > 0 && alpha != 0.0f) {
+        if (plan.workspace_bytes > size_t(SGEMM_NOALLOC_SCRATCH_BYTES)) return SGEMM_ERR_WORKSPACE;
+        s = noalloc_scratch(dev, &ws);
+        if (s != SGEMM_OK) return s;
+        // The buffer keeps whatever the previous call left; the tile counters
+        // must start at zero, so clear the ones this launch uses.
+        const size_t counter_bytes = size_t(plan.tiles_m * plan.tiles_n) * sizeof(unsigned);
+        const cudaError_t e = cudaMemsetAsync(ws, 0, counter_bytes, st);
+        if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
+    }
+    return run(plan, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, ws, st);
+}

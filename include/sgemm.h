@@ -143,6 +143,44 @@ sgemm_status sgemm_with_plan(const gemm_plan_t *plan, int64_t M, int64_t N, int6
                              int64_t ldc, void *workspace, size_t workspace_bytes,
                              void *stream);
 
+/* Capacity of the fixed scratch buffer sgemm_noalloc uses: 64 MiB per device. */
+#define SGEMM_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * sgemm_noalloc -- the same C = alpha*A*B + beta*C as sgemm, same arguments,
+ * same plan, same kernels and bit-identical results, for callers that must
+ * not allocate device memory.  The pages have no counterpart to this call.
+ *
+ * Who needs it: code that runs where a cudaMalloc is not allowed or not
+ * safe -- an application or framework that reserved the device memory up
+ * front and forbids its plugins from allocating (a library cudaMalloc would
+ * then fail or fragment its pool), latency-critical loops that must not
+ * allocate after start-up (cudaMalloc may synchronise the device and stall
+ * other streams), and callers that have no device-memory budget to give.
+ * sgemm may allocate its split-K workspace on first use per stream;
+ * sgemm_noalloc takes that scratch from a fixed buffer compiled into the
+ * library instead (SGEMM_NOALLOC_SCRATCH_BYTES per device, held by every
+ * GPU that loads the library until the process exits).
+ *
+ * It calls no cudaMalloc, cudaFree or other allocating routine.  The first
+ * call on each device looks up the buffer's device address (with that device
+ * current) and caches it; make that first call before any stream capture.
+ * Each call clears the tile counters it uses with cudaMemsetAsync on
+ * `stream`, then launches the GEMM.
+ *
+ * All calls on a device share the one buffer: calls that overlap on the GPU
+ * (different streams without ordering between them) race and give wrong
+ * results.  Order them on one stream, or with events.
+ *
+ * Returns SGEMM_ERR_WORKSPACE, with nothing launched, when the shape's plan
+ * needs more split-K scratch than SGEMM_NOALLOC_SCRATCH_BYTES (every plan
+ * gemm_plan makes for the GB300 workloads fits; forcing a large split can
+ * exceed it); otherwise the statuses of sgemm.
+ */
+sgemm_status sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
+                           const float *A, int64_t lda, const float *B, int64_t ldb,
+                           float beta, float *C, int64_t ldc, void *stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char *sgemm_status_string(sgemm_status status);
 
