@@ -46,6 +46,9 @@ EXPORTED_SYMBOLS = (
     "sgemm_last_cuda_error",
     "sgemm_ffma_probe",
     "sgemm_noalloc",
+    "sgemm_tf32x3",
+    "sgemm_device_status",
+    "sgemm_tf32x3_stall_selftest",
 )
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
@@ -133,6 +136,13 @@ def load_library() -> ctypes.CDLL:
         lib.sgemm_ffma_probe.restype = ctypes.c_int
         lib.sgemm_noalloc.argtypes = lib.sgemm.argtypes
         lib.sgemm_noalloc.restype = ctypes.c_int
+        lib.sgemm_tf32x3.argtypes = lib.sgemm.argtypes
+        lib.sgemm_tf32x3.restype = ctypes.c_int
+        lib.sgemm_device_status.argtypes = [_vp]
+        lib.sgemm_device_status.restype = ctypes.c_int
+        lib.sgemm_tf32x3_stall_selftest.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp,
+                                                    _i64, _i64, _vp]
+        lib.sgemm_tf32x3_stall_selftest.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -190,6 +200,28 @@ def sgemm_noalloc_ptr(M: int, N: int, K: int, alpha: float, A: int, lda: int, B:
     and race; keep them ordered."""
     _check(load_library().sgemm_noalloc(M, N, K, alpha, A or None, lda, B or None, ldb, beta,
                                         C or None, ldc, stream or None), "sgemm_noalloc")
+
+
+def sgemm_tf32x3_ptr(M: int, N: int, K: int, alpha: float, A: int, lda: int, B: int, ldb: int,
+                     beta: float, C: int, ldc: int, stream: int = 0) -> None:
+    """sgemm_tf32x3(): the 3xTF32 tensor-core mode (normalised error <= 1e-5)."""
+    _check(load_library().sgemm_tf32x3(M, N, K, alpha, A or None, lda, B or None, ldb, beta,
+                                       C or None, ldc, stream or None), "sgemm_tf32x3")
+
+
+def device_status(stream: int = 0) -> int:
+    """sgemm_device_status(): 0, or 5 (SGEMM_ERR_TIMEOUT) if a bounded
+    device-side wait expired since the last call.  Synchronises `stream`."""
+    return int(load_library().sgemm_device_status(stream or None))
+
+
+def tf32x3_stall_selftest(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, C: int,
+                          ldc: int, limit_us: int, stream: int = 0) -> int:
+    """sgemm_tf32x3_stall_selftest(): returns the status code (5 when the
+    bounded waits expired as intended)."""
+    return int(load_library().sgemm_tf32x3_stall_selftest(M, N, K, A or None, lda, B or None,
+                                                           ldb, C or None, ldc, limit_us,
+                                                           stream or None))
 
 
 def sgemm_with_plan_ptr(plan: GemmPlan, M: int, N: int, K: int, alpha: float, A: int, lda: int,
@@ -272,6 +304,28 @@ def sgemm(A, B, C=None, alpha: float = 1.0, beta: float = 0.0, stream=None):
     with torch.cuda.device(A.device):
         sgemm_ptr(M, N, K, float(alpha), a_ptr, lda, b_ptr, ldb, float(beta), c_ptr, ldc,
                   _stream_handle(stream))
+    return C
+
+
+def sgemm_tf32x3(A, B, C=None, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """The 3xTF32 tensor-core mode on torch tensors (same rules as sgemm())."""
+    import torch
+    if A.dim() != 2 or B.dim() != 2:
+        raise ValueError("sgemm_tf32x3 works on 2-D matrices only")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: A is {tuple(A.shape)}, B is {tuple(B.shape)}")
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs an input C")
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    a_ptr, lda = _row_major_view(A, "A")
+    b_ptr, ldb = _row_major_view(B, "B")
+    c_ptr, ldc = _row_major_view(C, "C")
+    with torch.cuda.device(A.device):
+        sgemm_tf32x3_ptr(M, N, K, float(alpha), a_ptr, max(lda, K, 1), b_ptr, max(ldb, N, 1),
+                         float(beta), c_ptr, max(ldc, N, 1), _stream_handle(stream))
     return C
 
 

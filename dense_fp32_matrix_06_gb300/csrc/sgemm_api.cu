@@ -420,3 +420,65 @@ extern "C" sgemm_status sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alp
     }
     return run(plan, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, ws, st);
 }
+
+// ---------------------------------------------------------------------------
+// 3xTF32 tensor-core mode
+// ---------------------------------------------------------------------------
+
+namespace {
+
+sgemm_status tf32x3_run(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                        int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                        int64_t ldc, uint64_t limit_ns, int inject_stall, void *stream) {
+    sgemm_status s = check_sizes(M, N, K, lda, ldb, ldc);
+    if (s != SGEMM_OK) return s;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    if (!C) return SGEMM_ERR_INVALID_ARG;
+    if (K > 0 && alpha != 0.0f && (!A || !B)) return SGEMM_ERR_INVALID_ARG;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return SGEMM_ERR_INVALID_ARG;
+    int dev = 0;
+    s = current_device(&dev, nullptr);
+    if (s != SGEMM_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (K == 0 || alpha == 0.0f) {
+        e = launch_scale(C, M, N, ldc, beta, st);
+        return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
+    }
+    void *ws = nullptr;
+    s = library_workspace(dev, st, tf32x3_workspace_bytes(M, N, K), &ws);
+    if (s != SGEMM_OK) return s;
+    e = launch_tf32x3(A, lda, B, ldb, C, ldc, M, N, K, alpha, beta, ws, limit_ns, inject_stall,
+                      st);
+    return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
+}
+
+}  // namespace
+
+extern "C" sgemm_status sgemm_tf32x3(int64_t M, int64_t N, int64_t K, float alpha,
+                                     const float *A, int64_t lda, const float *B, int64_t ldb,
+                                     float beta, float *C, int64_t ldc, void *stream) {
+    return tf32x3_run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, kWaitLimitNs, 0, stream);
+}
+
+extern "C" sgemm_status sgemm_device_status(void *stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_UNSUPPORTED_DEVICE;
+    unsigned word = 0;
+    const cudaError_t e = tf32x3_read_error(&word, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
+    return word ? SGEMM_ERR_TIMEOUT : SGEMM_OK;
+}
+
+extern "C" sgemm_status sgemm_tf32x3_stall_selftest(int64_t M, int64_t N, int64_t K,
+                                                    const float *A, int64_t lda, const float *B,
+                                                    int64_t ldb, float *C, int64_t ldc,
+                                                    int64_t limit_us, void *stream) {
+    if (limit_us <= 0 || limit_us > 1000000 || K <= 0) return SGEMM_ERR_INVALID_ARG;
+    sgemm_status s = sgemm_device_status(stream);   // start from a clear record
+    if (s != SGEMM_OK && s != SGEMM_ERR_TIMEOUT) return s;
+    s = tf32x3_run(M, N, K, 1.0f, A, lda, B, ldb, 0.0f, C, ldc, uint64_t(limit_us) * 1000ull, 1,
+                   stream);
+    if (s != SGEMM_OK) return s;
+    return sgemm_device_status(stream);
+}

@@ -1,0 +1,531 @@
+// tf32x3_gemm.cu -- the separately reported tensor-core mode: fp32 GEMM from
+// three TF32 tensor-core products (split precision), on sm_103a tcgen05.
+//
+// C = alpha * A * B + beta * C with A = A_hi + A_lo, B = B_hi + B_lo, where
+// x_hi is x rounded to TF32 (10 explicit mantissa bits, round to nearest
+// even) and x_lo = x - x_hi (exact in fp32) rounded to TF32 as well.  Then
+//     A*B ~= A_lo*B_hi + A_hi*B_lo + A_hi*B_hi
+// (the dropped A_lo*B_lo term is ~2^-22 of |A||B|), each product on the
+// tensor cores with fp32 accumulation in tensor memory.  The pages have no
+// tensor-core path; the computation is the same dense contraction as the
+// FFMA kernel, so the tensor cores are its natural home on this chip.
+//
+// Pipeline:
+//  1. split kernels: A (M x K) -> A_hi, A_lo (M x Kp, K-major);
+//     B (K x N) -> B_hi^T, B_lo^T (N x Kp, K-major, transposed through smem
+//     tiles), Kp = K rounded up to 4 so TMA row strides are 16-byte multiples.
+//  2. mma kernel, one 128 x BN output tile per CTA, 128 threads:
+//     warp 0 lane 0 issues TMA loads (128-byte swizzled boxes of 32 fp32 of K)
+//     of the four operand tiles into a STAGES-deep smem ring; warp 1 owns the
+//     tensor-memory allocation and lane 0 issues tcgen05.mma.kind::tf32
+//     (M=128, N=BN, K=8) three times per 8-wide K step, committing each stage
+//     back to its producer barrier; then all four warps read the accumulator
+//     out of TMEM (tcgen05.ld 32x32b) and apply alpha/beta.
+//  Every mbarrier wait is bounded by a time limit; on expiry the thread sets
+//  the device error word, the epilogue stores nothing, in-flight copies are
+//  waited for (bounded) and the TMEM is freed before the CTA exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "sgemm_internal.h"
+
+namespace sgemm_impl {
+
+// Device error word of the tensor-core mode (bit 0: a bounded wait expired).
+static __device__ unsigned g_tc_error;
+
+namespace {
+
+constexpr int kTcBM = 128;
+constexpr int kTcBK = 32;            // fp32 elements per 128-byte swizzle row
+constexpr int kTcThreads = 128;
+
+// ---------------------------------------------------------------------------
+// split into TF32 hi/lo parts
+// ---------------------------------------------------------------------------
+
+// Nearest TF32 value (ties to even) of a finite fp32 x; inf/NaN pass through.
+__device__ __forceinline__ float tf32_round(float x) {
+    uint32_t u = __float_as_uint(x);
+    if ((u & 0x7f800000u) == 0x7f800000u) return x;
+    const uint32_t r = (u + 0x00000fffu + ((u >> 13) & 1u)) & 0xffffe000u;
+    if ((r & 0x7f800000u) == 0x7f800000u) return __uint_as_float(u & 0xffffe000u);
+    return __uint_as_float(r);
+}
+
+__device__ __forceinline__ void split2(float x, float &hi, float &lo) {
+    hi = tf32_round(x);
+    lo = tf32_round(x - hi);
+}
+
+// X (rows x cols, row stride ldx) -> hi, lo (rows x cols, row stride ldo).
+__global__ void split_rows_kernel(const float *__restrict__ X, int64_t rows, int64_t cols,
+                                  int64_t ldx, float *__restrict__ hi, float *__restrict__ lo,
+                                  int64_t ldo) {
+    const int64_t total = rows * cols;
+    for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+         e += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t r = e / cols, c = e - r * cols;
+        float h, l;
+        split2(X[r * ldx + c], h, l);
+        hi[r * ldo + c] = h;
+        lo[r * ldo + c] = l;
+    }
+}
+
+// B (K x N, row stride ldb) -> hiT, loT (N x K, row stride ldo): 32 x 32 tiles
+// through padded smem so both the reads and the writes are coalesced.
+__global__ void split_transpose_kernel(const float *__restrict__ B, int64_t K, int64_t N,
+                                       int64_t ldb, float *__restrict__ hiT,
+                                       float *__restrict__ loT, int64_t ldo) {
+    __shared__ float th[32][33];
+    __shared__ float tl[32][33];
+    const int64_t k0 = int64_t(blockIdx.y) * 32, n0 = int64_t(blockIdx.x) * 32;
+    const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8
+    for (int i = ty; i < 32; i += 8) {
+        const int64_t k = k0 + i, n = n0 + tx;
+        float h = 0.0f, l = 0.0f;
+        if (k < K && n < N) split2(B[k * ldb + n], h, l);
+        th[i][tx] = h;
+        tl[i][tx] = l;
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+        const int64_t n = n0 + i, k = k0 + tx;
+        if (n < N && k < K) {
+            hiT[n * ldo + k] = th[tx][i];
+            loT[n * ldo + k] = tl[tx][i];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers (mbarrier, TMA, tcgen05)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait until the phase of parity `parity` of `bar` has completed, for at most
+// `limit_ns`.  On expiry set the error word and return false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > limit_ns) {
+            atomicOr(&g_tc_error, 1u);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t c0,
+                                            int32_t c1, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes in 8-row (1024-byte) swizzle atoms laid out back to back.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+    uint64_t d = 0;
+    d |= uint64_t((addr & 0x3FFFFu) >> 4);       // start address
+    d |= uint64_t(16 >> 4) << 16;                // leading byte offset (unused here)
+    d |= uint64_t(1024 >> 4) << 32;              // stride byte offset: next 8-row group
+    d |= uint64_t(1) << 46;                      // descriptor version
+    d |= uint64_t(2) << 61;                      // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: D fp32, A and B tf32, both K-major, M = 128, N = bn.
+__host__ __device__ constexpr uint32_t tf32_idesc(int bn) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | (uint32_t(bn >> 3) << 17) |
+           (uint32_t(kTcBM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+        "[%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+struct TcArgs {
+    float *C;
+    int64_t M, N, K, ldc;
+    float alpha, beta;
+    int32_t tiles_m, tiles_n;
+    uint64_t limit_ns;     // bound on every mbarrier wait
+    int32_t inject_stall;  // 1: the producer issues nothing (exercises the bounded waits)
+};
+
+template <int BN, int STAGES>
+struct TcSmem {
+    static constexpr int kABytes = kTcBM * kTcBK * 4;          // 16 KiB
+    static constexpr int kBBytes = BN * kTcBK * 4;
+    static constexpr int kStageBytes = 2 * kABytes + 2 * kBBytes;
+    static constexpr int kBarOffset = STAGES * kStageBytes;
+    // full[STAGES], empty[STAGES], done, then the TMEM address slot
+    static constexpr int kBytes = kBarOffset + (2 * STAGES + 1) * 8 + 8;
+    static constexpr int kDynBytes = kBytes + 1024;            // room to align to 1024
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kTcThreads, 1)
+tf32x3_mma_kernel(const __grid_constant__ CUtensorMap map_a_hi,
+                  const __grid_constant__ CUtensorMap map_a_lo,
+                  const __grid_constant__ CUtensorMap map_b_hi,
+                  const __grid_constant__ CUtensorMap map_b_lo, const TcArgs p) {
+    using L = TcSmem<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const uint32_t bar0 = base + L::kBarOffset;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    const uint32_t done_bar = bar0 + 8u * (2 * STAGES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + L::kBarOffset + (2 * STAGES + 1) * 8);
+    auto a_hi = [&](int s) { return base + s * L::kStageBytes; };
+    auto a_lo = [&](int s) { return base + s * L::kStageBytes + L::kABytes; };
+    auto b_hi = [&](int s) { return base + s * L::kStageBytes + 2 * L::kABytes; };
+    auto b_lo = [&](int s) { return base + s * L::kStageBytes + 2 * L::kABytes + L::kBBytes; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    __shared__ int s_mma_ok;
+
+    // grouped raster over 8 tile rows
+    const int pid = blockIdx.x;
+    const int per_group = 8 * p.tiles_n;
+    const int group = pid / per_group;
+    const int first_m = group * 8;
+    const int gm = min(p.tiles_m - first_m, 8);
+    const int in_group = pid - group * per_group;
+    const int tile_m = first_m + in_group % gm;
+    const int tile_n = in_group / gm;
+    const int m0 = tile_m * kTcBM;
+    const int n0 = tile_n * BN;
+    const int nkb = int((p.K + kTcBK - 1) / kTcBK);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(done_bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(uint32_t(BN))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    int issued = 0;   // k-blocks the producer issued (thread 0 only)
+    if (warp == 0 && lane == 0) {
+        // ---- TMA producer ----
+        if (!p.inject_stall) {
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % STAGES;
+                const uint32_t use = uint32_t(kb / STAGES);
+                if (kb >= STAGES && !mbar_wait(empty_bar(s), (use & 1u) ^ 1u, p.limit_ns)) break;
+                mbar_expect_tx(full_bar(s), uint32_t(L::kStageBytes));
+                const int kc = kb * kTcBK;
+                tma_load_2d(a_hi(s), &map_a_hi, kc, m0, full_bar(s));
+                tma_load_2d(a_lo(s), &map_a_lo, kc, m0, full_bar(s));
+                tma_load_2d(b_hi(s), &map_b_hi, kc, n0, full_bar(s));
+                tma_load_2d(b_lo(s), &map_b_lo, kc, n0, full_bar(s));
+                issued = kb + 1;
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer ----
+        constexpr uint32_t idesc = tf32_idesc(BN);
+        bool ok = true;
+        for (int kb = 0; kb < nkb && ok; ++kb) {
+            const int s = kb % STAGES;
+            const uint32_t use = uint32_t(kb / STAGES);
+            if (!mbar_wait(full_bar(s), use & 1u, p.limit_ns)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kTcBK / 8; ++kk) {
+                const uint32_t koff = uint32_t(kk) * 32u;   // 8 fp32 = 32 bytes along K
+                const uint64_t ah = sw128_desc(a_hi(s) + koff), al = sw128_desc(a_lo(s) + koff);
+                const uint64_t bh = sw128_desc(b_hi(s) + koff), bl = sw128_desc(b_lo(s) + koff);
+                mma_tf32(tmem, al, bh, idesc, (kb | kk) != 0 ? 1u : 0u);
+                mma_tf32(tmem, ah, bl, idesc, 1u);
+                mma_tf32(tmem, ah, bh, idesc, 1u);
+            }
+            mma_commit(empty_bar(s));   // stage s is free once these MMAs finish
+        }
+        s_mma_ok = ok ? 1 : 0;
+        // arrives once every MMA issued above has finished (at once if none were)
+        mma_commit(done_bar);
+    }
+    __syncwarp();
+    __syncthreads();   // both roles have finished issuing; s_mma_ok is visible
+
+    // ---- epilogue: TMEM -> registers -> C ----
+    const bool have = mbar_wait(done_bar, 0u, p.limit_ns);
+    tc_fence_after();
+    const bool clean = have && s_mma_ok != 0;
+    if (__all_sync(0xffffffffu, clean)) {
+        const int64_t row = int64_t(m0) + warp * 32 + lane;
+        const bool row_ok = row < p.M;
+        float *crow = p.C + (row_ok ? row : 0) * p.ldc;
+        const bool vec = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0) && (p.ldc % 4 == 0);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+            float v[32];
+            tmem_ld32(tmem + (uint32_t(warp * 32) << 16) + uint32_t(c0), v);
+            if (!row_ok) continue;
+            const int64_t col = int64_t(n0) + c0;
+            if (vec && col + 32 <= p.N) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    float4 o = make_float4(p.alpha * v[4 * q], p.alpha * v[4 * q + 1],
+                                           p.alpha * v[4 * q + 2], p.alpha * v[4 * q + 3]);
+                    float4 *dst = reinterpret_cast<float4 *>(crow + col + 4 * q);
+                    if (p.beta != 0.0f) {
+                        const float4 old = *dst;
+                        o.x = fmaf(p.beta, old.x, o.x);
+                        o.y = fmaf(p.beta, old.y, o.y);
+                        o.z = fmaf(p.beta, old.z, o.z);
+                        o.w = fmaf(p.beta, old.w, o.w);
+                    }
+                    *dst = o;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    if (col + j < p.N) {
+                        float o = p.alpha * v[j];
+                        if (p.beta != 0.0f) o = fmaf(p.beta, crow[col + j], o);
+                        crow[col + j] = o;
+                    }
+                }
+            }
+        }
+    }
+
+    // ---- teardown ----
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0 && lane == 0) {
+        // copies still in flight (only after an expired wait) land before exit
+        for (int kb = (issued > STAGES ? issued - STAGES : 0); kb < issued; ++kb)
+            mbar_wait(full_bar(kb % STAGES), uint32_t(kb / STAGES) & 1u, p.limit_ns);
+    }
+    if (warp == 1 && lane == 0 && !have) mbar_wait(done_bar, 0u, p.limit_ns);
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(uint32_t(BN))
+                     : "memory");
+    }
+}
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link-time
+// dependency on the driver library).
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+// 2-D fp32 tensor map over a K-major (rows x cols, row stride ld floats)
+// matrix, box = 32 columns x box_rows rows, 128-byte swizzle, zero fill.
+bool encode_kmajor(CUtensorMap *map, const float *ptr, int64_t rows, int64_t cols, int64_t ld,
+                   int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(ld) * 4};
+    const cuuint32_t box[2] = {cuuint32_t(kTcBK), cuuint32_t(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(ptr), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_mma(const CUtensorMap &ah, const CUtensorMap &al, const CUtensorMap &bh,
+                       const CUtensorMap &bl, const TcArgs &a, cudaStream_t stream) {
+    using L = TcSmem<BN, STAGES>;
+    // the attribute is per device; set it on every call (cheap, host-side)
+    cudaError_t e = cudaFuncSetAttribute(tf32x3_mma_kernel<BN, STAGES>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynBytes);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = unsigned(int64_t(a.tiles_m) * a.tiles_n);
+    tf32x3_mma_kernel<BN, STAGES><<<grid, kTcThreads, L::kDynBytes, stream>>>(ah, al, bh, bl, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    const int64_t kp = (K + 3) / 4 * 4;
+    const size_t a = (size_t(M) * kp * 4 + 255) / 256 * 256;
+    const size_t b = (size_t(N) * kp * 4 + 255) / 256 * 256;
+    return 2 * a + 2 * b;
+}
+
+cudaError_t launch_tf32x3(const float *A, int64_t lda, const float *B, int64_t ldb, float *C,
+                          int64_t ldc, int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                          void *workspace, uint64_t limit_ns, int inject_stall,
+                          cudaStream_t stream) {
+    constexpr int BN = 256, STAGES = 2;
+    const int64_t kp = (K + 3) / 4 * 4;
+    const size_t abytes = (size_t(M) * kp * 4 + 255) / 256 * 256;
+    const size_t bbytes = (size_t(N) * kp * 4 + 255) / 256 * 256;
+    char *w = static_cast<char *>(workspace);
+    float *a_hi = reinterpret_cast<float *>(w);
+    float *a_lo = reinterpret_cast<float *>(w + abytes);
+    float *b_hi = reinterpret_cast<float *>(w + 2 * abytes);
+    float *b_lo = reinterpret_cast<float *>(w + 2 * abytes + bbytes);
+
+    int64_t blocks = (M * K + 255) / 256;
+    if (blocks > 8192) blocks = 8192;
+    split_rows_kernel<<<unsigned(blocks), 256, 0, stream>>>(A, M, K, lda, a_hi, a_lo, kp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const dim3 tgrid(unsigned((N + 31) / 32), unsigned((K + 31) / 32));
+    split_transpose_kernel<<<tgrid, dim3(32, 8), 0, stream>>>(B, K, N, ldb, b_hi, b_lo, kp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    CUtensorMap ah, al, bh, bl;
+    if (!encode_kmajor(&ah, a_hi, M, K, kp, kTcBM) || !encode_kmajor(&al, a_lo, M, K, kp, kTcBM) ||
+        !encode_kmajor(&bh, b_hi, N, K, kp, BN) || !encode_kmajor(&bl, b_lo, N, K, kp, BN))
+        return cudaErrorInvalidValue;
+    TcArgs a;
+    a.C = C;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.ldc = ldc;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.tiles_m = int32_t((M + kTcBM - 1) / kTcBM);
+    a.tiles_n = int32_t((N + BN - 1) / BN);
+    a.limit_ns = limit_ns;
+    a.inject_stall = inject_stall;
+    return launch_mma<BN, STAGES>(ah, al, bh, bl, a, stream);
+}
+
+cudaError_t tf32x3_read_error(unsigned *out, cudaStream_t stream) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_tc_error, sizeof(unsigned), 0,
+                                              cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_tc_error, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice,
+                                stream);
+    if (e != cudaSuccess) return e;
+    return cudaStreamSynchronize(stream);
+}
+
+}  // namespace sgemm_impl

@@ -64,7 +64,8 @@ typedef enum {
 
 /* Arithmetic mode of a plan. */
 typedef enum {
-    SGEMM_MODE_FFMA = 0     /* fp32 CUDA-core FMA (the default product path) */
+    SGEMM_MODE_FFMA = 0,    /* fp32 CUDA-core FMA (the default product path) */
+    SGEMM_MODE_TF32X3 = 1   /* 3xTF32 split precision on the tensor cores (sgemm_tf32x3) */
 } sgemm_mode;
 
 /* Size of the tile-counter block at the start of a split-K workspace. */
@@ -180,6 +181,48 @@ sgemm_status sgemm_with_plan(const gemm_plan_t *plan, int64_t M, int64_t N, int6
 sgemm_status sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
                            const float *A, int64_t lda, const float *B, int64_t ldb,
                            float beta, float *C, int64_t ldc, void *stream);
+
+/*
+ * sgemm_tf32x3 -- the separately reported tensor-core mode of the same
+ * product, C = alpha*A*B + beta*C, with the arguments and conventions of
+ * sgemm.  The pages compute this product on CUDA cores only; this mode
+ * computes it as a dense contraction on the sm_103a tensor cores:
+ * A = A_hi + A_lo and B = B_hi + B_lo, x_hi = x rounded to TF32 (round to
+ * nearest even), x_lo = x - x_hi rounded to TF32, and
+ * C ~= alpha*(A_lo*B_hi + A_hi*B_lo + A_hi*B_hi) + beta*C with fp32
+ * accumulation in tensor memory (tcgen05.mma kind::tf32, TMA-fed).
+ * Accuracy: max|C - exact| / (K*max|A|*max|B| + |beta|*max|C0|) <= 1e-5;
+ * exact on integer inputs whose partial sums stay below 2^24 (their lo
+ * parts are zero).  Any alignment and leading dimension are accepted: a
+ * pre-pass copies A and B into K-major hi/lo arrays in a library-owned
+ * workspace of 8*(M+N)*ceil(K/4)*4 bytes per (device, stream), grown with
+ * stream-ordered allocation.  M, N, K must be below 2^31.  Every device-side
+ * wait gives up after 1 s: the kernel then stores nothing to C and records
+ * the event, which sgemm_device_status reports.
+ */
+sgemm_status sgemm_tf32x3(int64_t M, int64_t N, int64_t K, float alpha,
+                          const float *A, int64_t lda, const float *B, int64_t ldb,
+                          float beta, float *C, int64_t ldc, void *stream);
+
+/*
+ * sgemm_device_status -- synchronises `stream`, then reports (and clears)
+ * the record of expired device-side waits of the tensor-core mode:
+ * SGEMM_ERR_TIMEOUT if any wait gave up since the last call, else SGEMM_OK
+ * (SGEMM_ERR_LAUNCH if a CUDA call failed).
+ */
+sgemm_status sgemm_device_status(void *stream);
+
+/*
+ * sgemm_tf32x3_stall_selftest -- diagnostic of the bounded waits: runs the
+ * tensor-core kernel on the given buffers with its operand loads withheld,
+ * so every wait expires after `limit_us` microseconds (1..1e6), and returns
+ * sgemm_device_status: SGEMM_ERR_TIMEOUT when the bounds work.  C is not
+ * written.  Nothing faults or hangs; the context stays usable.
+ */
+sgemm_status sgemm_tf32x3_stall_selftest(int64_t M, int64_t N, int64_t K,
+                                         const float *A, int64_t lda, const float *B,
+                                         int64_t ldb, float *C, int64_t ldc,
+                                         int64_t limit_us, void *stream);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char *sgemm_status_string(sgemm_status status);
