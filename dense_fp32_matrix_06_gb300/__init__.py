@@ -78,12 +78,14 @@ class GemmPlan(ctypes.Structure):
         ("split_k", ctypes.c_int32),
         ("vec", ctypes.c_int32),
         ("edge", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("tail_split", ctypes.c_int32),
         ("k_per_split", ctypes.c_int64),
         ("tiles_m", ctypes.c_int64),
         ("tiles_n", ctypes.c_int64),
         ("grid_ctas", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_size_t),
+        ("tail_start", ctypes.c_int64),
+        ("tail_k_per_split", ctypes.c_int64),
     ]
 
     def as_dict(self) -> dict:

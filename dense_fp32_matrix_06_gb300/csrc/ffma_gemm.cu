@@ -40,10 +40,13 @@
 //  * Epilogue: c = alpha * acc, then c = fma(beta, C_old, c) only when
 //    beta != 0 (C is not read otherwise), stored with 128-bit stores.
 //  * Split-K: when the tile grid cannot fill the GPU, K is cut into split_k
-//    ranges.  Every CTA writes its partial tile to the workspace, the last
-//    CTA of a tile to arrive (atomic ticket, no waiting) sums the partials in
-//    ascending split order and runs the epilogue, then rearms the counter.
-//    The sum order is fixed, so results are deterministic run to run.
+//    ranges; when only the last wave of tiles is partly empty, just those
+//    tail tiles are cut (tail_split ranges), so the last wave finishes in a
+//    fraction of a full tile's time.  Every CTA of a split tile writes its
+//    partial tile to the workspace, the last CTA of the tile to arrive
+//    (atomic ticket, no waiting) sums the partials in ascending split order
+//    and runs the epilogue, then rearms the counter.  The sum order is fixed,
+//    so results are deterministic run to run.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -92,6 +95,43 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // 4 k-groups -- over all 32 banks.
 __device__ __forceinline__ int a_col(int k, int m) { return m ^ (((k >> 2) & 3) << 3); }
 
+// The (tile, K range) pair CTA `pid` computes, and the tile's coordinates.
+struct WorkItem {
+    int64_t tile;
+    int64_t row0, col0;
+    int64_t kbeg, kend;
+    int split, nsplit;
+};
+
+__device__ __forceinline__ WorkItem work_item(const GemmArgs &p, int64_t pid) {
+    WorkItem w;
+    const int64_t lead = p.tail_start * p.split_k;
+    int64_t kps;
+    if (pid < lead) {
+        w.tile = pid / p.split_k;
+        w.split = int(pid - w.tile * p.split_k);
+        w.nsplit = p.split_k;
+        kps = p.k_per_split;
+    } else {
+        const int64_t j = pid - lead;
+        w.tile = p.tail_start + j / p.tail_split;
+        w.split = int(j % p.tail_split);
+        w.nsplit = p.tail_split;
+        kps = p.tail_k_per_split;
+    }
+    // grouped raster over kGroupM tile rows (L2 reuse of A and B panels)
+    const int64_t per_group = int64_t(kGroupM) * p.tiles_n;
+    const int64_t group = w.tile / per_group;
+    const int64_t first_m = group * kGroupM;
+    const int64_t gm = min(int64_t(p.tiles_m) - first_m, int64_t(kGroupM));
+    const int64_t in_group = w.tile - group * per_group;
+    w.row0 = (first_m + in_group % gm) * kBM;
+    w.col0 = (in_group / gm) * kBN;
+    w.kbeg = int64_t(w.split) * kps;
+    w.kend = min(p.K, w.kbeg + kps);
+    return w;
+}
+
 template <bool kPacked, bool kVec, bool kEdge, bool kSplit>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 ffma_gemm_kernel(const GemmArgs p) {
@@ -103,22 +143,16 @@ ffma_gemm_kernel(const GemmArgs p) {
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
-    // ---- tile coordinates: grouped raster over kGroupM tile rows ----
-    const int pid = blockIdx.x;
-    const int tiles_n = p.tiles_n;
-    const int per_group = kGroupM * tiles_n;
-    const int group = pid / per_group;
-    const int first_m = group * kGroupM;
-    const int gm = min(p.tiles_m - first_m, kGroupM);
-    const int in_group = pid - group * per_group;
-    const int tile_m = first_m + in_group % gm;
-    const int tile_n = in_group / gm;
-    const int64_t row0 = int64_t(tile_m) * kBM;
-    const int64_t col0 = int64_t(tile_n) * kBN;
-
-    const int split = blockIdx.y;
-    const int64_t kbeg = int64_t(split) * p.k_per_split;
-    const int64_t kend = min(p.K, kbeg + p.k_per_split);
+    // ---- (tile, K range) of this CTA; recomputed after the main loop so
+    // none of it stays live in registers across it ----
+    int64_t row0, col0, kbeg, kend;
+    {
+        const WorkItem w = work_item(p, blockIdx.x);
+        row0 = w.row0;
+        col0 = w.col0;
+        kbeg = w.kbeg;
+        kend = w.kend;
+    }
     const int nslices = kend > kbeg ? int((kend - kbeg + kBK - 1) / kBK) : 0;
 
     // ---- compute mapping: warp = 4 (M) x 8 (N) threads ----
@@ -283,47 +317,53 @@ ffma_gemm_kernel(const GemmArgs p) {
 
     // ---- split-K: last CTA of the tile reduces the partials in order ----
     if constexpr (kSplit) {
-        const int S = p.split_k;
-        float4 *part = reinterpret_cast<float4 *>(p.partials);
-        const size_t tile_base = size_t(pid) * size_t(S) * 16 * kThreads;
-        float4 *mine = part + tile_base + size_t(split) * 16 * kThreads;
+        const WorkItem w = work_item(p, blockIdx.x);
+        if (w.nsplit > 1) {
+            const int S = w.nsplit;
+            const int split = w.split;
+            const int64_t pid = blockIdx.x;
+            float4 *part = reinterpret_cast<float4 *>(p.partials);
+            // slots of this tile's ranges are consecutive, starting at pid - split
+            const size_t tile_base = size_t(pid - split - p.part_base) * 16 * kThreads;
+            float4 *mine = part + tile_base + size_t(split) * 16 * kThreads;
+            unsigned *counter = p.counters + (w.tile - p.split_base);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int i = j >> 1, h = j & 1;
-            __stcg(mine + j * kThreads + tid,
-                   make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
-                               acc[i][2 * h + 1].y));
-        }
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) {
-            const unsigned prev = atomicAdd(p.counters + pid, 1u);
-            s_last = (prev == unsigned(S - 1));
-        }
-        __syncthreads();
-        if (!s_last) return;
-        __threadfence();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int i = j >> 1, h = j & 1;
-            float4 tot = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            for (int s = 0; s < S; ++s) {
-                float4 v;
-                if (s == split) {
-                    v = make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
-                                    acc[i][2 * h + 1].y);
-                } else {
-                    v = __ldcg(part + tile_base + size_t(s) * 16 * kThreads + j * kThreads + tid);
-                }
-                tot.x += v.x;
-                tot.y += v.y;
-                tot.z += v.z;
-                tot.w += v.w;
+            for (int j = 0; j < 16; ++j) {
+                const int i = j >> 1, h = j & 1;
+                __stcg(mine + j * kThreads + tid,
+                       make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
+                                   acc[i][2 * h + 1].y));
             }
-            acc[i][2 * h] = make_float2(tot.x, tot.y);
-            acc[i][2 * h + 1] = make_float2(tot.z, tot.w);
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) {
+                const unsigned prev = atomicAdd(counter, 1u);
+                s_last = (prev == unsigned(S - 1));
+            }
+            __syncthreads();
+            if (!s_last) return;
+            __threadfence();
+            // every partial, this CTA's own included, is read back from the
+            // workspace (each thread reads only what it wrote itself or what
+            // the fence and ticket made visible), so the sum order is the
+            // same whichever CTA arrives last
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int i = j >> 1, h = j & 1;
+                float4 tot = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                for (int s = 0; s < S; ++s) {
+                    const float4 v =
+                        __ldcg(part + tile_base + size_t(s) * 16 * kThreads + j * kThreads + tid);
+                    tot.x += v.x;
+                    tot.y += v.y;
+                    tot.z += v.z;
+                    tot.w += v.w;
+                }
+                acc[i][2 * h] = make_float2(tot.x, tot.y);
+                acc[i][2 * h + 1] = make_float2(tot.z, tot.w);
+            }
+            if (tid == 0) *counter = 0u;
         }
-        if (tid == 0) p.counters[pid] = 0u;
     }
 
     // ---- epilogue: C = alpha * acc (+ beta * C_old) ----
@@ -403,14 +443,16 @@ __global__ void __launch_bounds__(256) ffma_probe_kernel(int64_t iters, float *o
 
 template <bool kPacked, bool kVec, bool kEdge, bool kSplit>
 cudaError_t launch_variant(const GemmArgs &a, cudaStream_t stream) {
-    const dim3 grid(unsigned(int64_t(a.tiles_m) * a.tiles_n), unsigned(a.split_k), 1);
+    const int64_t tiles = int64_t(a.tiles_m) * a.tiles_n;
+    const dim3 grid(unsigned(a.tail_start * a.split_k + (tiles - a.tail_start) * a.tail_split),
+                    1, 1);
     ffma_gemm_kernel<kPacked, kVec, kEdge, kSplit><<<grid, kThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
 template <bool kPacked>
 cudaError_t launch_kind(const GemmArgs &a, bool vec, bool edge, cudaStream_t stream) {
-    const bool split = a.split_k > 1;
+    const bool split = a.split_k > 1 || a.tail_split > 1;
     if (!edge) {
         // full tiles are only planned on the vector path
         return split ? launch_variant<kPacked, true, false, true>(a, stream)

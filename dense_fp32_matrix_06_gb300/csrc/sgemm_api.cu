@@ -118,6 +118,39 @@ int choose_split(int64_t tiles, int64_t K, int sms, int64_t *k_per_split) {
     return best;
 }
 
+// Tail split (opt-in, SGEMM_FORCE_TAIL=s with s >= 2): cut only the tiles of
+// the last, partly filled wave of resident CTAs into s K ranges.  Off by
+// default: measured on GB300 it gains nothing (8192^3: 59.26 TFLOP/s either
+// way; 4096^3: 56.35 with, 56.93 without), because with two CTAs per SM a
+// CTA left alone on its SM in the last wave already runs at close to the
+// whole SM's rate.
+void choose_tail(int64_t tiles, int64_t K, int sms, int64_t *tail_start, int *tail_split,
+                 int64_t *tail_kps) {
+    const int64_t slots = int64_t(sms) * kCtasPerSm;
+    const int64_t kslices = ceil_div(K, kBK);
+    *tail_start = tiles;
+    *tail_split = 1;
+    *tail_kps = kslices * kBK;
+    const char *force = std::getenv("SGEMM_FORCE_TAIL");
+    const int want = force ? std::atoi(force) : 0;
+    if (want < 2 || tiles < slots) return;
+    const int64_t rem = tiles % slots;
+    if (rem == 0 || rem > kMaxSplitTiles) return;
+    const int64_t kps = ceil_div(kslices, want > kMaxSplit ? kMaxSplit : want) * kBK;
+    const int eff = int(ceil_div(K, kps));
+    if (eff < 2) return;
+    *tail_start = tiles - rem;
+    *tail_split = eff;
+    *tail_kps = kps;
+}
+
+size_t split_workspace(int64_t tiles, int split_k, int64_t tail_start, int tail_split) {
+    if (split_k > 1) return kCounterBytes + size_t(tiles) * split_k * kBM * kBN * sizeof(float);
+    if (tail_split > 1)
+        return kCounterBytes + size_t(tiles - tail_start) * tail_split * kBM * kBN * sizeof(float);
+    return 0;
+}
+
 // Kernel the planner names: the scalar-FMA kernel unless SGEMM_FORCE_KERNEL
 // (0 = scalar, 1 = packed) asks otherwise; the override exists for sweeps.
 // Measured on GB300 at 8192^3: scalar 59.0 TFLOP/s, packed 54.0 (a packed FMA
@@ -152,13 +185,18 @@ sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb
     int64_t kps = 0;
     p.split_k = (M > 0 && N > 0 && K > 0) ? choose_split(tiles, K, sms, &kps) : 1;
     p.k_per_split = kps;
+    int tail_split = 1;
+    p.tail_start = tiles;
+    p.tail_k_per_split = kps;
+    if (p.split_k == 1 && M > 0 && N > 0 && K > 0)
+        choose_tail(tiles, K, sms, &p.tail_start, &tail_split, &p.tail_k_per_split);
+    p.tail_split = tail_split;
     const bool full = (M % kBM == 0) && (N % kBN == 0) && (K % kBK == 0) &&
-                      (p.split_k == 1 || K % p.k_per_split == 0);
+                      (p.split_k == 1 || K % p.k_per_split == 0) &&
+                      (p.tail_split == 1 || K % p.tail_k_per_split == 0);
     p.edge = (p.vec && full) ? 0 : 1;
-    p.grid_ctas = tiles * p.split_k;
-    p.workspace_bytes =
-        p.split_k > 1 ? kCounterBytes + size_t(tiles) * p.split_k * kBM * kBN * sizeof(float)
-                      : 0;
+    p.grid_ctas = p.tail_start * p.split_k + (tiles - p.tail_start) * p.tail_split;
+    p.workspace_bytes = split_workspace(tiles, p.split_k, p.tail_start, p.tail_split);
     *out = p;
     return SGEMM_OK;
 }
@@ -225,12 +263,17 @@ sgemm_status run(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K, float
     a.alpha = alpha;
     a.beta = beta;
     a.k_per_split = plan.k_per_split;
+    a.tail_k_per_split = plan.tail_k_per_split;
+    a.tail_start = plan.tail_start;
     a.split_k = plan.split_k;
+    a.tail_split = plan.tail_split;
     a.tiles_m = int32_t(plan.tiles_m);
     a.tiles_n = int32_t(plan.tiles_n);
+    a.split_base = plan.split_k > 1 ? 0 : plan.tail_start;
+    a.part_base = plan.split_k > 1 ? 0 : plan.tail_start;
     a.counters = nullptr;
     a.partials = nullptr;
-    if (plan.split_k > 1) {
+    if (plan.split_k > 1 || plan.tail_split > 1) {
         a.counters = static_cast<unsigned *>(workspace);
         a.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + kCounterBytes);
     }
@@ -244,21 +287,29 @@ bool plan_matches(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int64_t
     if (p.kernel != kKernelFfma128 && p.kernel != kKernelFfma2x128) return false;
     if (p.bm != kBM || p.bn != kBN || p.bk != kBK || p.threads != kThreads) return false;
     if (p.tiles_m != ceil_div(M, kBM) || p.tiles_n != ceil_div(N, kBN)) return false;
+    const int64_t tiles = p.tiles_m * p.tiles_n;
     if (p.split_k < 1 || p.split_k > kMaxSplit) return false;
+    if (p.tail_split < 1 || p.tail_split > kMaxSplit) return false;
+    if (p.tail_start < 0 || p.tail_start > tiles) return false;
+    if (p.split_k > 1 && (p.tail_start != tiles || tiles > kMaxSplitTiles)) return false;
+    if (p.tail_split > 1 && tiles - p.tail_start > kMaxSplitTiles) return false;
     if (p.k_per_split <= 0 || p.k_per_split % kBK != 0) return false;
+    if (p.tail_k_per_split <= 0 || p.tail_k_per_split % kBK != 0) return false;
     if (K > 0 && ceil_div(K, p.k_per_split) != p.split_k) return false;
-    if (p.split_k > 1 && p.tiles_m * p.tiles_n > kMaxSplitTiles) return false;
+    if (K > 0 && p.tail_start < tiles && ceil_div(K, p.tail_k_per_split) != p.tail_split)
+        return false;
+    if (p.grid_ctas != p.tail_start * p.split_k + (tiles - p.tail_start) * p.tail_split)
+        return false;
     const bool vec_ok = lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0 && aligned16(A) &&
                         aligned16(B) && aligned16(C);
     if (p.vec && !vec_ok) return false;
     if (!p.edge) {
         if (!p.vec) return false;
-        if (M % kBM || N % kBN || K % kBK || (p.split_k > 1 && K % p.k_per_split)) return false;
+        if (M % kBM || N % kBN || K % kBK || (p.split_k > 1 && K % p.k_per_split) ||
+            (p.tail_split > 1 && K % p.tail_k_per_split))
+            return false;
     }
-    const size_t need =
-        p.split_k > 1
-            ? kCounterBytes + size_t(p.tiles_m * p.tiles_n) * p.split_k * kBM * kBN * sizeof(float)
-            : 0;
+    const size_t need = split_workspace(tiles, p.split_k, p.tail_start, p.tail_split);
     return p.workspace_bytes == need;
 }
 
@@ -414,7 +465,9 @@ extern "C" sgemm_status sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alp
         if (s != SGEMM_OK) return s;
         // The buffer keeps whatever the previous call left; the tile counters
         // must start at zero, so clear the ones this launch uses.
-        const size_t counter_bytes = size_t(plan.tiles_m * plan.tiles_n) * sizeof(unsigned);
+        const int64_t split_tiles = plan.split_k > 1 ? plan.tiles_m * plan.tiles_n
+                                                     : plan.tiles_m * plan.tiles_n - plan.tail_start;
+        const size_t counter_bytes = size_t(split_tiles) * sizeof(unsigned);
         const cudaError_t e = cudaMemsetAsync(ws, 0, counter_bytes, st);
         if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
     }
@@ -445,11 +498,13 @@ sgemm_status tf32x3_run(int64_t M, int64_t N, int64_t K, float alpha, const floa
         e = launch_scale(C, M, N, ldc, beta, st);
         return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
     }
+    // The per-stream workspace also carries the split-K tile counters, which
+    // must stay zero: the hi/lo operands go after the counter block.
     void *ws = nullptr;
-    s = library_workspace(dev, st, tf32x3_workspace_bytes(M, N, K), &ws);
+    s = library_workspace(dev, st, kCounterBytes + tf32x3_workspace_bytes(M, N, K), &ws);
     if (s != SGEMM_OK) return s;
-    e = launch_tf32x3(A, lda, B, ldb, C, ldc, M, N, K, alpha, beta, ws, limit_ns, inject_stall,
-                      st);
+    e = launch_tf32x3(A, lda, B, ldb, C, ldc, M, N, K, alpha, beta,
+                      static_cast<char *>(ws) + kCounterBytes, limit_ns, inject_stall, st);
     return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
 }
 

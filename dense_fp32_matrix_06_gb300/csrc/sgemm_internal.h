@@ -33,11 +33,22 @@ struct GemmArgs {
     int64_t M, N, K;
     int64_t lda, ldb, ldc;
     float alpha, beta;
-    int64_t k_per_split;   // multiple of kBK
+    // Work decomposition.  Tiles [0, tail_start) are cut into split_k K ranges
+    // of k_per_split each; tiles [tail_start, tiles) into tail_split ranges of
+    // tail_k_per_split.  CTA `pid` of the 1-D grid owns one (tile, range)
+    // pair; the ranges of one tile are consecutive pids.
+    int64_t k_per_split;       // multiple of kBK
+    int64_t tail_k_per_split;  // multiple of kBK
+    int64_t tail_start;
     int32_t split_k;
+    int32_t tail_split;
     int32_t tiles_m, tiles_n;
-    unsigned *counters;    // split_k > 1: one per tile, zero on entry and exit
-    float *partials;       // split_k > 1: tiles * split_k * kBM * kBN floats
+    // Split tiles only: counter of tile t is counters[t - split_base], partial
+    // of CTA pid is slot pid - part_base (16 x kThreads float4 per slot).
+    int64_t split_base;
+    int64_t part_base;
+    unsigned *counters;    // zero on entry and exit
+    float *partials;
 };
 
 // Kernel ids a plan can name.

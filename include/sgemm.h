@@ -81,14 +81,18 @@ typedef struct {
                               (same arithmetic and summation order) */
     int32_t bm, bn, bk;    /* CTA tile (rows of C, columns of C, K slice) */
     int32_t threads;       /* threads per CTA */
-    int32_t split_k;       /* number of K partitions (1 = none) */
+    int32_t split_k;       /* K partitions of tiles [0, tail_start) (1 = none) */
     int32_t vec;           /* 1: 16-byte vector loads/stores; 0: 4-byte */
     int32_t edge;          /* 1: bounds-checked tiles; 0: all tiles full */
-    int32_t reserved;
+    int32_t tail_split;    /* K partitions of tiles [tail_start, tiles) (1 = none) */
     int64_t k_per_split;   /* K extent of one partition (a multiple of bk) */
     int64_t tiles_m, tiles_n;
-    int64_t grid_ctas;     /* CTAs launched = tiles_m * tiles_n * split_k */
-    size_t workspace_bytes;/* device scratch the plan needs (0 if split_k == 1) */
+    int64_t grid_ctas;     /* CTAs launched */
+    size_t workspace_bytes;/* device scratch the plan needs (0 without split tiles) */
+    int64_t tail_start;    /* first tile (in launch order) of the tail region; tiles
+                              when there is none.  Only the last, partly filled wave
+                              of tiles is split, so it ends sooner */
+    int64_t tail_k_per_split; /* K extent of one tail partition */
 } gemm_plan_t;
 
 /*

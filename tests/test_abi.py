@@ -113,9 +113,28 @@ def test_plan_full_tiles_take_the_unchecked_vector_path(lib):
     p = plan(8192, 8192, 8192)
     assert (p.bm, p.bn, p.bk, p.threads) == (128, 128, 16, 256)
     assert p.tiles_m == 64 and p.tiles_n == 64
-    assert p.split_k == 1 and p.workspace_bytes == 0
     assert p.vec == 1 and p.edge == 0
-    assert p.grid_ctas == 4096
+    assert p.split_k == 1 and p.tail_split == 1 and p.tail_start == 4096
+    assert p.grid_ctas == 4096 and p.workspace_bytes == 0
+
+
+def test_plan_tail_split_is_opt_in(lib, monkeypatch):
+    monkeypatch.setenv("SGEMM_FORCE_TAIL", "2")
+    p = plan(8192, 8192, 8192)
+    # 4096 tiles over 304 resident slots: 13 full waves + 144 tiles, which
+    # are the ones split in two along K
+    assert p.split_k == 1
+    assert p.tail_start == 4096 - 144 and p.tail_split == 2 and p.tail_k_per_split == 4096
+    assert p.grid_ctas == 4096 - 144 + 2 * 144
+    assert p.workspace_bytes == sg.WORKSPACE_COUNTER_BYTES + 144 * 2 * 128 * 128 * 4
+    assert p.edge == 0
+    q = plan(2048, 2048, 2048)                              # 256 tiles: less than a wave
+    assert q.tail_split == 1 and q.tail_start == q.tiles_m * q.tiles_n
+    r = plan(1000, 1000, 100)                               # short K: nothing to split
+    assert r.tail_split == 1 or r.tail_k_per_split >= 16
+    monkeypatch.setenv("SGEMM_FORCE_TAIL", "0")
+    t = plan(8192, 8192, 8192)
+    assert t.tail_split == 1 and t.workspace_bytes == 0 and t.grid_ctas == 4096
 
 
 def test_plan_ragged_shape_takes_the_checked_scalar_path(lib):
@@ -136,6 +155,7 @@ def test_plan_split_k_fills_the_gpu_when_tiles_are_few(lib):
     assert p.k_per_split % p.bk == 0
     assert (16384 + p.k_per_split - 1) // p.k_per_split == p.split_k
     assert p.grid_ctas == 64 * p.split_k
+    assert p.tail_split == 1 and p.tail_start == 64
     assert p.workspace_bytes == sg.WORKSPACE_COUNTER_BYTES + 64 * p.split_k * 128 * 128 * 4
     # MLP-down: 48 tiles, K = 3072
     assert plan(1024, 768, 3072).split_k > 1

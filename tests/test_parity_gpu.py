@@ -216,6 +216,24 @@ def test_forced_kernel_and_split(sg, monkeypatch, kernel, split):
     run_and_check(sg, r)
 
 
+@pytest.mark.parametrize("M,N,K,dist,lds", [
+    (2560, 2048, 1024, "int4", None),        # 320 tiles: the tail tiles split 4 ways
+    (2560, 2048, 1040, "uniform", None),
+    (2500, 2000, 777, "uniform", (781, 2003, 2001)),   # ragged tail tiles, scalar path
+])
+def test_tail_split_parity(sg, monkeypatch, M, N, K, dist, lds):
+    lda, ldb, ldc = lds if lds else (None, None, None)
+    p = workloads.make(M, N, K, dist=dist, seed=51, lda=lda, ldb=ldb, ldc=ldc,
+                       alpha=1.5 if dist == "int4" else 0.75, beta=0.5,
+                       c0_dist="int4" if dist == "int4" else "uniform")
+    monkeypatch.setenv("SGEMM_FORCE_TAIL", "4")
+    plan = sg.gemm_plan_for_sms(p.M, p.N, p.K, p.lda, p.ldb, p.ldc, sm_count=152)
+    assert plan.tail_split > 1
+    run_and_check(sg, p, exact=dist == "int4")
+    monkeypatch.setenv("SGEMM_FORCE_TAIL", "0")
+    run_and_check(sg, p, exact=dist == "int4")
+
+
 def test_both_kernels_bit_identical(sg, monkeypatch):
     outs = []
     for kernel in ("0", "1"):

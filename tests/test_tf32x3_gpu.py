@@ -159,6 +159,37 @@ def test_large_sampled(sg, name, dist):
             <= TOL_TF32X3
 
 
+def test_split_k_after_tensor_mode_on_the_same_stream(sg):
+    """Both modes use the library's per-stream workspace; the tensor mode must
+    leave the split-K tile counters zero."""
+    import torch
+    stream = torch.cuda.current_stream().cuda_stream
+    p = workloads.workload("long_k")           # split-K FFMA plan (37.8 MB of workspace)
+    A = torch.from_numpy(p.A).cuda()
+    B = torch.from_numpy(p.B).cuda()
+    C = torch.full((p.M, p.N), float("nan"), device="cuda")
+    plan = sg.gemm_plan(p.M, p.N, p.K, p.lda, p.ldb, p.ldc, A.data_ptr(), B.data_ptr(),
+                        C.data_ptr())
+    assert plan.split_k > 1
+
+    def ffma():
+        sg.sgemm_ptr(p.M, p.N, p.K, 1.0, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, 0.0,
+                     C.data_ptr(), p.N, stream)
+
+    ffma()                                     # grows the workspace first
+    run(sg, workloads.workload("square1024ab"))   # tensor mode reuses it (16 MB)
+    C.fill_(float("nan"))
+    ffma()                                     # counters must still be zero
+    torch.cuda.synchronize()
+    Ch = C.cpu().numpy()
+    assert np.all(np.isfinite(Ch))
+    ii, jj = workloads.sample_indices(p.M, p.N, 2000, seed=3)
+    ref = oracle.sgemm_entries(p.M, p.N, p.K, 1.0, p.A, p.B, 0.0, None, ii, jj, lda=p.lda,
+                               ldb=p.ldb)
+    den = p.K * float(np.abs(p.A).max()) * float(np.abs(p.B).max())
+    assert float(np.abs(Ch[ii, jj].astype(np.float64) - ref).max()) / den <= 1e-6
+
+
 def test_bounded_waits_expire_cleanly(sg):
     """The operand loads are withheld, so every wait runs out after 20 ms: the
     call reports SGEMM_ERR_TIMEOUT, C is untouched, and the context stays
