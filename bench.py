@@ -364,6 +364,10 @@ def run_ours(args):
     if not args.no_tf32x3:
         tc = run_tf32x3(sg, p, A, B, C, stream, args, dist, device)
 
+    extras = None
+    if not args.no_extras and rank == 0:
+        extras = run_extras(sg, device, stream)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(p, target_s=args.cpu_seconds)
@@ -387,6 +391,8 @@ def run_ours(args):
             line["ffma_probe"] = probe
         if tc:
             line["tf32x3"] = tc
+        if extras:
+            line["sgemm_ex"] = extras
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -440,6 +446,63 @@ def run_tf32x3(sg, p, A, B, C, stream, args, dist, device):
                          "peak_source": src,
                          "note": "achieved = 3 tf32 products x 2MNK over the whole call "
                                  "(split pre-pass included)"}}
+
+
+# (name, op_a, op_b, M, N, K, batch, bias, act): batched, transposed and
+# fused-epilogue forms on GPT-2-small shapes and a square size
+EXTRA_CASES = [
+    ("gpt2_attn_qkT_12x1024x1024x64", 0, 1, 1024, 1024, 64, 12, False, 0),
+    ("gpt2_attn_pv_12x1024x64x1024", 0, 0, 1024, 64, 1024, 12, False, 0),
+    ("gpt2_mlp_up_1024x3072x768", 0, 0, 1024, 3072, 768, 1, False, 0),
+    ("gpt2_mlp_up_1024x3072x768_bias_gelu", 0, 0, 1024, 3072, 768, 1, True, 1),
+    ("square4096_nn", 0, 0, 4096, 4096, 4096, 1, False, 0),
+    ("square4096_nt", 0, 1, 4096, 4096, 4096, 1, False, 0),
+    ("square4096_tn", 1, 0, 4096, 4096, 4096, 1, False, 0),
+    ("square4096_tt", 1, 1, 4096, 4096, 4096, 1, False, 0),
+]
+
+
+def run_extras(sg, device, stream):
+    """TFLOP/s (2MNK*batch / time, CUDA events, median of reps) of sgemm_ex forms."""
+    import torch
+    out = {}
+    sh = stream.cuda_stream
+    g = torch.Generator(device=device)
+    g.manual_seed(5)
+    for name, op_a, op_b, M, N, K, batch, has_bias, act in EXTRA_CASES:
+        ra, ca = (K, M) if op_a else (M, K)
+        rb, cb = (N, K) if op_b else (K, N)
+        A = torch.rand((batch, ra, ca), device=device, generator=g) * 2 - 1
+        B = torch.rand((batch, rb, cb), device=device, generator=g) * 2 - 1
+        C = torch.empty((batch, M, N), device=device)
+        bias = (torch.rand(N, device=device, generator=g) - 0.5) if has_bias else None
+
+        def call():
+            sg.sgemm_ex_ptr(op_a, op_b, M, N, K, 1.0, A.data_ptr(), ca, ra * ca, B.data_ptr(),
+                            cb, rb * cb, 0.0, C.data_ptr(), N, M * N, batch,
+                            bias.data_ptr() if bias is not None else 0, act, sh)
+
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize(device)
+        flops = 2.0 * M * N * K * batch
+        reps = max(5, min(50, int(2e11 / flops)))
+        ts = []
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            torch.cuda.synchronize(device)
+            ts.append(e0.elapsed_time(e1) / 1e3)
+        ts.sort()
+        med = ts[len(ts) // 2]
+        out[name] = {"tflops": round(flops / med / 1e12, 3), "ms": round(med * 1e3, 4),
+                     "op": ("T" if op_a else "N") + ("T" if op_b else "N"), "batch": batch,
+                     "bias": has_bias, "act": "gelu_tanh" if act else None}
+        del A, B, C, bias
+    return out
 
 
 def ffma_probe(sg, device, sms):
@@ -517,6 +580,8 @@ def parse(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
     ap.add_argument("--probe", action="store_true", help="also time the fp32 FMA probe")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the batched / transposed / fused-epilogue sgemm_ex cases")
     ap.add_argument("--no-tf32x3", action="store_true",
                     help="skip the separately reported 3xTF32 tensor-core mode")
     return ap.parse_args(argv)

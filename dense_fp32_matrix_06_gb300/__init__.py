@@ -49,7 +49,10 @@ EXPORTED_SYMBOLS = (
     "sgemm_tf32x3",
     "sgemm_device_status",
     "sgemm_tf32x3_stall_selftest",
+    "sgemm_ex",
 )
+OP_N, OP_T = 0, 1
+ACT_NONE, ACT_GELU_TANH = 0, 1
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
@@ -136,6 +139,10 @@ def load_library() -> ctypes.CDLL:
         lib.sgemm_last_cuda_error.restype = ctypes.c_int
         lib.sgemm_ffma_probe.argtypes = [_i64, _i64, ctypes.c_int32, _vp, _vp]
         lib.sgemm_ffma_probe.restype = ctypes.c_int
+        lib.sgemm_ex.argtypes = [ctypes.c_int32, ctypes.c_int32, _i64, _i64, _i64, _f32, _vp,
+                                 _i64, _i64, _vp, _i64, _i64, _f32, _vp, _i64, _i64, _i64, _vp,
+                                 ctypes.c_int32, _vp]
+        lib.sgemm_ex.restype = ctypes.c_int
         lib.sgemm_noalloc.argtypes = lib.sgemm.argtypes
         lib.sgemm_noalloc.restype = ctypes.c_int
         lib.sgemm_tf32x3.argtypes = lib.sgemm.argtypes
@@ -202,6 +209,16 @@ def sgemm_noalloc_ptr(M: int, N: int, K: int, alpha: float, A: int, lda: int, B:
     and race; keep them ordered."""
     _check(load_library().sgemm_noalloc(M, N, K, alpha, A or None, lda, B or None, ldb, beta,
                                         C or None, ldc, stream or None), "sgemm_noalloc")
+
+
+def sgemm_ex_ptr(op_a: int, op_b: int, M: int, N: int, K: int, alpha: float, A: int, lda: int,
+                 stride_a: int, B: int, ldb: int, stride_b: int, beta: float, C: int, ldc: int,
+                 stride_c: int, batch: int = 1, bias: int = 0, act: int = ACT_NONE,
+                 stream: int = 0) -> None:
+    """sgemm_ex(): C_b = act(alpha op(A_b) op(B_b) + beta C_b + bias), b < batch."""
+    _check(load_library().sgemm_ex(op_a, op_b, M, N, K, alpha, A or None, lda, stride_a,
+                                   B or None, ldb, stride_b, beta, C or None, ldc, stride_c,
+                                   batch, bias or None, act, stream or None), "sgemm_ex")
 
 
 def sgemm_tf32x3_ptr(M: int, N: int, K: int, alpha: float, A: int, lda: int, B: int, ldb: int,
@@ -328,6 +345,59 @@ def sgemm_tf32x3(A, B, C=None, alpha: float = 1.0, beta: float = 0.0, stream=Non
     with torch.cuda.device(A.device):
         sgemm_tf32x3_ptr(M, N, K, float(alpha), a_ptr, max(lda, K, 1), b_ptr, max(ldb, N, 1),
                          float(beta), c_ptr, max(ldc, N, 1), _stream_handle(stream))
+    return C
+
+
+def matmul(A, B, bias=None, activation: str | None = None, trans_a: bool = False,
+           trans_b: bool = False, alpha: float = 1.0, C=None, beta: float = 0.0, stream=None):
+    """act(alpha * op(A) @ op(B) + beta * C + bias) on torch CUDA float32 tensors.
+
+    A, B (and C) are 2-D, or 3-D with a leading batch dimension (a 2-D operand
+    is shared by every batch).  trans_a / trans_b read the stored matrix
+    transposed (A stored K x M, B stored N x K).  bias: a length-N vector;
+    activation: None or "gelu_tanh".  Returns C.
+    """
+    import torch
+    for name, t in (("A", A), ("B", B)):
+        if not isinstance(t, torch.Tensor) or t.dim() not in (2, 3):
+            raise ValueError(f"{name} must be a 2-D or 3-D torch tensor")
+    batch = max(A.shape[0] if A.dim() == 3 else 1, B.shape[0] if B.dim() == 3 else 1)
+    for name, t in (("A", A), ("B", B)):
+        if t.dim() == 3 and t.shape[0] != batch:
+            raise ValueError(f"{name} has batch {t.shape[0]}, expected {batch}")
+    a2 = A if A.dim() == 2 else A[0]
+    b2 = B if B.dim() == 2 else B[0]
+    M, K = (a2.shape[1], a2.shape[0]) if trans_a else (a2.shape[0], a2.shape[1])
+    Kb, N = (b2.shape[1], b2.shape[0]) if trans_b else (b2.shape[0], b2.shape[1])
+    if K != Kb:
+        raise ValueError(f"inner dimensions differ: op(A) is {M}x{K}, op(B) is {Kb}x{N}")
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs an input C")
+        C = torch.empty((batch, M, N) if batch > 1 or A.dim() == 3 or B.dim() == 3 else (M, N),
+                        dtype=torch.float32, device=A.device)
+    c2 = C if C.dim() == 2 else C[0]
+    if tuple(c2.shape) != (M, N):
+        raise ValueError(f"C must be ({M}, {N}) per batch")
+    a_ptr, lda = _row_major_view(a2, "A")
+    b_ptr, ldb = _row_major_view(b2, "B")
+    c_ptr, ldc = _row_major_view(c2, "C")
+    sa = A.stride(0) if A.dim() == 3 and batch > 1 else 0
+    sb = B.stride(0) if B.dim() == 3 and batch > 1 else 0
+    sc = C.stride(0) if C.dim() == 3 and batch > 1 else 0
+    bias_ptr = 0
+    if bias is not None:
+        if bias.dtype != torch.float32 or bias.numel() != N or not bias.is_contiguous():
+            raise ValueError("bias must be a contiguous float32 vector of length N")
+        bias_ptr = bias.data_ptr()
+    act = {None: ACT_NONE, "none": ACT_NONE, "gelu_tanh": ACT_GELU_TANH}.get(activation)
+    if act is None:
+        raise ValueError(f"unknown activation {activation!r}")
+    with torch.cuda.device(A.device):
+        sgemm_ex_ptr(OP_T if trans_a else OP_N, OP_T if trans_b else OP_N, M, N, K, float(alpha),
+                     a_ptr, max(lda, (M if trans_a else K), 1), sa, b_ptr,
+                     max(ldb, (K if trans_b else N), 1), sb, float(beta), c_ptr, max(ldc, N, 1),
+                     sc, batch, bias_ptr, act, _stream_handle(stream))
     return C
 
 

@@ -1,406 +1,15 @@
-// ffma_gemm.cu -- the fp32 CUDA-core GEMM kernel for sm_103a.
-//
-// C = alpha * A * B + beta * C, row-major, any M, N, K.
-//
-// Design (prior art on the pages, re-derived for a 152-SM Blackwell part):
-//  * CTA tile 128 x 128, K slice 16, 256 threads, 8 x 8 accumulators per
-//    thread updated as outer products: for every k the thread reads 8 values
-//    of column k of the A tile and 8 of row k of the B tile and does 64 FMAs
-//    (velog @levelstage "AutoMinepp4", section "행렬곱: by 벡터의 외적": the
-//    product is a sum of outer products, which keeps the accumulators in
-//    registers; "Micro_gemm_4x4 - cuBLAS micro GEMM skeleton", section 8:
-//    the fully unrolled FMA pattern over the micro tile).
-//  * Two issue forms of the same arithmetic: scalar fma.rn.f32 (the
-//    default) or packed fma.rn.f32x2, each lane of which is an ordinary
-//    round-to-nearest fp32 FMA, so every accumulator sees exactly the same
-//    sequence of roundings either way and the two give bit-identical C.
-//    Measured on GB300 the packed form is slower: it holds the FMA pipe two
-//    cycles, so it saves issue slots but not pipe time, and the broadcast
-//    operand pairs push the kernel past its 128-register budget.
-//  * The 8 x 8 block is split into four 4 x 4 quadrants 64 rows / 64 columns
-//    apart, so one 128-bit shared load serves 4 rows (or columns) and the
-//    loads of a warp are conflict-free: a warp reads 4 distinct 16-byte A
-//    chunks (each broadcast to 8 lanes) and 8 distinct B chunks.
-//  * A is staged transposed (K-major -> M-major) through registers: a warp
-//    loads 8 rows x 16 k of A with 128-bit loads and scatters them into the
-//    smem page with an XOR swizzle that keeps the stores conflict-free
-//    (velog @levelstage "AutoMinepp7", section "직사각형 타일링": chunks are
-//    fetched into registers before the compute and split into the other
-//    local-memory page after it).  B rows are already N-contiguous and go
-//    straight into smem with 16-byte cp.async copies, holding no registers.
-//  * Two smem pages: slice t+1 is in flight (A in registers, B in async
-//    copies) while slice t is computed; one barrier per K slice
-//    ("Micro_gemm_4x4 - cuBLAS micro GEMM skeleton", section 8, double
-//    buffering, with the asynchronous copy the page suggests for Ampere and
-//    later).  Shared-memory fragments are double-buffered in registers
-//    across the 16 k steps of a slice.
-//  * Edges: out-of-range A/B elements load as 0 and C stores are predicated
-//    on row < M, col < N ("Micro_gemm_4x4 ...", sections 6 and 9; "GPU
-//    Target", section "타일링된 행렬 곱셈": out-of-range loads read as zero).
-//  * Epilogue: c = alpha * acc, then c = fma(beta, C_old, c) only when
-//    beta != 0 (C is not read otherwise), stored with 128-bit stores.
-//  * Split-K: when the tile grid cannot fill the GPU, K is cut into split_k
-//    ranges; when only the last wave of tiles is partly empty, just those
-//    tail tiles are cut (tail_split ranges), so the last wave finishes in a
-//    fraction of a full tile's time.  Every CTA of a split tile writes its
-//    partial tile to the workspace, the last CTA of the tile to arrive
-//    (atomic ticket, no waiting) sums the partials in ascending split order
-//    and runs the epilogue, then rearms the counter.  The sum order is fixed,
-//    so results are deterministic run to run.
+// ffma_gemm.cu -- the fp32 CUDA-core GEMM (kernel template in ffma_kernel.cuh):
+// the plain layout (op(A) = A, op(B) = B) in both issue forms, the dispatch
+// over layouts, and the small helper kernels (C = beta*C, the FMA-rate probe).
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
+#include "ffma_kernel.cuh"
 #include "sgemm_internal.h"
 
 namespace sgemm_impl {
 namespace {
-
-__device__ __forceinline__ float4 ldg4(const float *p) {
-    return __ldg(reinterpret_cast<const float4 *>(p));
-}
-
-__device__ __forceinline__ float ldg1(const float *p) { return __ldg(p); }
-
-__device__ __forceinline__ unsigned smem_addr(const void *p) {
-    return static_cast<unsigned>(__cvta_generic_to_shared(p));
-}
-
-// 16-byte async copy global -> shared; bytes past `src_bytes` are zero-filled
-// and not read.
-__device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_addr(dst)),
-                 "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-
-// 4-byte async copy; src_bytes == 0 writes a zero without reading.
-__device__ __forceinline__ void cp_async4(void *dst, const void *src, int src_bytes) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(smem_addr(dst)),
-                 "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;\n" ::: "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.wait_all;\n" ::: "memory");
-}
-
-// Column of A-tile element (k, m) inside its smem row.  XOR-ing bits 3..4 of m
-// with k/4 keeps every aligned group of 4 columns contiguous (so fragment
-// reads stay 128-bit) and spreads the transposing stores of a warp -- 8 rows x
-// 4 k-groups -- over all 32 banks.
-__device__ __forceinline__ int a_col(int k, int m) { return m ^ (((k >> 2) & 3) << 3); }
-
-// The (tile, K range) pair CTA `pid` computes, and the tile's coordinates.
-struct WorkItem {
-    int64_t tile;
-    int64_t row0, col0;
-    int64_t kbeg, kend;
-    int split, nsplit;
-};
-
-__device__ __forceinline__ WorkItem work_item(const GemmArgs &p, int64_t pid) {
-    WorkItem w;
-    const int64_t lead = p.tail_start * p.split_k;
-    int64_t kps;
-    if (pid < lead) {
-        w.tile = pid / p.split_k;
-        w.split = int(pid - w.tile * p.split_k);
-        w.nsplit = p.split_k;
-        kps = p.k_per_split;
-    } else {
-        const int64_t j = pid - lead;
-        w.tile = p.tail_start + j / p.tail_split;
-        w.split = int(j % p.tail_split);
-        w.nsplit = p.tail_split;
-        kps = p.tail_k_per_split;
-    }
-    // grouped raster over kGroupM tile rows (L2 reuse of A and B panels)
-    const int64_t per_group = int64_t(kGroupM) * p.tiles_n;
-    const int64_t group = w.tile / per_group;
-    const int64_t first_m = group * kGroupM;
-    const int64_t gm = min(int64_t(p.tiles_m) - first_m, int64_t(kGroupM));
-    const int64_t in_group = w.tile - group * per_group;
-    w.row0 = (first_m + in_group % gm) * kBM;
-    w.col0 = (in_group / gm) * kBN;
-    w.kbeg = int64_t(w.split) * kps;
-    w.kend = min(p.K, w.kbeg + kps);
-    return w;
-}
-
-template <bool kPacked, bool kVec, bool kEdge, bool kSplit>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
-ffma_gemm_kernel(const GemmArgs p) {
-    __shared__ __align__(16) float As[2][kBK][kBM];
-    __shared__ __align__(16) float Bs[2][kBK][kBN];
-    __shared__ int s_last;
-
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int lane = tid & 31;
-
-    // ---- (tile, K range) of this CTA; recomputed after the main loop so
-    // none of it stays live in registers across it ----
-    int64_t row0, col0, kbeg, kend;
-    {
-        const WorkItem w = work_item(p, blockIdx.x);
-        row0 = w.row0;
-        col0 = w.col0;
-        kbeg = w.kbeg;
-        kend = w.kend;
-    }
-    const int nslices = kend > kbeg ? int((kend - kbeg + kBK - 1) / kBK) : 0;
-
-    // ---- compute mapping: warp = 4 (M) x 8 (N) threads ----
-    const int tm = (warp >> 1) * 4 + (lane >> 3);   // 0..15
-    const int tn = (warp & 1) * 8 + (lane & 7);     // 0..15
-
-    // ---- load mapping ----
-    // A: rows a_row and a_row + 64, k group a_kc (4 consecutive k): a warp
-    // reads 8 rows x 64 contiguous bytes per load.
-    const int a_row = tid >> 2;              // 0..63
-    const int a_kc = tid & 3;                // 0..3
-    // B: rows b_row and b_row + 8, 4 columns at b_col: a warp reads one
-    // 512-byte row segment.
-    const int b_row = tid >> 5;              // 0..7
-    const int b_col = (tid & 31) * 4;        // 0..124
-
-    bool a_ok[2];
-    const float *a_ptr[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int64_t r = row0 + a_row + 64 * h;
-        a_ok[h] = !kEdge || r < p.M;
-        a_ptr[h] = p.A + (a_ok[h] ? r : 0) * p.lda + kbeg + a_kc * 4;
-    }
-    const float *b_ptr = p.B + (kbeg + b_row) * p.ldb + col0 + b_col;
-    const int64_t b_step = int64_t(kBK) * p.ldb;
-
-    float4 ra[2];
-
-    // A slice t -> registers (zero outside the matrix and outside [kbeg, kend)).
-    auto fetch_a = [&](int t) {
-        const int64_t koff = int64_t(t) * kBK;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const float *src = a_ptr[h] + koff;
-            if constexpr (!kEdge) {
-                ra[h] = ldg4(src);
-            } else {
-                const int64_t k = kbeg + koff + a_kc * 4;
-                if (kVec && a_ok[h] && k + 3 < kend) {
-                    ra[h] = ldg4(src);
-                } else {
-                    ra[h].x = (a_ok[h] && k + 0 < kend) ? ldg1(src + 0) : 0.0f;
-                    ra[h].y = (a_ok[h] && k + 1 < kend) ? ldg1(src + 1) : 0.0f;
-                    ra[h].z = (a_ok[h] && k + 2 < kend) ? ldg1(src + 2) : 0.0f;
-                    ra[h].w = (a_ok[h] && k + 3 < kend) ? ldg1(src + 3) : 0.0f;
-                }
-            }
-        }
-    };
-
-    // registers -> A page, transposed (M-contiguous) and swizzled.
-    auto stash_a = [&](int page) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int m = a_row + 64 * h;
-            const int k = a_kc * 4;
-            As[page][k + 0][a_col(k, m)] = ra[h].x;
-            As[page][k + 1][a_col(k, m)] = ra[h].y;
-            As[page][k + 2][a_col(k, m)] = ra[h].z;
-            As[page][k + 3][a_col(k, m)] = ra[h].w;
-        }
-    };
-
-    // B slice t -> B page with async copies (zero-filled outside).
-    auto copy_b = [&](int t, int page) {
-        const int64_t koff = int64_t(t) * kBK;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const float *src = b_ptr + t * b_step + int64_t(8 * h) * p.ldb;
-            float *dst = &Bs[page][b_row + 8 * h][b_col];
-            if constexpr (!kEdge) {
-                cp_async16(dst, src, 16);
-            } else {
-                const int64_t k = kbeg + koff + b_row + 8 * h;
-                const int64_t c = col0 + b_col;
-                const bool k_ok = k < kend;
-                if constexpr (kVec) {
-                    int64_t n = k_ok ? p.N - c : 0;
-                    n = n < 0 ? 0 : (n > 4 ? 4 : n);
-                    cp_async16(dst, n > 0 ? src : p.B, int(n) * 4);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const bool ok = k_ok && c + e < p.N;
-                        cp_async4(dst + e, ok ? src + e : p.B, ok ? 4 : 0);
-                    }
-                }
-            }
-        }
-        cp_async_commit();
-    };
-
-    float2 acc[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
-
-    if (nslices > 0) {
-        copy_b(0, 0);
-        fetch_a(0);
-        stash_a(0);
-        cp_async_wait_all();
-    }
-    __syncthreads();
-
-    for (int t = 0; t < nslices; ++t) {
-        const int page = t & 1;
-        const bool more = t + 1 < nslices;
-        if (more) {
-            copy_b(t + 1, page ^ 1);
-            fetch_a(t + 1);
-        }
-
-        float4 af[2][2], bf[2][2];
-        af[0][0] = *reinterpret_cast<const float4 *>(&As[page][0][a_col(0, tm * 4)]);
-        af[0][1] = *reinterpret_cast<const float4 *>(&As[page][0][a_col(0, 64 + tm * 4)]);
-        bf[0][0] = *reinterpret_cast<const float4 *>(&Bs[page][0][tn * 4]);
-        bf[0][1] = *reinterpret_cast<const float4 *>(&Bs[page][0][64 + tn * 4]);
-#pragma unroll
-        for (int kk = 0; kk < kBK; ++kk) {
-            const int cur = kk & 1;
-            if (kk + 1 < kBK) {
-                af[cur ^ 1][0] =
-                    *reinterpret_cast<const float4 *>(&As[page][kk + 1][a_col(kk + 1, tm * 4)]);
-                af[cur ^ 1][1] = *reinterpret_cast<const float4 *>(
-                    &As[page][kk + 1][a_col(kk + 1, 64 + tm * 4)]);
-                bf[cur ^ 1][0] = *reinterpret_cast<const float4 *>(&Bs[page][kk + 1][tn * 4]);
-                bf[cur ^ 1][1] = *reinterpret_cast<const float4 *>(&Bs[page][kk + 1][64 + tn * 4]);
-            }
-            const float a[8] = {af[cur][0].x, af[cur][0].y, af[cur][0].z, af[cur][0].w,
-                                af[cur][1].x, af[cur][1].y, af[cur][1].z, af[cur][1].w};
-            const float2 b[4] = {make_float2(bf[cur][0].x, bf[cur][0].y),
-                                 make_float2(bf[cur][0].z, bf[cur][0].w),
-                                 make_float2(bf[cur][1].x, bf[cur][1].y),
-                                 make_float2(bf[cur][1].z, bf[cur][1].w)};
-            if constexpr (kPacked) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float2 ai = make_float2(a[i], a[i]);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) acc[i][j] = __ffma2_rn(ai, b[j], acc[i][j]);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        acc[i][j].x = fmaf(a[i], b[j].x, acc[i][j].x);
-                        acc[i][j].y = fmaf(a[i], b[j].y, acc[i][j].y);
-                    }
-                }
-            }
-        }
-        if (more) {
-            stash_a(page ^ 1);
-            cp_async_wait_all();
-        }
-        __syncthreads();
-    }
-
-    // ---- split-K: last CTA of the tile reduces the partials in order ----
-    if constexpr (kSplit) {
-        const WorkItem w = work_item(p, blockIdx.x);
-        if (w.nsplit > 1) {
-            const int S = w.nsplit;
-            const int split = w.split;
-            const int64_t pid = blockIdx.x;
-            float4 *part = reinterpret_cast<float4 *>(p.partials);
-            // slots of this tile's ranges are consecutive, starting at pid - split
-            const size_t tile_base = size_t(pid - split - p.part_base) * 16 * kThreads;
-            float4 *mine = part + tile_base + size_t(split) * 16 * kThreads;
-            unsigned *counter = p.counters + (w.tile - p.split_base);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int i = j >> 1, h = j & 1;
-                __stcg(mine + j * kThreads + tid,
-                       make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
-                                   acc[i][2 * h + 1].y));
-            }
-            __threadfence();
-            __syncthreads();
-            if (tid == 0) {
-                const unsigned prev = atomicAdd(counter, 1u);
-                s_last = (prev == unsigned(S - 1));
-            }
-            __syncthreads();
-            if (!s_last) return;
-            __threadfence();
-            // every partial, this CTA's own included, is read back from the
-            // workspace (each thread reads only what it wrote itself or what
-            // the fence and ticket made visible), so the sum order is the
-            // same whichever CTA arrives last
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int i = j >> 1, h = j & 1;
-                float4 tot = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                for (int s = 0; s < S; ++s) {
-                    const float4 v =
-                        __ldcg(part + tile_base + size_t(s) * 16 * kThreads + j * kThreads + tid);
-                    tot.x += v.x;
-                    tot.y += v.y;
-                    tot.z += v.z;
-                    tot.w += v.w;
-                }
-                acc[i][2 * h] = make_float2(tot.x, tot.y);
-                acc[i][2 * h + 1] = make_float2(tot.z, tot.w);
-            }
-            if (tid == 0) *counter = 0u;
-        }
-    }
-
-    // ---- epilogue: C = alpha * acc (+ beta * C_old) ----
-    const float alpha = p.alpha, beta = p.beta;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int64_t row = row0 + (i < 4 ? tm * 4 + i : 64 + tm * 4 + (i - 4));
-        if (kEdge && row >= p.M) continue;
-        float *crow = p.C + row * p.ldc;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int64_t col = col0 + h * 64 + tn * 4;
-            float v[4] = {alpha * acc[i][2 * h].x, alpha * acc[i][2 * h].y,
-                          alpha * acc[i][2 * h + 1].x, alpha * acc[i][2 * h + 1].y};
-            float *cp = crow + col;
-            if (!kEdge || (kVec && col + 3 < p.N)) {
-                if (beta != 0.0f) {
-                    const float4 old = *reinterpret_cast<const float4 *>(cp);
-                    v[0] = fmaf(beta, old.x, v[0]);
-                    v[1] = fmaf(beta, old.y, v[1]);
-                    v[2] = fmaf(beta, old.z, v[2]);
-                    v[3] = fmaf(beta, old.w, v[3]);
-                }
-                *reinterpret_cast<float4 *>(cp) = make_float4(v[0], v[1], v[2], v[3]);
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if (col + c < p.N) {
-                        float x = v[c];
-                        if (beta != 0.0f) x = fmaf(beta, cp[c], x);
-                        cp[c] = x;
-                    }
-                }
-            }
-        }
-    }
-}
 
 // C = beta * C over the logical M x N part (beta == 0 stores zeros without
 // reading C).  Used for K == 0 and alpha == 0.
@@ -411,6 +20,24 @@ __global__ void scale_kernel(float *C, int64_t M, int64_t N, int64_t ldc, float 
         const int64_t i = e / N, j = e - i * N;
         float *c = C + i * ldc + j;
         *c = (beta == 0.0f) ? 0.0f : beta * *c;
+    }
+}
+
+// C_b = act(beta * C_b + bias) for the K == 0 / alpha == 0 case of the
+// batched, fused-epilogue call (beta == 0 does not read C).
+__global__ void epilogue_only_kernel(float *C, int64_t M, int64_t N, int64_t ldc,
+                                     int64_t strideC, int64_t batch, float beta,
+                                     const float *bias, int act) {
+    const int64_t per = M * N, total = per * batch;
+    for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+         e += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t b = e / per, r = e - b * per;
+        const int64_t i = r / N, j = r - i * N;
+        float *c = C + b * strideC + i * ldc + j;
+        float v = (beta == 0.0f) ? 0.0f : beta * *c;
+        if (bias) v += bias[j];
+        if (act == kActGeluTanh) v = ffma::gelu_tanh(v);
+        *c = v;
     }
 }
 
@@ -441,36 +68,16 @@ __global__ void __launch_bounds__(256) ffma_probe_kernel(int64_t iters, float *o
     out[int64_t(blockIdx.x) * blockDim.x + threadIdx.x] = s;
 }
 
-template <bool kPacked, bool kVec, bool kEdge, bool kSplit>
-cudaError_t launch_variant(const GemmArgs &a, cudaStream_t stream) {
-    const int64_t tiles = int64_t(a.tiles_m) * a.tiles_n;
-    const dim3 grid(unsigned(a.tail_start * a.split_k + (tiles - a.tail_start) * a.tail_split),
-                    1, 1);
-    ffma_gemm_kernel<kPacked, kVec, kEdge, kSplit><<<grid, kThreads, 0, stream>>>(a);
-    return cudaGetLastError();
-}
-
-template <bool kPacked>
-cudaError_t launch_kind(const GemmArgs &a, bool vec, bool edge, cudaStream_t stream) {
-    const bool split = a.split_k > 1 || a.tail_split > 1;
-    if (!edge) {
-        // full tiles are only planned on the vector path
-        return split ? launch_variant<kPacked, true, false, true>(a, stream)
-                     : launch_variant<kPacked, true, false, false>(a, stream);
-    }
-    if (vec)
-        return split ? launch_variant<kPacked, true, true, true>(a, stream)
-                     : launch_variant<kPacked, true, true, false>(a, stream);
-    return split ? launch_variant<kPacked, false, true, true>(a, stream)
-                 : launch_variant<kPacked, false, true, false>(a, stream);
-}
-
 }  // namespace
 
-cudaError_t launch_ffma(const GemmArgs &a, int kernel, bool vec, bool edge,
-                        cudaStream_t stream) {
-    return kernel == kKernelFfma2x128 ? launch_kind<true>(a, vec, edge, stream)
-                                      : launch_kind<false>(a, vec, edge, stream);
+cudaError_t launch_ffma(const GemmArgs &a, int kernel, bool vec, bool edge, bool trans_a,
+                        bool trans_b, cudaStream_t stream) {
+    if (trans_a) return trans_b ? launch_ffma_tt(a, vec, edge, stream)
+                                : launch_ffma_tn(a, vec, edge, stream);
+    if (trans_b) return launch_ffma_nt(a, vec, edge, stream);
+    return kernel == kKernelFfma2x128
+               ? ffma::launch_layout<true, false, false>(a, vec, edge, stream)
+               : ffma::launch_layout<false, false, false>(a, vec, edge, stream);
 }
 
 cudaError_t launch_scale(float *C, int64_t M, int64_t N, int64_t ldc, float beta,
@@ -480,6 +87,18 @@ cudaError_t launch_scale(float *C, int64_t M, int64_t N, int64_t ldc, float beta
     if (blocks > 4096) blocks = 4096;
     if (blocks < 1) blocks = 1;
     scale_kernel<<<unsigned(blocks), 256, 0, stream>>>(C, M, N, ldc, beta);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_epilogue_only(float *C, int64_t M, int64_t N, int64_t ldc, int64_t strideC,
+                                 int64_t batch, float beta, const float *bias, int act,
+                                 cudaStream_t stream) {
+    const int64_t total = M * N * batch;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    if (blocks < 1) blocks = 1;
+    epilogue_only_kernel<<<unsigned(blocks), 256, 0, stream>>>(C, M, N, ldc, strideC, batch, beta,
+                                                               bias, act);
     return cudaGetLastError();
 }
 
@@ -493,7 +112,8 @@ cudaError_t launch_ffma_probe(int64_t ctas, int64_t iters, bool packed, float *o
 }
 
 cudaError_t ffma_kernel_attributes(cudaFuncAttributes *attr) {
-    return cudaFuncGetAttributes(attr, ffma_gemm_kernel<false, true, false, false>);
+    return cudaFuncGetAttributes(attr,
+                                 ffma::ffma_gemm_kernel<false, true, false, false, false, false>);
 }
 
 }  // namespace sgemm_impl

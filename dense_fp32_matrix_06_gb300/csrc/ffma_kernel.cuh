@@ -1,0 +1,509 @@
+// ffma_kernel.cuh -- the fp32 CUDA-core GEMM kernel for sm_103a (template).
+//
+// C_b = act(alpha * op(A_b) * op(B_b) + beta * C_b + bias), row-major, any
+// M, N, K, for b in [0, batch); op(X) is X or X^T (the stored matrix read
+// transposed).  The plain case (batch 1, no transposes, no bias/act) is the
+// method's product C = alpha*A*B + beta*C.
+//
+// Design (prior art on the pages, re-derived for a 152-SM Blackwell part):
+//  * CTA tile 128 x 128, K slice 16, 256 threads, 8 x 8 accumulators per
+//    thread updated as outer products: for every k the thread reads 8 values
+//    of column k of the A tile and 8 of row k of the B tile and does 64 FMAs
+//    (velog @levelstage "AutoMinepp4", section "행렬곱: by 벡터의 외적": the
+//    product is a sum of outer products, which keeps the accumulators in
+//    registers; "Micro_gemm_4x4 - cuBLAS micro GEMM skeleton", section 8:
+//    the fully unrolled FMA pattern over the micro tile).
+//  * Two issue forms of the same arithmetic: scalar fma.rn.f32 (the
+//    default) or packed fma.rn.f32x2, each lane of which is an ordinary
+//    round-to-nearest fp32 FMA, so every accumulator sees exactly the same
+//    sequence of roundings either way and the two give bit-identical C.
+//    Measured on GB300 the packed form is slower: it holds the FMA pipe two
+//    cycles, so it saves issue slots but not pipe time, and the broadcast
+//    operand pairs push the kernel past its 128-register budget.
+//  * The 8 x 8 block is split into four 4 x 4 quadrants 64 rows / 64 columns
+//    apart, so one 128-bit shared load serves 4 rows (or columns) and the
+//    loads of a warp are conflict-free: a warp reads 4 distinct 16-byte A
+//    chunks (each broadcast to 8 lanes) and 8 distinct B chunks.
+//  * The smem tiles are k-major: As[k][m], Bs[k][n].  An operand whose
+//    stored rows run along M (A^T) or N (B) is copied straight into them
+//    with 16-byte cp.async.  An operand whose stored rows run along K (A, or
+//    B^T) is staged through registers: a warp loads 8 rows x 16 k with
+//    128-bit loads and scatters them into the tile with an XOR swizzle that
+//    keeps the stores conflict-free (velog @levelstage "AutoMinepp7",
+//    section "직사각형 타일링": chunks are fetched into registers before the
+//    compute and split into the other local-memory page after it).
+//  * Two smem pages: slice t+1 is in flight (registers and async copies)
+//    while slice t is computed; one barrier per K slice ("Micro_gemm_4x4 -
+//    cuBLAS micro GEMM skeleton", section 8, double buffering, with the
+//    asynchronous copy the page suggests for Ampere and later).  Shared-
+//    memory fragments are double-buffered in registers across the 16 k steps.
+//  * Edges: out-of-range A/B elements load as 0 and C stores are predicated
+//    on row < M, col < N ("Micro_gemm_4x4 ...", sections 6 and 9; "GPU
+//    Target", section "타일링된 행렬 곱셈": out-of-range loads read as zero).
+//  * Epilogue: c = alpha * acc, then c = fma(beta, C_old, c) only when
+//    beta != 0 (C is not read otherwise), then + bias[col] and the tanh
+//    GELU when asked ("GPU Target", GPT-2 sublayers: x @ W + b, then the
+//    outlined GELU kernel), stored with 128-bit stores.
+//  * Batches are an outer index of the tile grid ("GPU Target", section
+//    "타일링된 행렬 곱셈": the batched variant adds a grid dimension indexed
+//    by batch, used per attention head).
+//  * Split-K: when the tile grid cannot fill the GPU, K is cut into split_k
+//    ranges (and, opt-in, only the tiles of a partly filled last wave into
+//    tail_split ranges).  Every CTA of a split tile writes its partial tile
+//    to the workspace; the last CTA of the tile to arrive (atomic ticket, no
+//    waiting) sums all partials in ascending split order and runs the
+//    epilogue, then rearms the counter.  The sum order is fixed, so results
+//    are deterministic run to run.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "sgemm_internal.h"
+
+namespace sgemm_impl {
+namespace ffma {
+
+__device__ __forceinline__ float4 ldg4(const float *p) {
+    return __ldg(reinterpret_cast<const float4 *>(p));
+}
+
+__device__ __forceinline__ float ldg1(const float *p) { return __ldg(p); }
+
+__device__ __forceinline__ unsigned smem_addr(const void *p) {
+    return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte async copy global -> shared; bytes past `src_bytes` are zero-filled
+// and not read.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_addr(dst)),
+                 "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+// 4-byte async copy; src_bytes == 0 writes a zero without reading.
+__device__ __forceinline__ void cp_async4(void *dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(smem_addr(dst)),
+                 "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
+}
+
+// Column of tile element (k, x) inside its smem row.  For a tile filled by
+// transposing register stores, bits 3..4 of x are XOR-ed with k/4: every
+// aligned group of 4 columns stays contiguous (fragment reads stay 128-bit)
+// and the stores of a warp -- 8 rows x 4 k groups -- hit all 32 banks.  A tile
+// filled by row copies needs no swizzle.
+template <bool kSwizzle>
+__device__ __forceinline__ int tcol(int k, int x) {
+    if constexpr (kSwizzle)
+        return x ^ (((k >> 2) & 3) << 3);
+    else
+        return x;
+}
+
+// The tanh form of GELU used by GPT-2: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+__device__ __forceinline__ float gelu_tanh(float x) {
+    const float k0 = 0.7978845608028654f;   // sqrt(2/pi)
+    const float u = k0 * fmaf(0.044715f * x, x * x, x);
+    return 0.5f * x * (1.0f + tanhf(u));
+}
+
+// The (batch, tile, K range) CTA `pid` computes, and the tile's coordinates.
+struct WorkItem {
+    int64_t tile;   // global tile id over all batches
+    int64_t batch;
+    int64_t row0, col0;
+    int64_t kbeg, kend;
+    int split, nsplit;
+};
+
+__device__ __forceinline__ WorkItem work_item(const GemmArgs &p, int64_t pid) {
+    WorkItem w;
+    const int64_t lead = p.tail_start * p.split_k;
+    int64_t kps;
+    if (pid < lead) {
+        w.tile = pid / p.split_k;
+        w.split = int(pid - w.tile * p.split_k);
+        w.nsplit = p.split_k;
+        kps = p.k_per_split;
+    } else {
+        const int64_t j = pid - lead;
+        w.tile = p.tail_start + j / p.tail_split;
+        w.split = int(j % p.tail_split);
+        w.nsplit = p.tail_split;
+        kps = p.tail_k_per_split;
+    }
+    const int64_t per_batch = int64_t(p.tiles_m) * p.tiles_n;
+    w.batch = w.tile / per_batch;
+    const int64_t t = w.tile - w.batch * per_batch;
+    // grouped raster over kGroupM tile rows (L2 reuse of A and B panels)
+    const int64_t per_group = int64_t(kGroupM) * p.tiles_n;
+    const int64_t group = t / per_group;
+    const int64_t first_m = group * kGroupM;
+    const int64_t gm = min(int64_t(p.tiles_m) - first_m, int64_t(kGroupM));
+    const int64_t in_group = t - group * per_group;
+    w.row0 = (first_m + in_group % gm) * kBM;
+    w.col0 = (in_group / gm) * kBN;
+    w.kbeg = int64_t(w.split) * kps;
+    w.kend = min(p.K, w.kbeg + kps);
+    return w;
+}
+
+template <bool kPacked, bool kVec, bool kEdge, bool kSplit, bool kTransA, bool kTransB>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+ffma_gemm_kernel(const GemmArgs p) {
+    // A tile: As[k][m]; swizzled when filled by transposing stores (A not transposed)
+    // B tile: Bs[k][n]; swizzled when filled by transposing stores (B transposed)
+    constexpr bool kSwzA = !kTransA;
+    constexpr bool kSwzB = kTransB;
+    __shared__ __align__(16) float As[2][kBK][kBM];
+    __shared__ __align__(16) float Bs[2][kBK][kBN];
+    __shared__ int s_last;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+
+    // ---- (batch, tile, K range) of this CTA; recomputed after the main loop
+    // so none of it stays live in registers across it ----
+    int64_t row0, col0, kbeg, kend;
+    const float *Ab;
+    const float *Bb;
+    {
+        const WorkItem w = work_item(p, blockIdx.x);
+        row0 = w.row0;
+        col0 = w.col0;
+        kbeg = w.kbeg;
+        kend = w.kend;
+        Ab = p.A + w.batch * p.strideA;
+        Bb = p.B + w.batch * p.strideB;
+    }
+    const int nslices = kend > kbeg ? int((kend - kbeg + kBK - 1) / kBK) : 0;
+
+    // ---- compute mapping: warp = 4 (M) x 8 (N) threads ----
+    const int tm = (warp >> 1) * 4 + (lane >> 3);   // 0..15
+    const int tn = (warp & 1) * 8 + (lane & 7);     // 0..15
+
+    // ---- load mapping ----
+    // transposing operand (rows along K): rows r and r + 64 of the tile, k group
+    // kc (4 consecutive k): a warp reads 8 rows x 64 contiguous bytes per load.
+    const int t_row = tid >> 2;              // 0..63
+    const int t_kc = tid & 3;                // 0..3
+    // copied operand (rows along M or N): tile rows k and k + 8, 4 elements at
+    // c_col: a warp copies one 512-byte row segment.
+    const int c_row = tid >> 5;              // 0..7
+    const int c_col = (tid & 31) * 4;        // 0..124
+
+    // A
+    bool a_ok[2];
+    const float *a_ptr[2];
+    if constexpr (!kTransA) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t r = row0 + t_row + 64 * h;
+            a_ok[h] = !kEdge || r < p.M;
+            a_ptr[h] = Ab + (a_ok[h] ? r : 0) * p.lda + kbeg + t_kc * 4;
+        }
+    } else {
+        a_ok[0] = a_ok[1] = true;
+        a_ptr[0] = Ab + (kbeg + c_row) * p.lda + row0 + c_col;
+        a_ptr[1] = a_ptr[0];
+    }
+    // B
+    bool b_ok[2];
+    const float *b_ptr[2];
+    if constexpr (kTransB) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t n = col0 + t_row + 64 * h;
+            b_ok[h] = !kEdge || n < p.N;
+            b_ptr[h] = Bb + (b_ok[h] ? n : 0) * p.ldb + kbeg + t_kc * 4;
+        }
+    } else {
+        b_ok[0] = b_ok[1] = true;
+        b_ptr[0] = Bb + (kbeg + c_row) * p.ldb + col0 + c_col;
+        b_ptr[1] = b_ptr[0];
+    }
+
+    float4 ra[2], rb[2];
+
+    // rows along K -> registers (zero outside the matrix and outside [kbeg, kend))
+    auto fetch_t = [&](int t, const bool (&ok)[2], const float *const (&ptr)[2], float4 (&r)[2]) {
+        const int64_t koff = int64_t(t) * kBK;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float *src = ptr[h] + koff;
+            if constexpr (!kEdge) {
+                r[h] = ldg4(src);
+            } else {
+                const int64_t k = kbeg + koff + t_kc * 4;
+                if (kVec && ok[h] && k + 3 < kend) {
+                    r[h] = ldg4(src);
+                } else {
+                    r[h].x = (ok[h] && k + 0 < kend) ? ldg1(src + 0) : 0.0f;
+                    r[h].y = (ok[h] && k + 1 < kend) ? ldg1(src + 1) : 0.0f;
+                    r[h].z = (ok[h] && k + 2 < kend) ? ldg1(src + 2) : 0.0f;
+                    r[h].w = (ok[h] && k + 3 < kend) ? ldg1(src + 3) : 0.0f;
+                }
+            }
+        }
+    };
+    // registers -> tile rows k..k+3, transposed and swizzled
+    auto stash_t = [&](float (*T)[kBM], const float4 (&r)[2]) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int x = t_row + 64 * h;
+            const int k = t_kc * 4;
+            T[k + 0][tcol<true>(k, x)] = r[h].x;
+            T[k + 1][tcol<true>(k, x)] = r[h].y;
+            T[k + 2][tcol<true>(k, x)] = r[h].z;
+            T[k + 3][tcol<true>(k, x)] = r[h].w;
+        }
+    };
+    // rows along M/N -> tile, async copies (zero-filled outside); `lim` is M or N
+    auto copy_c = [&](int t, float (*T)[kBM], const float *base, int64_t ld, int64_t x0,
+                      int64_t lim, const float *dummy) {
+        const int64_t koff = int64_t(t) * kBK;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float *src = base + (koff + 8 * h) * ld;
+            float *dst = &T[c_row + 8 * h][c_col];
+            if constexpr (!kEdge) {
+                cp_async16(dst, src, 16);
+            } else {
+                const int64_t k = kbeg + koff + c_row + 8 * h;
+                const int64_t c = x0 + c_col;
+                const bool k_ok = k < kend;
+                if constexpr (kVec) {
+                    int64_t n = k_ok ? lim - c : 0;
+                    n = n < 0 ? 0 : (n > 4 ? 4 : n);
+                    cp_async16(dst, n > 0 ? src : dummy, int(n) * 4);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const bool ok = k_ok && c + e < lim;
+                        cp_async4(dst + e, ok ? src + e : dummy, ok ? 4 : 0);
+                    }
+                }
+            }
+        }
+    };
+
+    auto issue = [&](int t, int page) {
+        if constexpr (kTransA) copy_c(t, As[page], a_ptr[0], p.lda, row0, p.M, p.A);
+        if constexpr (!kTransB) copy_c(t, Bs[page], b_ptr[0], p.ldb, col0, p.N, p.B);
+        cp_async_commit();
+        if constexpr (!kTransA) fetch_t(t, a_ok, a_ptr, ra);
+        if constexpr (kTransB) fetch_t(t, b_ok, b_ptr, rb);
+    };
+    auto land = [&](int page) {
+        if constexpr (!kTransA) stash_t(As[page], ra);
+        if constexpr (kTransB) stash_t(Bs[page], rb);
+        cp_async_wait_all();
+    };
+
+    float2 acc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
+
+    if (nslices > 0) {
+        issue(0, 0);
+        land(0);
+    }
+    __syncthreads();
+
+    for (int t = 0; t < nslices; ++t) {
+        const int page = t & 1;
+        const bool more = t + 1 < nslices;
+        if (more) issue(t + 1, page ^ 1);
+
+        float4 af[2][2], bf[2][2];
+        af[0][0] = *reinterpret_cast<const float4 *>(&As[page][0][tcol<kSwzA>(0, tm * 4)]);
+        af[0][1] = *reinterpret_cast<const float4 *>(&As[page][0][tcol<kSwzA>(0, 64 + tm * 4)]);
+        bf[0][0] = *reinterpret_cast<const float4 *>(&Bs[page][0][tcol<kSwzB>(0, tn * 4)]);
+        bf[0][1] = *reinterpret_cast<const float4 *>(&Bs[page][0][tcol<kSwzB>(0, 64 + tn * 4)]);
+#pragma unroll
+        for (int kk = 0; kk < kBK; ++kk) {
+            const int cur = kk & 1;
+            if (kk + 1 < kBK) {
+                af[cur ^ 1][0] = *reinterpret_cast<const float4 *>(
+                    &As[page][kk + 1][tcol<kSwzA>(kk + 1, tm * 4)]);
+                af[cur ^ 1][1] = *reinterpret_cast<const float4 *>(
+                    &As[page][kk + 1][tcol<kSwzA>(kk + 1, 64 + tm * 4)]);
+                bf[cur ^ 1][0] = *reinterpret_cast<const float4 *>(
+                    &Bs[page][kk + 1][tcol<kSwzB>(kk + 1, tn * 4)]);
+                bf[cur ^ 1][1] = *reinterpret_cast<const float4 *>(
+                    &Bs[page][kk + 1][tcol<kSwzB>(kk + 1, 64 + tn * 4)]);
+            }
+            const float a[8] = {af[cur][0].x, af[cur][0].y, af[cur][0].z, af[cur][0].w,
+                                af[cur][1].x, af[cur][1].y, af[cur][1].z, af[cur][1].w};
+            const float2 b[4] = {make_float2(bf[cur][0].x, bf[cur][0].y),
+                                 make_float2(bf[cur][0].z, bf[cur][0].w),
+                                 make_float2(bf[cur][1].x, bf[cur][1].y),
+                                 make_float2(bf[cur][1].z, bf[cur][1].w)};
+            if constexpr (kPacked) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float2 ai = make_float2(a[i], a[i]);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[i][j] = __ffma2_rn(ai, b[j], acc[i][j]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        acc[i][j].x = fmaf(a[i], b[j].x, acc[i][j].x);
+                        acc[i][j].y = fmaf(a[i], b[j].y, acc[i][j].y);
+                    }
+                }
+            }
+        }
+        if (more) land(page ^ 1);
+        __syncthreads();
+    }
+
+    // ---- split-K: last CTA of the tile reduces the partials in order ----
+    if constexpr (kSplit) {
+        const WorkItem w = work_item(p, blockIdx.x);
+        if (w.nsplit > 1) {
+            const int S = w.nsplit;
+            const int split = w.split;
+            const int64_t pid = blockIdx.x;
+            float4 *part = reinterpret_cast<float4 *>(p.partials);
+            // slots of this tile's ranges are consecutive, starting at pid - split
+            const size_t tile_base = size_t(pid - split - p.part_base) * 16 * kThreads;
+            float4 *mine = part + tile_base + size_t(split) * 16 * kThreads;
+            unsigned *counter = p.counters + (w.tile - p.split_base);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int i = j >> 1, h = j & 1;
+                __stcg(mine + j * kThreads + tid,
+                       make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
+                                   acc[i][2 * h + 1].y));
+            }
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) {
+                const unsigned prev = atomicAdd(counter, 1u);
+                s_last = (prev == unsigned(S - 1));
+            }
+            __syncthreads();
+            if (!s_last) return;
+            __threadfence();
+            // every partial, this CTA's own included, is read back from the
+            // workspace (each thread reads only what it wrote itself or what
+            // the fence and ticket made visible), so the sum order is the
+            // same whichever CTA arrives last
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int i = j >> 1, h = j & 1;
+                float4 tot = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                for (int s = 0; s < S; ++s) {
+                    const float4 v =
+                        __ldcg(part + tile_base + size_t(s) * 16 * kThreads + j * kThreads + tid);
+                    tot.x += v.x;
+                    tot.y += v.y;
+                    tot.z += v.z;
+                    tot.w += v.w;
+                }
+                acc[i][2 * h] = make_float2(tot.x, tot.y);
+                acc[i][2 * h + 1] = make_float2(tot.z, tot.w);
+            }
+            if (tid == 0) *counter = 0u;
+        }
+    }
+
+    // ---- epilogue: C = act(alpha * acc (+ beta * C_old) (+ bias)) ----
+    const float alpha = p.alpha, beta = p.beta;
+    float *Cb = p.C;
+    if (p.batch > 1) Cb += work_item(p, blockIdx.x).batch * p.strideC;
+    const float *bias = p.bias;
+    const int act = p.act;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t row = row0 + (i < 4 ? tm * 4 + i : 64 + tm * 4 + (i - 4));
+        if (kEdge && row >= p.M) continue;
+        float *crow = Cb + row * p.ldc;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t col = col0 + h * 64 + tn * 4;
+            float v[4] = {alpha * acc[i][2 * h].x, alpha * acc[i][2 * h].y,
+                          alpha * acc[i][2 * h + 1].x, alpha * acc[i][2 * h + 1].y};
+            float *cp = crow + col;
+            if (!kEdge || (kVec && col + 3 < p.N)) {
+                if (beta != 0.0f) {
+                    const float4 old = *reinterpret_cast<const float4 *>(cp);
+                    v[0] = fmaf(beta, old.x, v[0]);
+                    v[1] = fmaf(beta, old.y, v[1]);
+                    v[2] = fmaf(beta, old.z, v[2]);
+                    v[3] = fmaf(beta, old.w, v[3]);
+                }
+                if (bias) {
+                    const float4 bv = *reinterpret_cast<const float4 *>(bias + col);
+                    v[0] += bv.x;
+                    v[1] += bv.y;
+                    v[2] += bv.z;
+                    v[3] += bv.w;
+                }
+                if (act == kActGeluTanh) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) v[c] = gelu_tanh(v[c]);
+                }
+                *reinterpret_cast<float4 *>(cp) = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (col + c < p.N) {
+                        float x = v[c];
+                        if (beta != 0.0f) x = fmaf(beta, cp[c], x);
+                        if (bias) x += bias[col + c];
+                        if (act == kActGeluTanh) x = gelu_tanh(x);
+                        cp[c] = x;
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <bool kPacked, bool kVec, bool kEdge, bool kSplit, bool kTransA, bool kTransB>
+cudaError_t launch_variant(const GemmArgs &a, cudaStream_t stream) {
+    const int64_t tiles = int64_t(a.tiles_m) * a.tiles_n * a.batch;
+    const dim3 grid(unsigned(a.tail_start * a.split_k + (tiles - a.tail_start) * a.tail_split),
+                    1, 1);
+    ffma_gemm_kernel<kPacked, kVec, kEdge, kSplit, kTransA, kTransB>
+        <<<grid, kThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+// All (vec, edge, split) variants of one layout and issue form.
+template <bool kPacked, bool kTransA, bool kTransB>
+cudaError_t launch_layout(const GemmArgs &a, bool vec, bool edge, cudaStream_t stream) {
+    const bool split = a.split_k > 1 || a.tail_split > 1;
+    if (!edge) {
+        // full tiles are only planned on the vector path
+        return split ? launch_variant<kPacked, true, false, true, kTransA, kTransB>(a, stream)
+                     : launch_variant<kPacked, true, false, false, kTransA, kTransB>(a, stream);
+    }
+    if (vec)
+        return split ? launch_variant<kPacked, true, true, true, kTransA, kTransB>(a, stream)
+                     : launch_variant<kPacked, true, true, false, kTransA, kTransB>(a, stream);
+    return split ? launch_variant<kPacked, false, true, true, kTransA, kTransB>(a, stream)
+                 : launch_variant<kPacked, false, true, false, kTransA, kTransB>(a, stream);
+}
+
+}  // namespace ffma
+}  // namespace sgemm_impl

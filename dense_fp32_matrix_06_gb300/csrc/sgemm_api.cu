@@ -11,6 +11,7 @@
 
 #include <cstdint>
 #include <cstdlib>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -164,9 +165,10 @@ int32_t default_kernel() {
     return kKernelFfma128;
 }
 
-sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
-                       int64_t ldc, const void *A, const void *B, const void *C,
-                       int sms, gemm_plan_t *out) {
+// Tiling and split choice for `batch` problems of M x N x K; `vec` says
+// whether 16-byte vector access is legal for every operand.
+void plan_core(int64_t M, int64_t N, int64_t K, int64_t batch, bool vec, int sms,
+               gemm_plan_t *out) {
     gemm_plan_t p;
     std::memset(&p, 0, sizeof(p));
     p.mode = SGEMM_MODE_FFMA;
@@ -175,19 +177,17 @@ sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb
     p.bn = kBN;
     p.bk = kBK;
     p.threads = kThreads;
-    p.vec = (lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0 && aligned16(A) && aligned16(B) &&
-             aligned16(C))
-                ? 1
-                : 0;
+    p.vec = vec ? 1 : 0;
     p.tiles_m = ceil_div(M, kBM);
     p.tiles_n = ceil_div(N, kBN);
-    const int64_t tiles = p.tiles_m * p.tiles_n;
+    const int64_t tiles = p.tiles_m * p.tiles_n * batch;
     int64_t kps = 0;
-    p.split_k = (M > 0 && N > 0 && K > 0) ? choose_split(tiles, K, sms, &kps) : 1;
-    p.k_per_split = kps;
+    p.split_k = (M > 0 && N > 0 && K > 0 && batch > 0) ? choose_split(tiles, K, sms, &kps) : 1;
+    if (p.split_k == 1) kps = ceil_div(K, kBK) * kBK;
+    p.k_per_split = kps > 0 ? kps : kBK;
     int tail_split = 1;
     p.tail_start = tiles;
-    p.tail_k_per_split = kps;
+    p.tail_k_per_split = p.k_per_split;
     if (p.split_k == 1 && M > 0 && N > 0 && K > 0)
         choose_tail(tiles, K, sms, &p.tail_start, &tail_split, &p.tail_k_per_split);
     p.tail_split = tail_split;
@@ -198,6 +198,14 @@ sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb
     p.grid_ctas = p.tail_start * p.split_k + (tiles - p.tail_start) * p.tail_split;
     p.workspace_bytes = split_workspace(tiles, p.split_k, p.tail_start, p.tail_split);
     *out = p;
+}
+
+sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                       int64_t ldc, const void *A, const void *B, const void *C,
+                       int sms, gemm_plan_t *out) {
+    const bool vec = lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0 && aligned16(A) &&
+                     aligned16(B) && aligned16(C);
+    plan_core(M, N, K, 1, vec, sms, out);
     return SGEMM_OK;
 }
 
@@ -262,6 +270,10 @@ sgemm_status run(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K, float
     a.ldc = ldc;
     a.alpha = alpha;
     a.beta = beta;
+    a.batch = 1;
+    a.strideA = a.strideB = a.strideC = 0;
+    a.bias = nullptr;
+    a.act = kActNone;
     a.k_per_split = plan.k_per_split;
     a.tail_k_per_split = plan.tail_k_per_split;
     a.tail_start = plan.tail_start;
@@ -277,7 +289,7 @@ sgemm_status run(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K, float
         a.counters = static_cast<unsigned *>(workspace);
         a.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + kCounterBytes);
     }
-    e = launch_ffma(a, plan.kernel, plan.vec != 0, plan.edge != 0, stream);
+    e = launch_ffma(a, plan.kernel, plan.vec != 0, plan.edge != 0, false, false, stream);
     return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
 }
 
@@ -536,4 +548,87 @@ extern "C" sgemm_status sgemm_tf32x3_stall_selftest(int64_t M, int64_t N, int64_
                    stream);
     if (s != SGEMM_OK) return s;
     return sgemm_device_status(stream);
+}
+
+// ---------------------------------------------------------------------------
+// sgemm_ex: batched, transposed-operand, fused bias/GELU form of the product
+// ---------------------------------------------------------------------------
+
+extern "C" sgemm_status sgemm_ex(int32_t op_a, int32_t op_b, int64_t M, int64_t N, int64_t K,
+                                 float alpha, const float *A, int64_t lda, int64_t stride_a,
+                                 const float *B, int64_t ldb, int64_t stride_b, float beta,
+                                 float *C, int64_t ldc, int64_t stride_c, int64_t batch,
+                                 const float *bias, int32_t act, void *stream) {
+    if (op_a != SGEMM_OP_N && op_a != SGEMM_OP_T) return SGEMM_ERR_INVALID_ARG;
+    if (op_b != SGEMM_OP_N && op_b != SGEMM_OP_T) return SGEMM_ERR_INVALID_ARG;
+    if (act != SGEMM_ACT_NONE && act != SGEMM_ACT_GELU_TANH) return SGEMM_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0 || batch < 0) return SGEMM_ERR_INVALID_ARG;
+    const bool ta = op_a == SGEMM_OP_T, tb = op_b == SGEMM_OP_T;
+    // leading dimension >= the stored row length
+    if (lda < std::max<int64_t>(1, ta ? M : K)) return SGEMM_ERR_INVALID_ARG;
+    if (ldb < std::max<int64_t>(1, tb ? K : N)) return SGEMM_ERR_INVALID_ARG;
+    if (ldc < std::max<int64_t>(1, N)) return SGEMM_ERR_INVALID_ARG;
+    if (stride_a < 0 || stride_b < 0 || stride_c < 0) return SGEMM_ERR_INVALID_ARG;
+    // the outputs of different batches may not overlap
+    if (batch > 1 && stride_c < (M > 0 ? (M - 1) * ldc + N : 0)) return SGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0 || batch == 0) return SGEMM_OK;
+    if (ceil_div(M, kBM) * ceil_div(N, kBN) > int64_t(INT32_MAX) / batch)
+        return SGEMM_ERR_INVALID_ARG;
+    if (!C) return SGEMM_ERR_INVALID_ARG;
+    if (K > 0 && alpha != 0.0f && (!A || !B)) return SGEMM_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    sgemm_status s = current_device(&dev, &sms);
+    if (s != SGEMM_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (K == 0 || alpha == 0.0f) {
+        e = launch_epilogue_only(C, M, N, ldc, stride_c, batch, beta, bias, act, st);
+        return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
+    }
+    const bool vec = lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0 && stride_a % 4 == 0 &&
+                     stride_b % 4 == 0 && stride_c % 4 == 0 && aligned16(A) && aligned16(B) &&
+                     aligned16(C) && aligned16(bias);
+    gemm_plan_t plan;
+    plan_core(M, N, K, batch, vec, sms, &plan);
+    if (ta || tb) plan.kernel = kKernelFfma128;   // the packed form exists for op N, N only
+    void *ws = nullptr;
+    if (plan.workspace_bytes > 0) {
+        s = library_workspace(dev, st, plan.workspace_bytes, &ws);
+        if (s != SGEMM_OK) return s;
+    }
+    GemmArgs a;
+    a.A = A;
+    a.B = B;
+    a.C = C;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.lda = lda;
+    a.ldb = ldb;
+    a.ldc = ldc;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.batch = batch;
+    a.strideA = stride_a;
+    a.strideB = stride_b;
+    a.strideC = stride_c;
+    a.bias = bias;
+    a.act = act;
+    a.k_per_split = plan.k_per_split;
+    a.tail_k_per_split = plan.tail_k_per_split;
+    a.tail_start = plan.tail_start;
+    a.split_k = plan.split_k;
+    a.tail_split = plan.tail_split;
+    a.tiles_m = int32_t(plan.tiles_m);
+    a.tiles_n = int32_t(plan.tiles_n);
+    a.split_base = plan.split_k > 1 ? 0 : plan.tail_start;
+    a.part_base = plan.split_k > 1 ? 0 : plan.tail_start;
+    a.counters = nullptr;
+    a.partials = nullptr;
+    if (plan.workspace_bytes > 0) {
+        a.counters = static_cast<unsigned *>(ws);
+        a.partials = reinterpret_cast<float *>(static_cast<char *>(ws) + kCounterBytes);
+    }
+    e = launch_ffma(a, plan.kernel, plan.vec != 0, plan.edge != 0, ta, tb, st);
+    return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
 }

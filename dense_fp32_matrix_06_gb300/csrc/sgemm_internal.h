@@ -25,6 +25,10 @@ constexpr size_t kCounterBytes = 16384;
 constexpr int64_t kMaxSplitTiles = kCounterBytes / sizeof(unsigned);
 constexpr int kMaxSplit = 32;
 
+// Epilogue activations.
+constexpr int kActNone = 0;
+constexpr int kActGeluTanh = 1;
+
 // Everything a GEMM launch needs, by value.
 struct GemmArgs {
     const float *A;
@@ -33,6 +37,11 @@ struct GemmArgs {
     int64_t M, N, K;
     int64_t lda, ldb, ldc;
     float alpha, beta;
+    // batch b reads A + b*strideA, B + b*strideB and writes C + b*strideC
+    int64_t batch;
+    int64_t strideA, strideB, strideC;
+    const float *bias;     // length-N vector added to every row, or nullptr
+    int32_t act;           // kActNone or kActGeluTanh
     // Work decomposition.  Tiles [0, tail_start) are cut into split_k K ranges
     // of k_per_split each; tiles [tail_start, tiles) into tail_split ranges of
     // tail_k_per_split.  CTA `pid` of the 1-D grid owns one (tile, range)
@@ -43,6 +52,7 @@ struct GemmArgs {
     int32_t split_k;
     int32_t tail_split;
     int32_t tiles_m, tiles_n;
+    // Tiles are numbered over all batches (batch-major).
     // Split tiles only: counter of tile t is counters[t - split_base], partial
     // of CTA pid is slot pid - part_base (16 x kThreads float4 per slot).
     int64_t split_base;
@@ -60,10 +70,18 @@ enum KernelId : int32_t {
     kKernelFfma2x128 = 1,  // packed fma.rn.f32x2 (two FMAs per instruction)
 };
 
-cudaError_t launch_ffma(const GemmArgs &a, int kernel, bool vec, bool edge,
-                        cudaStream_t stream);
+// op(A) = A^T when trans_a (A stored K x M), op(B) = B^T when trans_b.
+cudaError_t launch_ffma(const GemmArgs &a, int kernel, bool vec, bool edge, bool trans_a,
+                        bool trans_b, cudaStream_t stream);
+// the transposed layouts, one translation unit each
+cudaError_t launch_ffma_nt(const GemmArgs &a, bool vec, bool edge, cudaStream_t stream);
+cudaError_t launch_ffma_tn(const GemmArgs &a, bool vec, bool edge, cudaStream_t stream);
+cudaError_t launch_ffma_tt(const GemmArgs &a, bool vec, bool edge, cudaStream_t stream);
 cudaError_t launch_scale(float *C, int64_t M, int64_t N, int64_t ldc, float beta,
                          cudaStream_t stream);
+cudaError_t launch_epilogue_only(float *C, int64_t M, int64_t N, int64_t ldc, int64_t strideC,
+                                 int64_t batch, float beta, const float *bias, int act,
+                                 cudaStream_t stream);
 cudaError_t launch_ffma_probe(int64_t ctas, int64_t iters, bool packed, float *out,
                               cudaStream_t stream);
 cudaError_t ffma_kernel_attributes(cudaFuncAttributes *attr);

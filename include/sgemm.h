@@ -68,6 +68,16 @@ typedef enum {
     SGEMM_MODE_TF32X3 = 1   /* 3xTF32 split precision on the tensor cores (sgemm_tf32x3) */
 } sgemm_mode;
 
+/* Operand forms of sgemm_ex: op(X) = X, or X^T (the stored matrix read
+ * transposed). */
+typedef enum { SGEMM_OP_N = 0, SGEMM_OP_T = 1 } sgemm_op;
+
+/* Activations of sgemm_ex's fused epilogue. */
+typedef enum {
+    SGEMM_ACT_NONE = 0,
+    SGEMM_ACT_GELU_TANH = 1  /* 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) */
+} sgemm_act;
+
 /* Size of the tile-counter block at the start of a split-K workspace. */
 #define SGEMM_WORKSPACE_COUNTER_BYTES 16384
 
@@ -227,6 +237,39 @@ sgemm_status sgemm_tf32x3_stall_selftest(int64_t M, int64_t N, int64_t K,
                                          const float *A, int64_t lda, const float *B,
                                          int64_t ldb, float *C, int64_t ldc,
                                          int64_t limit_us, void *stream);
+
+/*
+ * sgemm_ex -- the general form: for b in [0, batch)
+ *
+ *     C_b = act(alpha * op(A_b) * op(B_b) + beta * C_b + bias)
+ *
+ * with A_b = A + b*stride_a, B_b = B + b*stride_b, C_b = C + b*stride_c
+ * (strides in elements), op(A_b) M x K, op(B_b) K x N, C_b M x N.
+ *   - op_a == SGEMM_OP_N: A_b is M x K row-major, lda >= max(1, K);
+ *     op_a == SGEMM_OP_T: A_b is stored K x M row-major, lda >= max(1, M),
+ *     and read transposed.  Likewise B: N -> K x N, ldb >= max(1, N);
+ *     T -> stored N x K, ldb >= max(1, K).
+ *   - bias: NULL, or a device vector of N floats added to every row of C
+ *     after the beta term; act: SGEMM_ACT_NONE or SGEMM_ACT_GELU_TANH,
+ *     applied last (both as in a GPT-2 projection, x @ W + b, and its MLP's
+ *     tanh GELU: "GPU Target" (MLIR tutorial), GPT-2 sublayers and the
+ *     outlined GELU kernel).
+ *   - batch: the per-head batch dimension of the MLIR page's batched
+ *     matmul ("타일링된 행렬 곱셈"); stride_a or stride_b may be 0 (one
+ *     operand shared by every batch); the batches of C may not overlap
+ *     (stride_c >= (M-1)*ldc + N when batch > 1).
+ * With batch = 1, op N/N, bias NULL and act NONE this is exactly sgemm.
+ * K == 0 or alpha == 0 gives C = act(beta*C + bias) without reading A or B.
+ * Same conventions as sgemm otherwise (device pointers, asynchronous on
+ * `stream`, beta == 0 does not read C, padding columns untouched, library
+ * workspace for split-K).  Returns SGEMM_ERR_INVALID_ARG for a bad op, act,
+ * size, leading dimension, stride or pointer.
+ */
+sgemm_status sgemm_ex(int32_t op_a, int32_t op_b, int64_t M, int64_t N, int64_t K,
+                      float alpha, const float *A, int64_t lda, int64_t stride_a,
+                      const float *B, int64_t ldb, int64_t stride_b, float beta, float *C,
+                      int64_t ldc, int64_t stride_c, int64_t batch, const float *bias,
+                      int32_t act, void *stream);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char *sgemm_status_string(sgemm_status status);

@@ -42,7 +42,7 @@ def build(force: bool = False) -> str:
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
-           "-shared", "-fPIC", "-std=c11", _SRC, "-o", tmp]
+           "-shared", "-fPIC", "-std=c11", _SRC, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
     return _LIB
@@ -62,6 +62,11 @@ def _load():
             lib.oracle_sgemm_rows.restype = ctypes.c_int
             lib.oracle_sgemm_entries.argtypes = common + [_i64p, _i64p, _i64, _f32p]
             lib.oracle_sgemm_entries.restype = ctypes.c_int
+            lib.oracle_sgemm_ex.argtypes = [ctypes.c_int, ctypes.c_int, _i64, _i64, _i64,
+                                            ctypes.c_float, _f32p, _i64, _i64, _f32p, _i64,
+                                            _i64, ctypes.c_float, _f32p, _i64, _i64, _i64,
+                                            _f32p, ctypes.c_int, _f32p, ctypes.c_int]
+            lib.oracle_sgemm_ex.restype = ctypes.c_int
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -138,6 +143,35 @@ def sgemm_entries(M, N, K, alpha, A, B, beta, C0, ii, jj, *, lda=None, ldb=None,
                                       len(ii), _fp(out))
         if rc:
             raise RuntimeError("oracle_sgemm_entries failed")
+    return out
+
+
+def sgemm_ex(op_a: int, op_b: int, M: int, N: int, K: int, alpha: float, A: np.ndarray,
+             lda: int, stride_a: int, B: np.ndarray, ldb: int, stride_b: int, beta: float,
+             C0: np.ndarray | None, ldc0: int, stride_c0: int, batch: int,
+             bias: np.ndarray | None = None, act: int = 0, *, nthreads: int = 0) -> np.ndarray:
+    """The general form (see oracle_sgemm_ex in oracle_sgemm.c): batched,
+    op(X) = X or X^T, + bias[j], act 0 (none) or 1 (tanh GELU).  A, B, C0 are
+    the flat backing buffers the strides index.  Returns (batch, M, N)."""
+    lib = _load()
+    A = np.ascontiguousarray(A, dtype=np.float32).ravel()
+    B = np.ascontiguousarray(B, dtype=np.float32).ravel()
+    if C0 is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs C0")
+        C0 = np.zeros(1, np.float32)
+    C0 = np.ascontiguousarray(C0, dtype=np.float32).ravel()
+    bias_p = None
+    if bias is not None:
+        bias = np.ascontiguousarray(bias, dtype=np.float32).ravel()
+        bias_p = _fp(bias)
+    out = np.empty((batch, M, N), dtype=np.float32)
+    if batch and M and N:
+        rc = lib.oracle_sgemm_ex(int(op_a), int(op_b), M, N, K, float(alpha), _fp(A), lda,
+                                 stride_a, _fp(B), ldb, stride_b, float(beta), _fp(C0), ldc0,
+                                 stride_c0, batch, bias_p, int(act), _fp(out), int(nthreads))
+        if rc:
+            raise RuntimeError("oracle_sgemm_ex failed")
     return out
 
 

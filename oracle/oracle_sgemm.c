@@ -35,6 +35,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#include <math.h>
 #ifdef _OPENMP
 #include <omp.h>
 #endif
@@ -153,6 +154,81 @@ int oracle_sgemm_entries(int64_t M, int64_t N, int64_t K, float alpha,
         double v = (alpha != 0.0f) ? (double)alpha * s : 0.0;
         if (beta != 0.0f) v += (double)beta * (double)C0[i * ldc0 + j];
         out[t] = (float)v;
+    }
+    return bad;
+}
+
+/*
+ * The general form, for b in [0, batch):
+ *
+ *   C_b[i][j] = fl32( act( alpha * S_b[i][j] + beta * C0_b[i][j] + bias[j] ) )
+ *   S_b[i][j] = sum_k opA_b[i][k] * opB_b[k][j]
+ *   opA_b[i][k] = A[b*sa + i*lda + k]  (op_a = 0)   or  A[b*sa + k*lda + i]  (op_a = 1)
+ *   opB_b[k][j] = B[b*sb + k*ldb + j]  (op_b = 0)   or  B[b*sb + j*ldb + k]  (op_b = 1)
+ *
+ * - "GPU Target" (MLIR tutorial), section "타일링된 행렬 곱셈": the batched
+ *   variant indexes a third dimension by batch (per attention head), and
+ *   operands are strided views (a transposed matrix is a view with swapped
+ *   strides).
+ * - "GPU Target", GPT-2 sublayers: a projection is x @ W + b; the MLP applies
+ *   GELU in its tanh form, 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+ *   act = 0: none, act = 1: that GELU.  bias == NULL: no bias.
+ * Everything in double, one final rounding to float; S in ascending k.  The
+ * same special cases as oracle_sgemm (alpha == 0 or K == 0: A and B not
+ * read; beta == 0: C0 not read).  Output: C[b*M*N + i*N + j] (dense).
+ */
+static double oracle_gelu_tanh(double x)
+{
+    const double c = sqrt(2.0 / 3.14159265358979323846);
+    return 0.5 * x * (1.0 + tanh(c * (x + 0.044715 * x * x * x)));
+}
+
+int oracle_sgemm_ex(int op_a, int op_b, int64_t M, int64_t N, int64_t K, float alpha,
+                    const float *A, int64_t lda, int64_t sa, const float *B, int64_t ldb,
+                    int64_t sb, float beta, const float *C0, int64_t ldc0, int64_t sc,
+                    int64_t batch, const float *bias, int act, float *C, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0 || batch < 0) return 1;
+    if (M == 0 || N == 0 || batch == 0) return 0;
+    int bad = 0;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads) reduction(| : bad)
+#endif
+    {
+        double *acc = (double *)malloc((size_t)N * sizeof(double));
+        if (!acc) {
+            bad = 1;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1) collapse(2)
+#endif
+            for (int64_t b = 0; b < batch; ++b) {
+                for (int64_t i = 0; i < M; ++i) {
+                    const float *Ab = A + b * sa;
+                    const float *Bb = B + b * sb;
+                    for (int64_t j = 0; j < N; ++j) acc[j] = 0.0;
+                    if (alpha != 0.0f) {
+                        for (int64_t k = 0; k < K; ++k) {
+                            const double a = (double)(op_a ? Ab[k * lda + i] : Ab[i * lda + k]);
+                            for (int64_t j = 0; j < N; ++j) {
+                                const double bv =
+                                    (double)(op_b ? Bb[j * ldb + k] : Bb[k * ldb + j]);
+                                acc[j] += a * bv;
+                            }
+                        }
+                    }
+                    for (int64_t j = 0; j < N; ++j) {
+                        double v = (alpha != 0.0f) ? (double)alpha * acc[j] : 0.0;
+                        if (beta != 0.0f) v += (double)beta * (double)C0[b * sc + i * ldc0 + j];
+                        if (bias) v += (double)bias[j];
+                        if (act == 1) v = oracle_gelu_tanh(v);
+                        C[(b * M + i) * N + j] = (float)v;
+                    }
+                }
+            }
+            free(acc);
+        }
     }
     return bad;
 }
