@@ -46,7 +46,8 @@ METRIC = "SGEMM TFLOP/s (2MNK/t) at M=N=K=8192 fp32; % of GB300 FP32 FFMA peak"
 UNIT = "TFLOP/s"
 FMA_PER_SM_PER_CLK = 128      # fp32 FMA lanes per SM (4 sub-partitions x 32)
 L2_BYTES = 129 * 1000 * 1000
-KERNEL_SOURCE = os.path.join(ROOT, "dense_fp32_matrix_06_gb300", "csrc", "ffma_gemm.cu")
+KERNEL_SOURCES = [os.path.join(ROOT, "dense_fp32_matrix_06_gb300", "csrc", f)
+                  for f in ("ffma_kernel.cuh", "ffma_gemm.cu", "sgemm_internal.h")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -213,8 +214,12 @@ def cpu_baseline(p: workloads.Problem, target_s: float = 15.0) -> dict:
 # --------------------------------------------------------------------------
 
 def source_hash() -> str:
-    with open(KERNEL_SOURCE, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of the FFMA kernel's sources (traffic figures are tied to it)."""
+    h = hashlib.sha256()
+    for path in KERNEL_SOURCES:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def committed_traffic(kernel_id: int, workload: str, flops_per_launch: float):
