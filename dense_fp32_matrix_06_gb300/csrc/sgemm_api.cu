@@ -501,8 +501,8 @@ sgemm_status tf32x3_run(int64_t M, int64_t N, int64_t K, float alpha, const floa
     if (!C) return SGEMM_ERR_INVALID_ARG;
     if (K > 0 && alpha != 0.0f && (!A || !B)) return SGEMM_ERR_INVALID_ARG;
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return SGEMM_ERR_INVALID_ARG;
-    int dev = 0;
-    s = current_device(&dev, nullptr);
+    int dev = 0, sms = 0;
+    s = current_device(&dev, &sms);
     if (s != SGEMM_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
@@ -510,13 +510,19 @@ sgemm_status tf32x3_run(int64_t M, int64_t N, int64_t K, float alpha, const floa
         e = launch_scale(C, M, N, ldc, beta, st);
         return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
     }
-    // The per-stream workspace also carries the split-K tile counters, which
-    // must stay zero: the hi/lo operands go after the counter block.
+    int split = tf32x3_choose_split(M, N, K, sms);
+    if (const char *force = std::getenv("SGEMM_TF32X3_FORCE_SPLIT")) {
+        const int f = std::atoi(force);
+        if (f >= 1 && f <= 64) split = f;
+    }
+    // The per-stream workspace starts with the split-K tile counters, which
+    // stay zero between calls; the hi/lo operands and partials follow.
     void *ws = nullptr;
-    s = library_workspace(dev, st, kCounterBytes + tf32x3_workspace_bytes(M, N, K), &ws);
+    s = library_workspace(dev, st, kCounterBytes + tf32x3_workspace_bytes(M, N, K, split), &ws);
     if (s != SGEMM_OK) return s;
     e = launch_tf32x3(A, lda, B, ldb, C, ldc, M, N, K, alpha, beta,
-                      static_cast<char *>(ws) + kCounterBytes, limit_ns, inject_stall, st);
+                      static_cast<char *>(ws) + kCounterBytes, static_cast<unsigned *>(ws), split,
+                      limit_ns, inject_stall, st);
     return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
 }
 

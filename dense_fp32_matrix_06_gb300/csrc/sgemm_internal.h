@@ -87,11 +87,12 @@ cudaError_t launch_ffma_probe(int64_t ctas, int64_t iters, bool packed, float *o
 cudaError_t ffma_kernel_attributes(cudaFuncAttributes *attr);
 
 // 3xTF32 tensor-core mode (tf32x3_gemm.cu).
-size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K);
+int tf32x3_choose_split(int64_t M, int64_t N, int64_t K, int sms);
+size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, int split);
 cudaError_t launch_tf32x3(const float *A, int64_t lda, const float *B, int64_t ldb, float *C,
                           int64_t ldc, int64_t M, int64_t N, int64_t K, float alpha, float beta,
-                          void *workspace, uint64_t limit_ns, int inject_stall,
-                          cudaStream_t stream);
+                          void *workspace, unsigned *counters, int split, uint64_t limit_ns,
+                          int inject_stall, cudaStream_t stream);
 // Reads and clears the mode's device error word (synchronises `stream`).
 cudaError_t tf32x3_read_error(unsigned *out, cudaStream_t stream);
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s bound on every device-side wait

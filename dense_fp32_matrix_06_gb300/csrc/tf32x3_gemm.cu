@@ -27,6 +27,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "sgemm_internal.h"
@@ -232,6 +233,12 @@ struct TcArgs {
     int32_t tiles_m, tiles_n;
     uint64_t limit_ns;     // bound on every mbarrier wait
     int32_t inject_stall;  // 1: the producer issues nothing (exercises the bounded waits)
+    // split-K: tile t's K blocks are cut into `split` ranges of kb_per_split
+    // blocks; CTA pid computes range pid % split of tile pid / split
+    int32_t split;
+    int32_t kb_per_split;
+    unsigned *counters;    // split > 1: one ticket per tile, zero on entry and exit
+    float *partials;       // split > 1: tiles * split partial tiles of 128 x BN
 };
 
 template <int BN, int STAGES>
@@ -269,9 +276,11 @@ tf32x3_mma_kernel(const __grid_constant__ CUtensorMap map_a_hi,
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     __shared__ int s_mma_ok;
+    __shared__ unsigned s_ticket;
 
-    // grouped raster over 8 tile rows
-    const int pid = blockIdx.x;
+    // (tile, K range) of this CTA; grouped raster over 8 tile rows
+    const int pid = blockIdx.x / p.split;
+    const int split_idx = blockIdx.x - pid * p.split;
     const int per_group = 8 * p.tiles_n;
     const int group = pid / per_group;
     const int first_m = group * 8;
@@ -281,7 +290,9 @@ tf32x3_mma_kernel(const __grid_constant__ CUtensorMap map_a_hi,
     const int tile_n = in_group / gm;
     const int m0 = tile_m * kTcBM;
     const int n0 = tile_n * BN;
-    const int nkb = int((p.K + kTcBK - 1) / kTcBK);
+    const int nkb_all = int((p.K + kTcBK - 1) / kTcBK);
+    const int kb0 = split_idx * p.kb_per_split;
+    const int nkb = max(0, min(nkb_all, kb0 + p.kb_per_split) - kb0);   // K blocks of this CTA
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -313,7 +324,7 @@ tf32x3_mma_kernel(const __grid_constant__ CUtensorMap map_a_hi,
                 const uint32_t use = uint32_t(kb / STAGES);
                 if (kb >= STAGES && !mbar_wait(empty_bar(s), (use & 1u) ^ 1u, p.limit_ns)) break;
                 mbar_expect_tx(full_bar(s), uint32_t(L::kStageBytes));
-                const int kc = kb * kTcBK;
+                const int kc = (kb0 + kb) * kTcBK;
                 tma_load_2d(a_hi(s), &map_a_hi, kc, m0, full_bar(s));
                 tma_load_2d(a_lo(s), &map_a_lo, kc, m0, full_bar(s));
                 tma_load_2d(b_hi(s), &map_b_hi, kc, n0, full_bar(s));
@@ -355,41 +366,103 @@ tf32x3_mma_kernel(const __grid_constant__ CUtensorMap map_a_hi,
     const bool have = mbar_wait(done_bar, 0u, p.limit_ns);
     tc_fence_after();
     const bool clean = have && s_mma_ok != 0;
-    if (__all_sync(0xffffffffu, clean)) {
-        const int64_t row = int64_t(m0) + warp * 32 + lane;
-        const bool row_ok = row < p.M;
-        float *crow = p.C + (row_ok ? row : 0) * p.ldc;
-        const bool vec = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0) && (p.ldc % 4 == 0);
+    const int64_t row = int64_t(m0) + warp * 32 + lane;
+    const bool row_ok = row < p.M;
+    const bool vec = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0) && (p.ldc % 4 == 0);
+    float *crow = p.C + (row_ok ? row : 0) * p.ldc;
+
+    // alpha/beta on 32 consecutive columns of this thread's row
+    auto store32 = [&](int c0, const float (&v)[32]) {
+        const int64_t col = int64_t(n0) + c0;
+        if (vec && col + 32 <= p.N) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                float4 o = make_float4(p.alpha * v[4 * q], p.alpha * v[4 * q + 1],
+                                       p.alpha * v[4 * q + 2], p.alpha * v[4 * q + 3]);
+                float4 *dst = reinterpret_cast<float4 *>(crow + col + 4 * q);
+                if (p.beta != 0.0f) {
+                    const float4 old = *dst;
+                    o.x = fmaf(p.beta, old.x, o.x);
+                    o.y = fmaf(p.beta, old.y, o.y);
+                    o.z = fmaf(p.beta, old.z, o.z);
+                    o.w = fmaf(p.beta, old.w, o.w);
+                }
+                *dst = o;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                if (col + j < p.N) {
+                    float o = p.alpha * v[j];
+                    if (p.beta != 0.0f) o = fmaf(p.beta, crow[col + j], o);
+                    crow[col + j] = o;
+                }
+            }
+        }
+    };
+
+    if (p.split == 1) {
+        if (__all_sync(0xffffffffu, clean)) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-            float v[32];
-            tmem_ld32(tmem + (uint32_t(warp * 32) << 16) + uint32_t(c0), v);
-            if (!row_ok) continue;
-            const int64_t col = int64_t(n0) + c0;
-            if (vec && col + 32 <= p.N) {
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                float v[32];
+                tmem_ld32(tmem + (uint32_t(warp * 32) << 16) + uint32_t(c0), v);
+                if (row_ok) store32(c0, v);
+            }
+        }
+    } else {
+        // partial tile of this K range: slot blockIdx.x, row-major 128 x BN
+        const size_t slot = size_t(kTcBM) * BN;
+        float *part = p.partials + size_t(pid) * p.split * slot;
+        float *mine = part + size_t(split_idx) * slot + size_t(warp * 32 + lane) * BN;
+        if (__all_sync(0xffffffffu, clean)) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                float v[32];
+                if (nkb > 0) {
+                    tmem_ld32(tmem + (uint32_t(warp * 32) << 16) + uint32_t(c0), v);
+                } else {   // an empty K range contributes zeros (TMEM was never written)
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    float4 o = make_float4(p.alpha * v[4 * q], p.alpha * v[4 * q + 1],
-                                           p.alpha * v[4 * q + 2], p.alpha * v[4 * q + 3]);
-                    float4 *dst = reinterpret_cast<float4 *>(crow + col + 4 * q);
-                    if (p.beta != 0.0f) {
-                        const float4 old = *dst;
-                        o.x = fmaf(p.beta, old.x, o.x);
-                        o.y = fmaf(p.beta, old.y, o.y);
-                        o.z = fmaf(p.beta, old.z, o.z);
-                        o.w = fmaf(p.beta, old.w, o.w);
-                    }
-                    *dst = o;
+                    for (int j = 0; j < 32; ++j) v[j] = 0.0f;
                 }
-            } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    if (col + j < p.N) {
-                        float o = p.alpha * v[j];
-                        if (p.beta != 0.0f) o = fmaf(p.beta, crow[col + j], o);
-                        crow[col + j] = o;
+                for (int q = 0; q < 8; ++q)
+                    __stcg(reinterpret_cast<float4 *>(mine + c0 + 4 * q),
+                           make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+            }
+        }
+        __threadfence();
+        __syncthreads();
+        // ticket: +1 per finished range; a range whose waits expired adds
+        // 0x10001, so the tile still completes (and rearms) but is not stored
+        if (threadIdx.x == 0) {
+            const unsigned add = clean ? 1u : 0x10001u;
+            const unsigned now = atomicAdd(p.counters + pid, add) + add;
+            s_ticket = now;
+            if ((now & 0xffffu) == unsigned(p.split)) p.counters[pid] = 0u;
+        }
+        __syncthreads();
+        const unsigned now = s_ticket;
+        if ((now & 0xffffu) == unsigned(p.split) && (now >> 16) == 0u && row_ok) {
+            __threadfence();
+            const float *base = part + size_t(warp * 32 + lane) * BN;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                for (int sidx = 0; sidx < p.split; ++sidx) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 x = __ldcg(reinterpret_cast<const float4 *>(
+                            base + size_t(sidx) * slot + c0 + 4 * q));
+                        v[4 * q] += x.x;
+                        v[4 * q + 1] += x.y;
+                        v[4 * q + 2] += x.z;
+                        v[4 * q + 3] += x.w;
                     }
                 }
+                store32(c0, v);
             }
         }
     }
@@ -458,33 +531,59 @@ cudaError_t launch_mma(const CUtensorMap &ah, const CUtensorMap &al, const CUten
     cudaError_t e = cudaFuncSetAttribute(tf32x3_mma_kernel<BN, STAGES>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynBytes);
     if (e != cudaSuccess) return e;
-    const unsigned grid = unsigned(int64_t(a.tiles_m) * a.tiles_n);
+    const unsigned grid = unsigned(int64_t(a.tiles_m) * a.tiles_n * a.split);
     tf32x3_mma_kernel<BN, STAGES><<<grid, kTcThreads, L::kDynBytes, stream>>>(ah, al, bh, bl, a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+namespace {
+constexpr int kTcBN = 256;
+constexpr int kTcStages = 2;
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+}  // namespace
+
+// K ranges per tile.  One CTA runs per SM, so a grid of fewer tiles than SMs
+// leaves SMs idle; cutting K fills them but costs a partial-tile write and
+// read per range plus a second pass of prologue and epilogue.  Measured on
+// GB300 (forced splits 1..8): splitting paid off only when the grid filled at
+// most half the SMs and every range kept >= 24 K blocks (768 of K) --
+// 1024x1024x16384: 51 -> 111 TFLOP/s at 4 ranges, 1024x768x3072: 40 -> 54 at
+// 3-4 -- and lost everywhere else (1024^3, GPT-2 QKV/MLP-up, 2048^3, 4096^3).
+int tf32x3_choose_split(int64_t M, int64_t N, int64_t K, int sms) {
+    const int64_t tiles = ((M + kTcBM - 1) / kTcBM) * ((N + kTcBN - 1) / kTcBN);
+    const int64_t nkb = (K + kTcBK - 1) / kTcBK;
+    if (sms <= 0 || tiles > kMaxSplitTiles || 2 * tiles > sms) return 1;
+    int64_t s = std::min<int64_t>(sms / tiles, nkb / 24);
+    s = std::min<int64_t>(s, 16);
+    return s > 1 ? int(s) : 1;
+}
+
+size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, int split) {
     const int64_t kp = (K + 3) / 4 * 4;
-    const size_t a = (size_t(M) * kp * 4 + 255) / 256 * 256;
-    const size_t b = (size_t(N) * kp * 4 + 255) / 256 * 256;
-    return 2 * a + 2 * b;
+    const size_t a = round256(size_t(M) * kp * 4);
+    const size_t b = round256(size_t(N) * kp * 4);
+    const int64_t tiles = ((M + kTcBM - 1) / kTcBM) * ((N + kTcBN - 1) / kTcBN);
+    const size_t parts = split > 1 ? size_t(tiles) * split * kTcBM * kTcBN * 4 : 0;
+    return 2 * a + 2 * b + parts;
 }
 
 cudaError_t launch_tf32x3(const float *A, int64_t lda, const float *B, int64_t ldb, float *C,
                           int64_t ldc, int64_t M, int64_t N, int64_t K, float alpha, float beta,
-                          void *workspace, uint64_t limit_ns, int inject_stall,
-                          cudaStream_t stream) {
-    constexpr int BN = 256, STAGES = 2;
+                          void *workspace, unsigned *counters, int split, uint64_t limit_ns,
+                          int inject_stall, cudaStream_t stream) {
+    constexpr int BN = kTcBN, STAGES = kTcStages;
     const int64_t kp = (K + 3) / 4 * 4;
-    const size_t abytes = (size_t(M) * kp * 4 + 255) / 256 * 256;
-    const size_t bbytes = (size_t(N) * kp * 4 + 255) / 256 * 256;
+    const size_t abytes = round256(size_t(M) * kp * 4);
+    const size_t bbytes = round256(size_t(N) * kp * 4);
     char *w = static_cast<char *>(workspace);
     float *a_hi = reinterpret_cast<float *>(w);
     float *a_lo = reinterpret_cast<float *>(w + abytes);
     float *b_hi = reinterpret_cast<float *>(w + 2 * abytes);
     float *b_lo = reinterpret_cast<float *>(w + 2 * abytes + bbytes);
+    float *parts = reinterpret_cast<float *>(w + 2 * abytes + 2 * bbytes);
 
     int64_t blocks = (M * K + 255) / 256;
     if (blocks > 8192) blocks = 8192;
@@ -512,6 +611,11 @@ cudaError_t launch_tf32x3(const float *A, int64_t lda, const float *B, int64_t l
     a.tiles_n = int32_t((N + BN - 1) / BN);
     a.limit_ns = limit_ns;
     a.inject_stall = inject_stall;
+    const int64_t nkb = (K + kTcBK - 1) / kTcBK;
+    a.split = split > 1 ? split : 1;
+    a.kb_per_split = int32_t((nkb + a.split - 1) / a.split);
+    a.counters = counters;
+    a.partials = parts;
     return launch_mma<BN, STAGES>(ah, al, bh, bl, a, stream);
 }
 

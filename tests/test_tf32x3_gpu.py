@@ -122,8 +122,24 @@ def test_beta_zero_alpha_zero_k_zero(sg):
     assert np.array_equal(run(sg, r), oracle.problem(r))
 
 
+@pytest.mark.parametrize("split", ["2", "3", "5", "16"])
+def test_forced_split(sg, monkeypatch, split):
+    monkeypatch.setenv("SGEMM_TF32X3_FORCE_SPLIT", split)
+    p = workloads.make(300, 520, 1000, seed=31, beta=0.5, c0_dist="uniform", alpha=0.75)
+    check(p, run(sg, p), exact=False)
+    q = workloads.make(256, 256, 320, dist="int4", seed=32, alpha=1.5, beta=0.5, c0_dist="int4")
+    check(q, run(sg, q), exact=True)        # 10 K blocks: split 16 leaves empty ranges
+
+
+def test_split_plans_for_small_grids(sg):
+    # these run with more K ranges than tiles; parity at full size
+    for name in ("long_k", "gpt2_mlp_down", "square1024ab"):
+        p = workloads.workload(name)
+        check(p, run(sg, p), exact=False)
+
+
 def test_deterministic(sg):
-    p = workloads.workload("gpt2_mlp_down")
+    p = workloads.workload("long_k")
     first = run(sg, p)
     for _ in range(2):
         assert np.array_equal(run(sg, p).view(np.uint32), first.view(np.uint32))
