@@ -439,6 +439,46 @@ def run_tf32x3(sg, p, A, B, C, stream, args, dist, device):
     status = sg.device_status(sh)
     world = dist.get_world_size() if dist is not None else 1
     per_call = el / args.steps
+
+    # B packed once (weights reused), and the opt-in in-kernel split of A
+    nb = sg.tf32x3_packed_b_bytes(p.K, p.N)
+    packed = torch.empty(nb, dtype=torch.uint8, device=device)
+    sg.tf32x3_pack_b_ptr(p.K, p.N, B.data_ptr(), p.ldb, packed.data_ptr(), nb, sh)
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(device)
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n):
+            fn()
+        a1.record(stream)
+        torch.cuda.synchronize(device)
+        return a0.elapsed_time(a1) / 1e3 / n
+
+    def packed_call():
+        sg.sgemm_tf32x3_packed_ptr(p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, packed.data_ptr(),
+                                   p.beta, C.data_ptr(), p.ldc, sh)
+
+    n_var = max(3, min(args.steps, 10))
+    t_packed = timed(packed_call, n_var)
+    old = os.environ.get("SGEMM_TF32X3_FUSE_A")
+    os.environ["SGEMM_TF32X3_FUSE_A"] = "1"
+    try:
+        t_fused = timed(call, n_var)
+    finally:
+        if old is None:
+            os.environ.pop("SGEMM_TF32X3_FUSE_A", None)
+        else:
+            os.environ["SGEMM_TF32X3_FUSE_A"] = old
+    variants = {"packed_b": {"value": round(flops / t_packed / 1e12, 3),
+                             "note": "B split and transposed once (sgemm_tf32x3_pack_b); per call "
+                                     "A pre-pass + tensor kernel"},
+                "fused_a_opt_in": {"value": round(flops / t_fused / 1e12, 3),
+                                   "note": "A split in shared memory (SGEMM_TF32X3_FUSE_A=1); "
+                                           "slower, off by default"}}
     peak, src = tf32_peak_tflops()
     achieved = 3 * flops / per_call / 1e12
     return {"value": round(throughput(flops, args.steps, world, el), 3), "unit": UNIT,
@@ -450,7 +490,8 @@ def run_tf32x3(sg, p, A, B, C, stream, args, dist, device):
                          "kernel": "tf32x3_mma_kernel<256,2> (+ split pre-pass)",
                          "peak_source": src,
                          "note": "achieved = 3 tf32 products x 2MNK over the whole call "
-                                 "(split pre-pass included)"}}
+                                 "(split pre-pass included)"},
+            "variants": variants}
 
 
 # (name, op_a, op_b, M, N, K, batch, bias, act): batched, transposed and

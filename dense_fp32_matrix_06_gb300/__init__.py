@@ -50,6 +50,9 @@ EXPORTED_SYMBOLS = (
     "sgemm_device_status",
     "sgemm_tf32x3_stall_selftest",
     "sgemm_ex",
+    "sgemm_tf32x3_packed_b_bytes",
+    "sgemm_tf32x3_pack_b",
+    "sgemm_tf32x3_packed",
 )
 OP_N, OP_T = 0, 1
 ACT_NONE, ACT_GELU_TANH = 0, 1
@@ -143,6 +146,13 @@ def load_library() -> ctypes.CDLL:
                                  _i64, _i64, _vp, _i64, _i64, _f32, _vp, _i64, _i64, _i64, _vp,
                                  ctypes.c_int32, _vp]
         lib.sgemm_ex.restype = ctypes.c_int
+        lib.sgemm_tf32x3_packed_b_bytes.argtypes = [_i64, _i64]
+        lib.sgemm_tf32x3_packed_b_bytes.restype = ctypes.c_size_t
+        lib.sgemm_tf32x3_pack_b.argtypes = [_i64, _i64, _vp, _i64, _vp, ctypes.c_size_t, _vp]
+        lib.sgemm_tf32x3_pack_b.restype = ctypes.c_int
+        lib.sgemm_tf32x3_packed.argtypes = [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _f32, _vp,
+                                            _i64, _vp]
+        lib.sgemm_tf32x3_packed.restype = ctypes.c_int
         lib.sgemm_noalloc.argtypes = lib.sgemm.argtypes
         lib.sgemm_noalloc.restype = ctypes.c_int
         lib.sgemm_tf32x3.argtypes = lib.sgemm.argtypes
@@ -226,6 +236,28 @@ def sgemm_tf32x3_ptr(M: int, N: int, K: int, alpha: float, A: int, lda: int, B: 
     """sgemm_tf32x3(): the 3xTF32 tensor-core mode (normalised error <= 1e-5)."""
     _check(load_library().sgemm_tf32x3(M, N, K, alpha, A or None, lda, B or None, ldb, beta,
                                        C or None, ldc, stream or None), "sgemm_tf32x3")
+
+
+def tf32x3_packed_b_bytes(K: int, N: int) -> int:
+    """sgemm_tf32x3_packed_b_bytes(): bytes of the packed form of a K x N B."""
+    return int(load_library().sgemm_tf32x3_packed_b_bytes(K, N))
+
+
+def tf32x3_pack_b_ptr(K: int, N: int, B: int, ldb: int, packed: int, packed_bytes: int,
+                      stream: int = 0) -> None:
+    """sgemm_tf32x3_pack_b(): split and transpose B once for the tensor-core mode."""
+    _check(load_library().sgemm_tf32x3_pack_b(K, N, B or None, ldb, packed or None,
+                                              packed_bytes, stream or None),
+           "sgemm_tf32x3_pack_b")
+
+
+def sgemm_tf32x3_packed_ptr(M: int, N: int, K: int, alpha: float, A: int, lda: int,
+                            packed_b: int, beta: float, C: int, ldc: int,
+                            stream: int = 0) -> None:
+    """sgemm_tf32x3_packed(): the tensor-core mode with a packed B."""
+    _check(load_library().sgemm_tf32x3_packed(M, N, K, alpha, A or None, lda,
+                                              packed_b or None, beta, C or None, ldc,
+                                              stream or None), "sgemm_tf32x3_packed")
 
 
 def device_status(stream: int = 0) -> int:

@@ -518,7 +518,10 @@ sgemm_status tf32x3_run(int64_t M, int64_t N, int64_t K, float alpha, const floa
     // The per-stream workspace starts with the split-K tile counters, which
     // stay zero between calls; the hi/lo operands and partials follow.
     void *ws = nullptr;
-    s = library_workspace(dev, st, kCounterBytes + tf32x3_workspace_bytes(M, N, K, split), &ws);
+    s = library_workspace(
+        dev, st,
+        kCounterBytes + tf32x3_workspace_bytes(M, N, K, split, tf32x3_use_fused_a(A, lda), false),
+        &ws);
     if (s != SGEMM_OK) return s;
     e = launch_tf32x3(A, lda, B, ldb, C, ldc, M, N, K, alpha, beta,
                       static_cast<char *>(ws) + kCounterBytes, static_cast<unsigned *>(ws), split,
@@ -636,5 +639,64 @@ extern "C" sgemm_status sgemm_ex(int32_t op_a, int32_t op_b, int64_t M, int64_t 
         a.partials = reinterpret_cast<float *>(static_cast<char *>(ws) + kCounterBytes);
     }
     e = launch_ffma(a, plan.kernel, plan.vec != 0, plan.edge != 0, ta, tb, st);
+    return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
+}
+
+// ---------------------------------------------------------------------------
+// 3xTF32 with B packed once
+// ---------------------------------------------------------------------------
+
+extern "C" size_t sgemm_tf32x3_packed_b_bytes(int64_t K, int64_t N) {
+    if (K <= 0 || N <= 0) return 0;
+    return tf32x3_packed_b_bytes(K, N);
+}
+
+extern "C" sgemm_status sgemm_tf32x3_pack_b(int64_t K, int64_t N, const float *B, int64_t ldb,
+                                           void *packed, size_t packed_bytes, void *stream) {
+    if (K <= 0 || N <= 0 || K > INT32_MAX || N > INT32_MAX) return SGEMM_ERR_INVALID_ARG;
+    if (ldb < N || !B || !packed) return SGEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(packed) & 255u) != 0) return SGEMM_ERR_MISALIGNED;
+    if (packed_bytes < tf32x3_packed_b_bytes(K, N)) return SGEMM_ERR_WORKSPACE;
+    sgemm_status s = current_device(nullptr, nullptr);
+    if (s != SGEMM_OK) return s;
+    const cudaError_t e = tf32x3_pack_b(K, N, B, ldb, packed, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
+}
+
+extern "C" sgemm_status sgemm_tf32x3_packed(int64_t M, int64_t N, int64_t K, float alpha,
+                                           const float *A, int64_t lda, const void *packed_b,
+                                           float beta, float *C, int64_t ldc, void *stream) {
+    if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+        return SGEMM_ERR_INVALID_ARG;
+    if (lda < std::max<int64_t>(1, K) || ldc < std::max<int64_t>(1, N))
+        return SGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    if (!C) return SGEMM_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    sgemm_status s = current_device(&dev, &sms);
+    if (s != SGEMM_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (K == 0 || alpha == 0.0f) {
+        e = launch_scale(C, M, N, ldc, beta, st);
+        return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
+    }
+    if (!A || !packed_b) return SGEMM_ERR_INVALID_ARG;
+    if (!tf32x3_fusable_a(A, lda) || (reinterpret_cast<uintptr_t>(packed_b) & 255u) != 0)
+        return SGEMM_ERR_MISALIGNED;
+    int split = tf32x3_choose_split(M, N, K, sms);
+    if (const char *force = std::getenv("SGEMM_TF32X3_FORCE_SPLIT")) {
+        const int f = std::atoi(force);
+        if (f >= 1 && f <= 64) split = f;
+    }
+    void *ws = nullptr;
+    s = library_workspace(
+        dev, st,
+        kCounterBytes + tf32x3_workspace_bytes(M, N, K, split, tf32x3_use_fused_a(A, lda), true),
+        &ws);
+    if (s != SGEMM_OK) return s;
+    e = launch_tf32x3_packed(A, lda, packed_b, C, ldc, M, N, K, alpha, beta,
+                             static_cast<char *>(ws) + kCounterBytes, static_cast<unsigned *>(ws),
+                             split, kWaitLimitNs, 0, st);
     return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
 }

@@ -88,7 +88,17 @@ cudaError_t ffma_kernel_attributes(cudaFuncAttributes *attr);
 
 // 3xTF32 tensor-core mode (tf32x3_gemm.cu).
 int tf32x3_choose_split(int64_t M, int64_t N, int64_t K, int sms);
-size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, int split);
+size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, int split, bool fused,
+                              bool packed_b);
+size_t tf32x3_packed_b_bytes(int64_t K, int64_t N);
+bool tf32x3_fusable_a(const float *A, int64_t lda);
+bool tf32x3_use_fused_a(const float *A, int64_t lda);
+cudaError_t tf32x3_pack_b(int64_t K, int64_t N, const float *B, int64_t ldb, void *packed,
+                          cudaStream_t stream);
+cudaError_t launch_tf32x3_packed(const float *A, int64_t lda, const void *packed_b, float *C,
+                                 int64_t ldc, int64_t M, int64_t N, int64_t K, float alpha,
+                                 float beta, void *workspace, unsigned *counters, int split,
+                                 uint64_t limit_ns, int inject_stall, cudaStream_t stream);
 cudaError_t launch_tf32x3(const float *A, int64_t lda, const float *B, int64_t ldb, float *C,
                           int64_t ldc, int64_t M, int64_t N, int64_t K, float alpha, float beta,
                           void *workspace, unsigned *counters, int split, uint64_t limit_ns,

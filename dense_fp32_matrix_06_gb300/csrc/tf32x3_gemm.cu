@@ -29,6 +29,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstdlib>
 
 #include "sgemm_internal.h"
 
@@ -485,6 +486,292 @@ tf32x3_mma_kernel(const __grid_constant__ CUtensorMap map_a_hi,
     }
 }
 
+// ---------------------------------------------------------------------------
+// Fused variant: A's split happens in shared memory.
+//
+// A is K-major as stored, so its tile arrives by TMA as raw fp32 in exactly
+// the swizzled layout the MMA reads.  The raw tile lands in the A_lo slot of
+// the stage; four converter warps (threads 128..255) read it, write
+// A_hi = tf32(x) into the A_hi slot and overwrite the slot with
+// A_lo = tf32(x - A_hi) -- same offsets, no address arithmetic -- then fence
+// the generic-proxy writes for the tensor cores' async-proxy reads and arrive
+// on the stage's `conv` barrier, which the MMA issuer waits on instead of the
+// TMA barrier.  B must be K-major for the MMA, i.e. transposed from its
+// stored layout, so it arrives already split (B_hi^T, B_lo^T, packed once).
+// All eight warps share the epilogue: warp w reads TMEM lanes
+// 32*(w%4)..+31, warps 0-3 the left half of the columns, 4-7 the right half.
+// ---------------------------------------------------------------------------
+
+constexpr int kFusedThreads = 256;
+
+template <int BN, int STAGES>
+struct FusedSmem {
+    static constexpr int kABytes = kTcBM * kTcBK * 4;          // 16 KiB
+    static constexpr int kBBytes = BN * kTcBK * 4;
+    static constexpr int kStageBytes = 2 * kABytes + 2 * kBBytes;
+    static constexpr int kTxBytes = kABytes + 2 * kBBytes;      // raw A + B_hi + B_lo
+    static constexpr int kBarOffset = STAGES * kStageBytes;
+    // full[STAGES], conv[STAGES], empty[STAGES], done, then the TMEM address slot
+    static constexpr int kBytes = kBarOffset + (3 * STAGES + 1) * 8 + 8;
+    static constexpr int kDynBytes = kBytes + 1024;
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kFusedThreads, 1)
+tf32x3_fused_kernel(const __grid_constant__ CUtensorMap map_a,
+                    const __grid_constant__ CUtensorMap map_b_hi,
+                    const __grid_constant__ CUtensorMap map_b_lo, const TcArgs p) {
+    using L = FusedSmem<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const uint32_t bar0 = base + L::kBarOffset;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto conv_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+    const uint32_t done_bar = bar0 + 8u * (3 * STAGES);
+    uint32_t *tmem_slot =
+        reinterpret_cast<uint32_t *>(gbase + L::kBarOffset + (3 * STAGES + 1) * 8);
+    auto a_hi = [&](int s) { return base + s * L::kStageBytes; };
+    auto a_lo = [&](int s) { return base + s * L::kStageBytes + L::kABytes; };
+    auto b_hi = [&](int s) { return base + s * L::kStageBytes + 2 * L::kABytes; };
+    auto b_lo = [&](int s) { return base + s * L::kStageBytes + 2 * L::kABytes + L::kBBytes; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    __shared__ int s_mma_ok;
+    __shared__ unsigned s_ticket;
+
+    // (tile, K range) of this CTA; grouped raster over 8 tile rows
+    const int pid = blockIdx.x / p.split;
+    const int split_idx = blockIdx.x - pid * p.split;
+    const int per_group = 8 * p.tiles_n;
+    const int group = pid / per_group;
+    const int first_m = group * 8;
+    const int gm = min(p.tiles_m - first_m, 8);
+    const int in_group = pid - group * per_group;
+    const int tile_m = first_m + in_group % gm;
+    const int tile_n = in_group / gm;
+    const int m0 = tile_m * kTcBM;
+    const int n0 = tile_n * BN;
+    const int nkb_all = int((p.K + kTcBK - 1) / kTcBK);
+    const int kb0 = split_idx * p.kb_per_split;
+    const int nkb = max(0, min(nkb_all, kb0 + p.kb_per_split) - kb0);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(conv_bar(s), kFusedThreads - 128);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(done_bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(uint32_t(BN))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    int issued = 0;
+    if (warp == 0 && lane == 0) {
+        // ---- TMA producer: raw A into the A_lo slot, packed B_hi/B_lo ----
+        if (!p.inject_stall) {
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % STAGES;
+                const uint32_t use = uint32_t(kb / STAGES);
+                if (kb >= STAGES && !mbar_wait(empty_bar(s), (use & 1u) ^ 1u, p.limit_ns)) break;
+                mbar_expect_tx(full_bar(s), uint32_t(L::kTxBytes));
+                const int kc = (kb0 + kb) * kTcBK;
+                tma_load_2d(a_lo(s), &map_a, kc, m0, full_bar(s));
+                tma_load_2d(b_hi(s), &map_b_hi, kc, n0, full_bar(s));
+                tma_load_2d(b_lo(s), &map_b_lo, kc, n0, full_bar(s));
+                issued = kb + 1;
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer ----
+        constexpr uint32_t idesc = tf32_idesc(BN);
+        bool ok = true;
+        for (int kb = 0; kb < nkb && ok; ++kb) {
+            const int s = kb % STAGES;
+            const uint32_t use = uint32_t(kb / STAGES);
+            if (!mbar_wait(conv_bar(s), use & 1u, p.limit_ns)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kTcBK / 8; ++kk) {
+                const uint32_t koff = uint32_t(kk) * 32u;
+                const uint64_t ah = sw128_desc(a_hi(s) + koff), al = sw128_desc(a_lo(s) + koff);
+                const uint64_t bh = sw128_desc(b_hi(s) + koff), bl = sw128_desc(b_lo(s) + koff);
+                mma_tf32(tmem, al, bh, idesc, (kb | kk) != 0 ? 1u : 0u);
+                mma_tf32(tmem, ah, bl, idesc, 1u);
+                mma_tf32(tmem, ah, bh, idesc, 1u);
+            }
+            mma_commit(empty_bar(s));
+        }
+        s_mma_ok = ok ? 1 : 0;
+        mma_commit(done_bar);
+    } else if (warp >= 4) {
+        // ---- converters: split the raw A tile in place ----
+        const int c = threadIdx.x - 128;
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int s = kb % STAGES;
+            const uint32_t use = uint32_t(kb / STAGES);
+            if (!mbar_wait(full_bar(s), use & 1u, p.limit_ns)) break;
+            float4 *lo = reinterpret_cast<float4 *>(gbase + (a_lo(s) - base));
+            float4 *hi = reinterpret_cast<float4 *>(gbase + (a_hi(s) - base));
+#pragma unroll
+            for (int q = 0; q < L::kABytes / 16 / 128; ++q) {
+                const int i = c + 128 * q;
+                const float4 x = lo[i];
+                float4 h, l;
+                split2(x.x, h.x, l.x);
+                split2(x.y, h.y, l.y);
+                split2(x.z, h.z, l.z);
+                split2(x.w, h.w, l.w);
+                hi[i] = h;
+                lo[i] = l;
+            }
+            // make the generic-proxy writes visible to the tensor cores
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(conv_bar(s));
+        }
+    }
+    __syncwarp();
+    __syncthreads();   // every role has finished issuing; s_mma_ok is visible
+
+    // ---- epilogue: TMEM -> registers -> C (or partials) ----
+    const bool have = mbar_wait(done_bar, 0u, p.limit_ns);
+    tc_fence_after();
+    const bool clean = have && s_mma_ok != 0;
+    const int lrow = (warp & 3) * 32 + lane;          // TMEM lane = row in the tile
+    const int cbeg = (warp >> 2) * (BN / 2);          // this warp's column half
+    const int64_t row = int64_t(m0) + lrow;
+    const bool row_ok = row < p.M;
+    const bool vec = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0) && (p.ldc % 4 == 0);
+    float *crow = p.C + (row_ok ? row : 0) * p.ldc;
+    const uint32_t taddr = tmem + (uint32_t((warp & 3) * 32) << 16);
+
+    auto store32 = [&](int c0, const float (&v)[32]) {
+        const int64_t col = int64_t(n0) + c0;
+        if (vec && col + 32 <= p.N) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                float4 o = make_float4(p.alpha * v[4 * q], p.alpha * v[4 * q + 1],
+                                       p.alpha * v[4 * q + 2], p.alpha * v[4 * q + 3]);
+                float4 *dst = reinterpret_cast<float4 *>(crow + col + 4 * q);
+                if (p.beta != 0.0f) {
+                    const float4 old = *dst;
+                    o.x = fmaf(p.beta, old.x, o.x);
+                    o.y = fmaf(p.beta, old.y, o.y);
+                    o.z = fmaf(p.beta, old.z, o.z);
+                    o.w = fmaf(p.beta, old.w, o.w);
+                }
+                *dst = o;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                if (col + j < p.N) {
+                    float o = p.alpha * v[j];
+                    if (p.beta != 0.0f) o = fmaf(p.beta, crow[col + j], o);
+                    crow[col + j] = o;
+                }
+            }
+        }
+    };
+
+    if (p.split == 1) {
+        if (__all_sync(0xffffffffu, clean)) {
+#pragma unroll 1
+            for (int c0 = cbeg; c0 < cbeg + BN / 2; c0 += 32) {
+                float v[32];
+                tmem_ld32(taddr + uint32_t(c0), v);
+                if (row_ok) store32(c0, v);
+            }
+        }
+    } else {
+        const size_t slot = size_t(kTcBM) * BN;
+        float *part = p.partials + size_t(pid) * p.split * slot;
+        float *mine = part + size_t(split_idx) * slot + size_t(lrow) * BN;
+        if (__all_sync(0xffffffffu, clean)) {
+#pragma unroll 1
+            for (int c0 = cbeg; c0 < cbeg + BN / 2; c0 += 32) {
+                float v[32];
+                if (nkb > 0) {
+                    tmem_ld32(taddr + uint32_t(c0), v);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    __stcg(reinterpret_cast<float4 *>(mine + c0 + 4 * q),
+                           make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+            }
+        }
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const unsigned add = clean ? 1u : 0x10001u;
+            const unsigned now = atomicAdd(p.counters + pid, add) + add;
+            s_ticket = now;
+            if ((now & 0xffffu) == unsigned(p.split)) p.counters[pid] = 0u;
+        }
+        __syncthreads();
+        const unsigned now = s_ticket;
+        if ((now & 0xffffu) == unsigned(p.split) && (now >> 16) == 0u && row_ok) {
+            __threadfence();
+            const float *rowp = part + size_t(lrow) * BN;
+#pragma unroll 1
+            for (int c0 = cbeg; c0 < cbeg + BN / 2; c0 += 32) {
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                for (int sidx = 0; sidx < p.split; ++sidx) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 x = __ldcg(reinterpret_cast<const float4 *>(
+                            rowp + size_t(sidx) * slot + c0 + 4 * q));
+                        v[4 * q] += x.x;
+                        v[4 * q + 1] += x.y;
+                        v[4 * q + 2] += x.z;
+                        v[4 * q + 3] += x.w;
+                    }
+                }
+                store32(c0, v);
+            }
+        }
+    }
+
+    // ---- teardown ----
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0 && lane == 0) {
+        for (int kb = (issued > STAGES ? issued - STAGES : 0); kb < issued; ++kb)
+            mbar_wait(full_bar(kb % STAGES), uint32_t(kb / STAGES) & 1u, p.limit_ns);
+    }
+    if (warp == 1 && lane == 0 && !have) mbar_wait(done_bar, 0u, p.limit_ns);
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(uint32_t(BN))
+                     : "memory");
+    }
+}
+
 // cuTensorMapEncodeTiled, looked up once through the runtime (no link-time
 // dependency on the driver library).
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -536,6 +823,18 @@ cudaError_t launch_mma(const CUtensorMap &ah, const CUtensorMap &al, const CUten
     return cudaGetLastError();
 }
 
+template <int BN, int STAGES>
+cudaError_t launch_fused(const CUtensorMap &a, const CUtensorMap &bh, const CUtensorMap &bl,
+                         const TcArgs &args, cudaStream_t stream) {
+    using L = FusedSmem<BN, STAGES>;
+    cudaError_t e = cudaFuncSetAttribute(tf32x3_fused_kernel<BN, STAGES>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynBytes);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = unsigned(int64_t(args.tiles_m) * args.tiles_n * args.split);
+    tf32x3_fused_kernel<BN, STAGES><<<grid, kFusedThreads, L::kDynBytes, stream>>>(a, bh, bl, args);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 namespace {
@@ -561,13 +860,109 @@ int tf32x3_choose_split(int64_t M, int64_t N, int64_t K, int sms) {
     return s > 1 ? int(s) : 1;
 }
 
-size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, int split) {
+size_t tf32x3_packed_b_bytes(int64_t K, int64_t N) {
     const int64_t kp = (K + 3) / 4 * 4;
-    const size_t a = round256(size_t(M) * kp * 4);
-    const size_t b = round256(size_t(N) * kp * 4);
+    return 2 * round256(size_t(N) * kp * 4);
+}
+
+bool tf32x3_fusable_a(const float *A, int64_t lda) {
+    return (reinterpret_cast<uintptr_t>(A) & 15u) == 0 && lda % 4 == 0;
+}
+
+// The in-smem split of A (tf32x3_fused_kernel) is opt-in: measured on GB300
+// it is slower than the pre-pass (8192^3: 114 against 259 TFLOP/s), because
+// with two 96 KiB stages the conversion sits between the TMA landing and the
+// MMA on the critical path, which the two-deep ring cannot hide.
+bool tf32x3_use_fused_a(const float *A, int64_t lda) {
+    const char *env = std::getenv("SGEMM_TF32X3_FUSE_A");
+    return env && std::atoi(env) != 0 && tf32x3_fusable_a(A, lda);
+}
+
+size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, int split, bool fused,
+                              bool packed_b) {
+    const int64_t kp = (K + 3) / 4 * 4;
+    const size_t a = fused ? 0 : 2 * round256(size_t(M) * kp * 4);
+    const size_t b = packed_b ? 0 : tf32x3_packed_b_bytes(K, N);
     const int64_t tiles = ((M + kTcBM - 1) / kTcBM) * ((N + kTcBN - 1) / kTcBN);
     const size_t parts = split > 1 ? size_t(tiles) * split * kTcBM * kTcBN * 4 : 0;
-    return 2 * a + 2 * b + parts;
+    return a + b + parts;
+}
+
+cudaError_t tf32x3_pack_b(int64_t K, int64_t N, const float *B, int64_t ldb, void *packed,
+                          cudaStream_t stream) {
+    const int64_t kp = (K + 3) / 4 * 4;
+    float *b_hi = static_cast<float *>(packed);
+    float *b_lo = reinterpret_cast<float *>(static_cast<char *>(packed) +
+                                            round256(size_t(N) * kp * 4));
+    const dim3 tgrid(unsigned((N + 31) / 32), unsigned((K + 31) / 32));
+    split_transpose_kernel<<<tgrid, dim3(32, 8), 0, stream>>>(B, K, N, ldb, b_hi, b_lo, kp);
+    return cudaGetLastError();
+}
+
+namespace {
+
+TcArgs make_args(float *C, int64_t ldc, int64_t M, int64_t N, int64_t K, float alpha,
+                 float beta, unsigned *counters, float *parts, int split, uint64_t limit_ns,
+                 int inject_stall) {
+    TcArgs a;
+    a.C = C;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.ldc = ldc;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.tiles_m = int32_t((M + kTcBM - 1) / kTcBM);
+    a.tiles_n = int32_t((N + kTcBN - 1) / kTcBN);
+    a.limit_ns = limit_ns;
+    a.inject_stall = inject_stall;
+    const int64_t nkb = (K + kTcBK - 1) / kTcBK;
+    a.split = split > 1 ? split : 1;
+    a.kb_per_split = int32_t((nkb + a.split - 1) / a.split);
+    a.counters = counters;
+    a.partials = parts;
+    return a;
+}
+
+}  // namespace
+
+// C = alpha*A*B + beta*C with B packed; `workspace` holds A's hi/lo (unless A
+// is split in shared memory) followed by the split-K partials.
+cudaError_t launch_tf32x3_packed(const float *A, int64_t lda, const void *packed_b, float *C,
+                                 int64_t ldc, int64_t M, int64_t N, int64_t K, float alpha,
+                                 float beta, void *workspace, unsigned *counters, int split,
+                                 uint64_t limit_ns, int inject_stall, cudaStream_t stream) {
+    const int64_t kp = (K + 3) / 4 * 4;
+    const float *b_hi = static_cast<const float *>(packed_b);
+    const float *b_lo = reinterpret_cast<const float *>(static_cast<const char *>(packed_b) +
+                                                        round256(size_t(N) * kp * 4));
+    char *w = static_cast<char *>(workspace);
+    const bool fused = tf32x3_use_fused_a(A, lda);
+    if (fused) {
+        CUtensorMap am, bh, bl;
+        if (!encode_kmajor(&am, A, M, K, lda, kTcBM) ||
+            !encode_kmajor(&bh, b_hi, N, K, kp, kTcBN) || !encode_kmajor(&bl, b_lo, N, K, kp, kTcBN))
+            return cudaErrorInvalidValue;
+        const TcArgs a = make_args(C, ldc, M, N, K, alpha, beta, counters,
+                                   reinterpret_cast<float *>(w), split, limit_ns, inject_stall);
+        return launch_fused<kTcBN, kTcStages>(am, bh, bl, a, stream);
+    }
+    const size_t abytes = round256(size_t(M) * kp * 4);
+    float *a_hi = reinterpret_cast<float *>(w);
+    float *a_lo = reinterpret_cast<float *>(w + abytes);
+    float *parts = reinterpret_cast<float *>(w + 2 * abytes);
+    int64_t blocks = (M * K + 255) / 256;
+    if (blocks > 8192) blocks = 8192;
+    split_rows_kernel<<<unsigned(blocks), 256, 0, stream>>>(A, M, K, lda, a_hi, a_lo, kp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    CUtensorMap ah, al, bh, bl;
+    if (!encode_kmajor(&ah, a_hi, M, K, kp, kTcBM) || !encode_kmajor(&al, a_lo, M, K, kp, kTcBM) ||
+        !encode_kmajor(&bh, b_hi, N, K, kp, kTcBN) || !encode_kmajor(&bl, b_lo, N, K, kp, kTcBN))
+        return cudaErrorInvalidValue;
+    const TcArgs a = make_args(C, ldc, M, N, K, alpha, beta, counters, parts, split, limit_ns,
+                               inject_stall);
+    return launch_mma<kTcBN, kTcStages>(ah, al, bh, bl, a, stream);
 }
 
 cudaError_t launch_tf32x3(const float *A, int64_t lda, const float *B, int64_t ldb, float *C,
@@ -576,9 +971,18 @@ cudaError_t launch_tf32x3(const float *A, int64_t lda, const float *B, int64_t l
                           int inject_stall, cudaStream_t stream) {
     constexpr int BN = kTcBN, STAGES = kTcStages;
     const int64_t kp = (K + 3) / 4 * 4;
+    char *w = static_cast<char *>(workspace);
+    if (tf32x3_use_fused_a(A, lda)) {
+        // B split and transposed into the workspace; A split in shared memory
+        cudaError_t e = tf32x3_pack_b(K, N, B, ldb, w, stream);
+        if (e != cudaSuccess) return e;
+        return launch_tf32x3_packed(A, lda, w, C, ldc, M, N, K, alpha, beta,
+                                    w + tf32x3_packed_b_bytes(K, N), counters, split, limit_ns,
+                                    inject_stall, stream);
+    }
+    // both operands split (and B transposed) in a pre-pass
     const size_t abytes = round256(size_t(M) * kp * 4);
     const size_t bbytes = round256(size_t(N) * kp * 4);
-    char *w = static_cast<char *>(workspace);
     float *a_hi = reinterpret_cast<float *>(w);
     float *a_lo = reinterpret_cast<float *>(w + abytes);
     float *b_hi = reinterpret_cast<float *>(w + 2 * abytes);
@@ -590,32 +994,15 @@ cudaError_t launch_tf32x3(const float *A, int64_t lda, const float *B, int64_t l
     split_rows_kernel<<<unsigned(blocks), 256, 0, stream>>>(A, M, K, lda, a_hi, a_lo, kp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const dim3 tgrid(unsigned((N + 31) / 32), unsigned((K + 31) / 32));
-    split_transpose_kernel<<<tgrid, dim3(32, 8), 0, stream>>>(B, K, N, ldb, b_hi, b_lo, kp);
-    e = cudaGetLastError();
+    e = tf32x3_pack_b(K, N, B, ldb, w + 2 * abytes, stream);
     if (e != cudaSuccess) return e;
 
     CUtensorMap ah, al, bh, bl;
     if (!encode_kmajor(&ah, a_hi, M, K, kp, kTcBM) || !encode_kmajor(&al, a_lo, M, K, kp, kTcBM) ||
         !encode_kmajor(&bh, b_hi, N, K, kp, BN) || !encode_kmajor(&bl, b_lo, N, K, kp, BN))
         return cudaErrorInvalidValue;
-    TcArgs a;
-    a.C = C;
-    a.M = M;
-    a.N = N;
-    a.K = K;
-    a.ldc = ldc;
-    a.alpha = alpha;
-    a.beta = beta;
-    a.tiles_m = int32_t((M + kTcBM - 1) / kTcBM);
-    a.tiles_n = int32_t((N + BN - 1) / BN);
-    a.limit_ns = limit_ns;
-    a.inject_stall = inject_stall;
-    const int64_t nkb = (K + kTcBK - 1) / kTcBK;
-    a.split = split > 1 ? split : 1;
-    a.kb_per_split = int32_t((nkb + a.split - 1) / a.split);
-    a.counters = counters;
-    a.partials = parts;
+    const TcArgs a = make_args(C, ldc, M, N, K, alpha, beta, counters, parts, split, limit_ns,
+                               inject_stall);
     return launch_mma<BN, STAGES>(ah, al, bh, bl, a, stream);
 }
 

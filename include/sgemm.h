@@ -208,15 +208,48 @@ sgemm_status sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
  * Accuracy: max|C - exact| / (K*max|A|*max|B| + |beta|*max|C0|) <= 1e-5;
  * exact on integer inputs whose partial sums stay below 2^24 (their lo
  * parts are zero).  Any alignment and leading dimension are accepted: a
- * pre-pass copies A and B into K-major hi/lo arrays in a library-owned
- * workspace of 8*(M+N)*ceil(K/4)*4 bytes per (device, stream), grown with
- * stream-ordered allocation.  M, N, K must be below 2^31.  Every device-side
+ * pre-pass splits A and B (B transposed) into a library-owned workspace of
+ * about 8*(M+N)*ceil(K/4)*4 bytes per (device, stream), grown with
+ * stream-ordered allocation (see below for splitting A in the kernel
+ * instead).  Grids smaller than half the GPU are split along K (partials in
+ * the same workspace).  M, N, K must be below 2^31.  Every device-side
  * wait gives up after 1 s: the kernel then stores nothing to C and records
  * the event, which sgemm_device_status reports.
  */
 sgemm_status sgemm_tf32x3(int64_t M, int64_t N, int64_t K, float alpha,
                           const float *A, int64_t lda, const float *B, int64_t ldb,
                           float beta, float *C, int64_t ldc, void *stream);
+
+/*
+ * 3xTF32 with B packed once.  The tensor cores read both operands K-major,
+ * and B is stored K x N (N-major), so sgemm_tf32x3 transposes and splits B
+ * into TF32 hi/lo parts on every call; these calls let a B that is
+ * multiplied many times (weights) be packed once.  A is split per call, in a
+ * pre-pass (default) or, with SGEMM_TF32X3_FUSE_A=1 in the environment and
+ * A 16-byte aligned with lda % 4 == 0, inside the kernel's shared-memory
+ * stage (the raw fp32 tile arrives by TMA and is split in place; no HBM pass
+ * over A).  The in-kernel split is measured slower on GB300 and so is off by
+ * default.
+ *
+ * sgemm_tf32x3_packed_b_bytes -- size of the packed form of a K x N matrix
+ *   (0 for K or N <= 0).
+ * sgemm_tf32x3_pack_b -- writes the packed form of B (K x N, row-major,
+ *   ldb >= N, device pointer) into `packed` (device, 256-byte aligned,
+ *   packed_bytes >= sgemm_tf32x3_packed_b_bytes(K, N)), asynchronously on
+ *   `stream`.  SGEMM_ERR_MISALIGNED for a misaligned `packed`,
+ *   SGEMM_ERR_WORKSPACE when packed_bytes is too small.
+ * sgemm_tf32x3_packed -- C = alpha*A*B + beta*C with B given in packed form
+ *   (made by sgemm_tf32x3_pack_b with the same K and N).  A must be 16-byte
+ *   aligned with lda % 4 == 0 (SGEMM_ERR_MISALIGNED otherwise).  Accuracy,
+ *   workspace (A's hi/lo and split-K partials) and bounded waits as
+ *   sgemm_tf32x3.
+ */
+size_t sgemm_tf32x3_packed_b_bytes(int64_t K, int64_t N);
+sgemm_status sgemm_tf32x3_pack_b(int64_t K, int64_t N, const float *B, int64_t ldb,
+                                 void *packed, size_t packed_bytes, void *stream);
+sgemm_status sgemm_tf32x3_packed(int64_t M, int64_t N, int64_t K, float alpha,
+                                 const float *A, int64_t lda, const void *packed_b,
+                                 float beta, float *C, int64_t ldc, void *stream);
 
 /*
  * sgemm_device_status -- synchronises `stream`, then reports (and clears)

@@ -131,6 +131,32 @@ def test_forced_split(sg, monkeypatch, split):
     check(q, run(sg, q), exact=True)        # 10 K blocks: split 16 leaves empty ranges
 
 
+@pytest.mark.parametrize("name", ["square1024ab", "ragged", "gpt2_mlp_down", "long_k",
+                                  "square256_int"])
+def test_in_kernel_split_of_a(sg, monkeypatch, name):
+    """SGEMM_TF32X3_FUSE_A=1: A split in shared memory (when its stride allows TMA)."""
+    monkeypatch.setenv("SGEMM_TF32X3_FUSE_A", "1")
+    p = workloads.workload(name)
+    check(p, run(sg, p), exact=p.meta["dist"] == "int4")
+    q = workloads.make(200, 300, 72, dist="int4", seed=81, alpha=1.5, beta=0.5, c0_dist="int4")
+    check(q, run(sg, q), exact=True)
+
+
+def test_in_kernel_split_bounded_waits(sg, monkeypatch):
+    import torch
+    monkeypatch.setenv("SGEMM_TF32X3_FUSE_A", "1")
+    M, N, K = 256, 512, 128
+    A = torch.ones((M, K), device="cuda")
+    B = torch.ones((K, N), device="cuda")
+    C = torch.full((M, N), 3.0, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    rc = sg.tf32x3_stall_selftest(M, N, K, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N,
+                                  20000, stream)
+    assert rc == 5
+    assert bool((C == 3.0).all())
+    assert sg.device_status(stream) == 0
+
+
 def test_split_plans_for_small_grids(sg):
     # these run with more K ranges than tiles; parity at full size
     for name in ("long_k", "gpt2_mlp_down", "square1024ab"):
@@ -225,6 +251,54 @@ def test_bounded_waits_expire_cleanly(sg):
                         stream)
     assert sg.device_status(stream) == 0
     assert bool((C == float(K)).all())
+
+
+@pytest.mark.parametrize("fuse", ["0", "1"])
+@pytest.mark.parametrize("M,N,K", [(1024, 768, 3072), (300, 520, 1000), (128, 256, 32),
+                                   (1, 33, 7), (1024, 1024, 16384)])
+def test_packed_b_reused_for_two_a(sg, monkeypatch, M, N, K, fuse):
+    import torch
+    monkeypatch.setenv("SGEMM_TF32X3_FUSE_A", fuse)
+    stream = torch.cuda.current_stream().cuda_stream
+    lda = (K + 3) // 4 * 4          # the packed call needs a 16-byte row stride for A
+    p1 = workloads.make(M, N, K, seed=71, beta=0.5, c0_dist="uniform", alpha=1.25, lda=lda)
+    p2 = workloads.make(M, N, K, seed=72, lda=lda)
+    B = torch.from_numpy(p1.B).cuda()
+    nbytes = sg.tf32x3_packed_b_bytes(K, N)
+    assert nbytes >= 2 * N * K * 4
+    packed = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    sg.tf32x3_pack_b_ptr(K, N, B.data_ptr(), p1.ldb, packed.data_ptr(), nbytes, stream)
+    for p in (p1, p2):
+        p.B = p1.B                       # both products use the packed B
+        A = torch.from_numpy(p.A).cuda()
+        C = torch.from_numpy(p.C0).cuda()
+        sg.sgemm_tf32x3_packed_ptr(p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, packed.data_ptr(),
+                                   p.beta, C.data_ptr(), p.ldc, stream)
+        assert sg.device_status(stream) == 0
+        check(p, C.cpu().numpy()[:, :p.N], exact=False)
+
+
+def test_packed_b_integer_exact_and_errors(sg):
+    import torch
+    stream = torch.cuda.current_stream().cuda_stream
+    p = workloads.make(257, 300, 96, dist="int4", seed=73, alpha=1.5, beta=0.5, c0_dist="int4")
+    B = torch.from_numpy(p.B).cuda()
+    nbytes = sg.tf32x3_packed_b_bytes(p.K, p.N)
+    packed = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    sg.tf32x3_pack_b_ptr(p.K, p.N, B.data_ptr(), p.ldb, packed.data_ptr(), nbytes, stream)
+    A = torch.from_numpy(p.A).cuda()
+    C = torch.from_numpy(p.C0).cuda()
+    sg.sgemm_tf32x3_packed_ptr(p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, packed.data_ptr(),
+                               p.beta, C.data_ptr(), p.ldc, stream)
+    check(p, C.cpu().numpy()[:, :p.N], exact=True)
+    with pytest.raises(sg.SgemmError) as e:        # A not 16-byte aligned
+        sg.sgemm_tf32x3_packed_ptr(p.M, p.N, p.K, 1.0, A.data_ptr() + 4, p.lda, packed.data_ptr(),
+                                   0.0, C.data_ptr(), p.ldc, stream)
+    assert e.value.status == 2
+    with pytest.raises(sg.SgemmError) as e:        # packed buffer too small
+        sg.tf32x3_pack_b_ptr(p.K, p.N, B.data_ptr(), p.ldb, packed.data_ptr(), nbytes - 4, stream)
+    assert e.value.status == 7
+    assert sg.tf32x3_packed_b_bytes(0, 5) == 0
 
 
 def test_torch_api(sg):
