@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 
 #include "ffma_kernel.cuh"
 #include "sgemm_internal.h"
@@ -75,9 +76,23 @@ cudaError_t launch_ffma(const GemmArgs &a, int kernel, bool vec, bool edge, bool
     if (trans_a) return trans_b ? launch_ffma_tt(a, vec, edge, stream)
                                 : launch_ffma_tn(a, vec, edge, stream);
     if (trans_b) return launch_ffma_nt(a, vec, edge, stream);
+    // Plain products can run either instantiation (the extended one with
+    // batch 1, no bias, no activation computes the same thing).  ptxas
+    // allocates the two differently, and measured on GB300 neither wins
+    // everywhere: the extended build is faster for full tiles without
+    // split-K (8192^3: 60.8 against 60.0 TFLOP/s) and for bounds-checked
+    // vector split-K (1024x1024x16384: 47.0 against 45.4); the plain build
+    // for full-tile split-K (GPT-2 QKV 41.8 against 39.9, 1024^3 31.5
+    // against 29.7).  SGEMM_FFMA_EXT=0/1 overrides the choice for sweeps.
+    const bool split = a.split_k > 1 || a.tail_split > 1;
+    bool ext = a.batch > 1 || a.bias != nullptr || a.act != kActNone;
+    bool pick_ext = (!edge && !split) || (edge && vec && split);
+    if (const char *force = std::getenv("SGEMM_FFMA_EXT")) pick_ext = std::atoi(force) != 0;
+    if (ext || (kernel != kKernelFfma2x128 && pick_ext))
+        return ffma::launch_layout<false, false, false, true>(a, vec, edge, stream);
     return kernel == kKernelFfma2x128
-               ? ffma::launch_layout<true, false, false>(a, vec, edge, stream)
-               : ffma::launch_layout<false, false, false>(a, vec, edge, stream);
+               ? ffma::launch_layout<true, false, false, false>(a, vec, edge, stream)
+               : ffma::launch_layout<false, false, false, false>(a, vec, edge, stream);
 }
 
 cudaError_t launch_scale(float *C, int64_t M, int64_t N, int64_t ldc, float beta,
@@ -113,7 +128,8 @@ cudaError_t launch_ffma_probe(int64_t ctas, int64_t iters, bool packed, float *o
 
 cudaError_t ffma_kernel_attributes(cudaFuncAttributes *attr) {
     return cudaFuncGetAttributes(attr,
-                                 ffma::ffma_gemm_kernel<false, true, false, false, false, false>);
+                                 ffma::ffma_gemm_kernel<false, true, false, false, false, false,
+                                                        false>);
 }
 
 }  // namespace sgemm_impl

@@ -5,7 +5,7 @@
 namespace sgemm_impl {
 
 cudaError_t launch_ffma_nt(const GemmArgs &a, bool vec, bool edge, cudaStream_t stream) {
-    return ffma::launch_layout<false, false, true>(a, vec, edge, stream);
+    return ffma::launch_layout<false, false, true, true>(a, vec, edge, stream);
 }
 
 }  // namespace sgemm_impl

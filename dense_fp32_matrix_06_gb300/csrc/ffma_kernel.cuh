@@ -159,7 +159,10 @@ __device__ __forceinline__ WorkItem work_item(const GemmArgs &p, int64_t pid) {
     return w;
 }
 
-template <bool kPacked, bool kVec, bool kEdge, bool kSplit, bool kTransA, bool kTransB>
+// kExt: batches, bias and activation are compiled in (sgemm_ex); the plain
+// product (sgemm) is built without them, which leaves it more registers.
+template <bool kPacked, bool kVec, bool kEdge, bool kSplit, bool kTransA, bool kTransB,
+          bool kExt>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 ffma_gemm_kernel(const GemmArgs p) {
     // A tile: As[k][m]; swizzled when filled by transposing stores (A not transposed)
@@ -185,8 +188,8 @@ ffma_gemm_kernel(const GemmArgs p) {
         col0 = w.col0;
         kbeg = w.kbeg;
         kend = w.kend;
-        Ab = p.A + w.batch * p.strideA;
-        Bb = p.B + w.batch * p.strideB;
+        Ab = kExt ? p.A + w.batch * p.strideA : p.A;
+        Bb = kExt ? p.B + w.batch * p.strideB : p.B;
     }
     const int nslices = kend > kbeg ? int((kend - kbeg + kBK - 1) / kBK) : 0;
 
@@ -361,12 +364,27 @@ ffma_gemm_kernel(const GemmArgs p) {
                     for (int j = 0; j < 4; ++j) acc[i][j] = __ffma2_rn(ai, b[j], acc[i][j]);
                 }
             } else {
+                // Boustrophedon order over the 8 x 8 block: along row i the
+                // FMAs share a[i]; odd rows run right to left (column pairs
+                // and the two columns of a pair reversed), so the last FMA of
+                // a row and the first of the next share b[j].  Every two
+                // consecutive FMAs thus share a source operand, which the
+                // operand reuse path can serve; measured on GB300 this order
+                // is 1-2 % faster than plain row order and 5-8 % faster than
+                // column order.  The order of the k steps, and so every
+                // accumulator's rounding sequence, is unchanged.
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        acc[i][j].x = fmaf(a[i], b[j].x, acc[i][j].x);
-                        acc[i][j].y = fmaf(a[i], b[j].y, acc[i][j].y);
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int j = (i & 1) ? 3 - jj : jj;
+                        if (i & 1) {
+                            acc[i][j].y = fmaf(a[i], b[j].y, acc[i][j].y);
+                            acc[i][j].x = fmaf(a[i], b[j].x, acc[i][j].x);
+                        } else {
+                            acc[i][j].x = fmaf(a[i], b[j].x, acc[i][j].x);
+                            acc[i][j].y = fmaf(a[i], b[j].y, acc[i][j].y);
+                        }
                     }
                 }
             }
@@ -429,9 +447,9 @@ ffma_gemm_kernel(const GemmArgs p) {
     // ---- epilogue: C = act(alpha * acc (+ beta * C_old) (+ bias)) ----
     const float alpha = p.alpha, beta = p.beta;
     float *Cb = p.C;
-    if (p.batch > 1) Cb += work_item(p, blockIdx.x).batch * p.strideC;
-    const float *bias = p.bias;
-    const int act = p.act;
+    if (kExt && p.batch > 1) Cb += work_item(p, blockIdx.x).batch * p.strideC;
+    const float *bias = kExt ? p.bias : nullptr;
+    const int act = kExt ? p.act : kActNone;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int64_t row = row0 + (i < 4 ? tm * 4 + i : 64 + tm * 4 + (i - 4));
@@ -479,30 +497,31 @@ ffma_gemm_kernel(const GemmArgs p) {
     }
 }
 
-template <bool kPacked, bool kVec, bool kEdge, bool kSplit, bool kTransA, bool kTransB>
+template <bool kPacked, bool kVec, bool kEdge, bool kSplit, bool kTransA, bool kTransB,
+          bool kExt>
 cudaError_t launch_variant(const GemmArgs &a, cudaStream_t stream) {
     const int64_t tiles = int64_t(a.tiles_m) * a.tiles_n * a.batch;
     const dim3 grid(unsigned(a.tail_start * a.split_k + (tiles - a.tail_start) * a.tail_split),
                     1, 1);
-    ffma_gemm_kernel<kPacked, kVec, kEdge, kSplit, kTransA, kTransB>
+    ffma_gemm_kernel<kPacked, kVec, kEdge, kSplit, kTransA, kTransB, kExt>
         <<<grid, kThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
 // All (vec, edge, split) variants of one layout and issue form.
-template <bool kPacked, bool kTransA, bool kTransB>
+template <bool kPacked, bool kTransA, bool kTransB, bool kExt>
 cudaError_t launch_layout(const GemmArgs &a, bool vec, bool edge, cudaStream_t stream) {
     const bool split = a.split_k > 1 || a.tail_split > 1;
     if (!edge) {
         // full tiles are only planned on the vector path
-        return split ? launch_variant<kPacked, true, false, true, kTransA, kTransB>(a, stream)
-                     : launch_variant<kPacked, true, false, false, kTransA, kTransB>(a, stream);
+        return split ? launch_variant<kPacked, true, false, true, kTransA, kTransB, kExt>(a, stream)
+                     : launch_variant<kPacked, true, false, false, kTransA, kTransB, kExt>(a, stream);
     }
     if (vec)
-        return split ? launch_variant<kPacked, true, true, true, kTransA, kTransB>(a, stream)
-                     : launch_variant<kPacked, true, true, false, kTransA, kTransB>(a, stream);
-    return split ? launch_variant<kPacked, false, true, true, kTransA, kTransB>(a, stream)
-                 : launch_variant<kPacked, false, true, false, kTransA, kTransB>(a, stream);
+        return split ? launch_variant<kPacked, true, true, true, kTransA, kTransB, kExt>(a, stream)
+                     : launch_variant<kPacked, true, true, false, kTransA, kTransB, kExt>(a, stream);
+    return split ? launch_variant<kPacked, false, true, true, kTransA, kTransB, kExt>(a, stream)
+                 : launch_variant<kPacked, false, true, false, kTransA, kTransB, kExt>(a, stream);
 }
 
 }  // namespace ffma
