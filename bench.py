@@ -344,8 +344,10 @@ def run_ours(args):
         tc = run_tf32x3(sg, p, A, B, C, stream, args, dist, device)
 
     extras = None
+    per_config = None
     if not args.no_extras and rank == 0:
         extras = run_extras(sg, device, stream)
+        per_config = run_configs(sg, device, stream)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -372,6 +374,8 @@ def run_ours(args):
             line["tf32x3"] = tc
         if extras:
             line["sgemm_ex"] = extras
+        if per_config:
+            line["workloads"] = per_config
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -587,6 +591,49 @@ def run_extras(sg, device, stream):
                      "op": ("T" if op_a else "N") + ("T" if op_b else "N"), "batch": batch,
                      "bias": has_bias, "act": "gelu_tanh" if act else None}
         del A, B, C, bias
+    return out
+
+
+def run_configs(sg, device, stream):
+    """TFLOP/s of sgemm and sgemm_tf32x3 on every configured workload (inputs
+    resident, CUDA events, median; workloads under 200 MB get the L2 flushed
+    between repetitions)."""
+    import torch
+    sh = stream.cuda_stream
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    out = {}
+    for name in workloads.WORKLOADS:
+        p = workloads.workload(name)
+        A = torch.from_numpy(p.A).to(device)
+        B = torch.from_numpy(p.B).to(device)
+        C = torch.from_numpy(p.C0).to(device)
+        small = p.A.nbytes + p.B.nbytes + p.C0.nbytes < 200 << 20
+        res = {}
+        for mode, fn in (("ffma", sg.sgemm_ptr), ("tf32x3", sg.sgemm_tf32x3_ptr)):
+            def call():
+                fn(p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
+                   C.data_ptr(), p.ldc, sh)
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize(device)
+            reps = max(5, min(40, int(1e12 / p.flops)))
+            ts = []
+            for _ in range(reps):
+                if small:
+                    flush.zero_()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                call()
+                e1.record(stream)
+                torch.cuda.synchronize(device)
+                ts.append(e0.elapsed_time(e1) / 1e3)
+            ts.sort()
+            res[mode] = round(p.flops / ts[len(ts) // 2] / 1e12, 3)
+        res["shape"] = f"{p.M}x{p.N}x{p.K}"
+        res["l2_flushed"] = small
+        out[name] = res
+        del A, B, C
     return out
 
 
