@@ -71,11 +71,16 @@ __global__ void __launch_bounds__(256) ffma_probe_kernel(int64_t iters, float *o
 
 }  // namespace
 
-cudaError_t launch_ffma(const GemmArgs &a, int kernel, bool vec, bool edge, bool trans_a,
-                        bool trans_b, cudaStream_t stream) {
-    if (trans_a) return trans_b ? launch_ffma_tt(a, vec, edge, stream)
-                                : launch_ffma_tn(a, vec, edge, stream);
-    if (trans_b) return launch_ffma_nt(a, vec, edge, stream);
+cudaError_t launch_ffma(const GemmArgs &a, int kernel, int tile, bool vec, bool edge,
+                        bool trans_a, bool trans_b, cudaStream_t stream) {
+    if (trans_a) return trans_b ? launch_ffma_tt(a, tile, vec, edge, stream)
+                                : launch_ffma_tn(a, tile, vec, edge, stream);
+    if (trans_b) return launch_ffma_nt(a, tile, vec, edge, stream);
+    const bool ext = a.batch > 1 || a.bias != nullptr || a.act != kActNone;
+    if (tile == kSmallTile)
+        return ext ? ffma::launch_layout<kSmallTile, false, false, false, true>(a, vec, edge, stream)
+                   : ffma::launch_layout<kSmallTile, false, false, false, false>(a, vec, edge,
+                                                                                 stream);
     // Plain products can run either instantiation (the extended one with
     // batch 1, no bias, no activation computes the same thing).  ptxas
     // allocates the two differently, and measured on GB300 neither wins
@@ -85,14 +90,13 @@ cudaError_t launch_ffma(const GemmArgs &a, int kernel, bool vec, bool edge, bool
     // for full-tile split-K (GPT-2 QKV 41.8 against 39.9, 1024^3 31.5
     // against 29.7).  SGEMM_FFMA_EXT=0/1 overrides the choice for sweeps.
     const bool split = a.split_k > 1 || a.tail_split > 1;
-    bool ext = a.batch > 1 || a.bias != nullptr || a.act != kActNone;
     bool pick_ext = (!edge && !split) || (edge && vec && split);
     if (const char *force = std::getenv("SGEMM_FFMA_EXT")) pick_ext = std::atoi(force) != 0;
     if (ext || (kernel != kKernelFfma2x128 && pick_ext))
-        return ffma::launch_layout<false, false, false, true>(a, vec, edge, stream);
+        return ffma::launch_layout<128, false, false, false, true>(a, vec, edge, stream);
     return kernel == kKernelFfma2x128
-               ? ffma::launch_layout<true, false, false, false>(a, vec, edge, stream)
-               : ffma::launch_layout<false, false, false, false>(a, vec, edge, stream);
+               ? ffma::launch_layout<128, true, false, false, false>(a, vec, edge, stream)
+               : ffma::launch_layout<128, false, false, false, false>(a, vec, edge, stream);
 }
 
 cudaError_t launch_scale(float *C, int64_t M, int64_t N, int64_t ldc, float beta,
@@ -128,8 +132,8 @@ cudaError_t launch_ffma_probe(int64_t ctas, int64_t iters, bool packed, float *o
 
 cudaError_t ffma_kernel_attributes(cudaFuncAttributes *attr) {
     return cudaFuncGetAttributes(attr,
-                                 ffma::ffma_gemm_kernel<false, true, false, false, false, false,
-                                                        false>);
+                                 ffma::ffma_gemm_kernel<128, false, true, false, false, false,
+                                                        false, false>);
 }
 
 }  // namespace sgemm_impl

@@ -4,8 +4,11 @@
 
 namespace sgemm_impl {
 
-cudaError_t launch_ffma_tt(const GemmArgs &a, bool vec, bool edge, cudaStream_t stream) {
-    return ffma::launch_layout<false, true, true, true>(a, vec, edge, stream);
+cudaError_t launch_ffma_tt(const GemmArgs &a, int tile, bool vec, bool edge,
+                           cudaStream_t stream) {
+    return tile == kSmallTile
+               ? ffma::launch_layout<kSmallTile, false, true, true, true>(a, vec, edge, stream)
+               : ffma::launch_layout<128, false, true, true, true>(a, vec, edge, stream);
 }
 
 }  // namespace sgemm_impl

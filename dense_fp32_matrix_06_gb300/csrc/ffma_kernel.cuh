@@ -103,13 +103,31 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // aligned group of 4 columns stays contiguous (fragment reads stay 128-bit)
 // and the stores of a warp -- 8 rows x 4 k groups -- hit all 32 banks.  A tile
 // filled by row copies needs no swizzle.
-template <bool kSwizzle>
+template <bool kSwizzle, int kKG = 4, int kShift = 3>
 __device__ __forceinline__ int tcol(int k, int x) {
     if constexpr (kSwizzle)
-        return x ^ (((k >> 2) & 3) << 3);
+        return x ^ (((k >> 2) & (kKG - 1)) << kShift);
     else
         return x;
 }
+
+// A square CTA tile of T x T outputs with K slices of T/8: 8 x 8 accumulators
+// per thread in four 4 x 4 quadrants T/2 apart, (T/8)^2 threads, warps of 4
+// (M) x 8 (N) threads.  With K slices of T/8 every thread stages exactly two
+// float4 of each operand per slice, whatever T is.  T = 128 is the main
+// tile; T = 64 serves grids too small to fill the GPU with 128-wide tiles.
+template <int T>
+struct TileCfg {
+    static constexpr int kT = T;
+    static constexpr int kBK = T / 8;
+    static constexpr int kThreads = (T / 8) * (T / 8);
+    static constexpr int kWarpsN = T / 64;              // warps along N
+    static constexpr int kKG = kBK / 4;                 // 4-wide k groups per slice
+    static constexpr int kShift = kKG == 4 ? 3 : 4;     // log2(32 / kKG)
+    static constexpr int kCopyRows = T / 16;            // tile rows per copy pass
+    static constexpr int kMinBlocks = T == 128 ? 2 : 8; // resident CTAs per SM
+    static_assert(T == 128 || T == 64, "tile is 128 or 64");
+};
 
 // The tanh form of GELU used by GPT-2: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
 __device__ __forceinline__ float gelu_tanh(float x) {
@@ -127,7 +145,7 @@ struct WorkItem {
     int split, nsplit;
 };
 
-__device__ __forceinline__ WorkItem work_item(const GemmArgs &p, int64_t pid) {
+__device__ __forceinline__ WorkItem work_item(const GemmArgs &p, int64_t pid, int tile) {
     WorkItem w;
     const int64_t lead = p.tail_start * p.split_k;
     int64_t kps;
@@ -152,8 +170,8 @@ __device__ __forceinline__ WorkItem work_item(const GemmArgs &p, int64_t pid) {
     const int64_t first_m = group * kGroupM;
     const int64_t gm = min(int64_t(p.tiles_m) - first_m, int64_t(kGroupM));
     const int64_t in_group = t - group * per_group;
-    w.row0 = (first_m + in_group % gm) * kBM;
-    w.col0 = (in_group / gm) * kBN;
+    w.row0 = (first_m + in_group % gm) * tile;
+    w.col0 = (in_group / gm) * tile;
     w.kbeg = int64_t(w.split) * kps;
     w.kend = min(p.K, w.kbeg + kps);
     return w;
@@ -161,16 +179,18 @@ __device__ __forceinline__ WorkItem work_item(const GemmArgs &p, int64_t pid) {
 
 // kExt: batches, bias and activation are compiled in (sgemm_ex); the plain
 // product (sgemm) is built without them, which leaves it more registers.
-template <bool kPacked, bool kVec, bool kEdge, bool kSplit, bool kTransA, bool kTransB,
-          bool kExt>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+template <int kTile, bool kPacked, bool kVec, bool kEdge, bool kSplit, bool kTransA,
+          bool kTransB, bool kExt>
+__global__ void __launch_bounds__(TileCfg<kTile>::kThreads, TileCfg<kTile>::kMinBlocks)
 ffma_gemm_kernel(const GemmArgs p) {
+    using TC = TileCfg<kTile>;
+    constexpr int T = TC::kT, BK = TC::kBK, NT = TC::kThreads, KG = TC::kKG, SH = TC::kShift;
     // A tile: As[k][m]; swizzled when filled by transposing stores (A not transposed)
     // B tile: Bs[k][n]; swizzled when filled by transposing stores (B transposed)
     constexpr bool kSwzA = !kTransA;
     constexpr bool kSwzB = kTransB;
-    __shared__ __align__(16) float As[2][kBK][kBM];
-    __shared__ __align__(16) float Bs[2][kBK][kBN];
+    __shared__ __align__(16) float As[2][BK][T];
+    __shared__ __align__(16) float Bs[2][BK][T];
     __shared__ int s_last;
 
     const int tid = threadIdx.x;
@@ -183,7 +203,7 @@ ffma_gemm_kernel(const GemmArgs p) {
     const float *Ab;
     const float *Bb;
     {
-        const WorkItem w = work_item(p, blockIdx.x);
+        const WorkItem w = work_item(p, blockIdx.x, T);
         row0 = w.row0;
         col0 = w.col0;
         kbeg = w.kbeg;
@@ -191,21 +211,21 @@ ffma_gemm_kernel(const GemmArgs p) {
         Ab = kExt ? p.A + w.batch * p.strideA : p.A;
         Bb = kExt ? p.B + w.batch * p.strideB : p.B;
     }
-    const int nslices = kend > kbeg ? int((kend - kbeg + kBK - 1) / kBK) : 0;
+    const int nslices = kend > kbeg ? int((kend - kbeg + BK - 1) / BK) : 0;
 
     // ---- compute mapping: warp = 4 (M) x 8 (N) threads ----
-    const int tm = (warp >> 1) * 4 + (lane >> 3);   // 0..15
-    const int tn = (warp & 1) * 8 + (lane & 7);     // 0..15
+    const int tm = (warp / TC::kWarpsN) * 4 + (lane >> 3);   // 0..T/8-1
+    const int tn = (warp % TC::kWarpsN) * 8 + (lane & 7);    // 0..T/8-1
 
     // ---- load mapping ----
-    // transposing operand (rows along K): rows r and r + 64 of the tile, k group
-    // kc (4 consecutive k): a warp reads 8 rows x 64 contiguous bytes per load.
-    const int t_row = tid >> 2;              // 0..63
-    const int t_kc = tid & 3;                // 0..3
-    // copied operand (rows along M or N): tile rows k and k + 8, 4 elements at
-    // c_col: a warp copies one 512-byte row segment.
-    const int c_row = tid >> 5;              // 0..7
-    const int c_col = (tid & 31) * 4;        // 0..124
+    // transposing operand (rows along K): rows r and r + T/2 of the tile, k
+    // group kc (4 consecutive k): a warp reads 32/KG rows x KG*16 bytes a load.
+    const int t_row = tid / KG;              // 0..T/2-1
+    const int t_kc = tid % KG;               // 0..KG-1
+    // copied operand (rows along M or N): tile rows k and k + T/16, 4 elements
+    // at c_col.
+    const int c_row = tid / (T / 4);         // 0..T/16-1
+    const int c_col = (tid % (T / 4)) * 4;   // 0..T-4
 
     // A
     bool a_ok[2];
@@ -213,7 +233,7 @@ ffma_gemm_kernel(const GemmArgs p) {
     if constexpr (!kTransA) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int64_t r = row0 + t_row + 64 * h;
+            const int64_t r = row0 + t_row + (T / 2) * h;
             a_ok[h] = !kEdge || r < p.M;
             a_ptr[h] = Ab + (a_ok[h] ? r : 0) * p.lda + kbeg + t_kc * 4;
         }
@@ -228,7 +248,7 @@ ffma_gemm_kernel(const GemmArgs p) {
     if constexpr (kTransB) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int64_t n = col0 + t_row + 64 * h;
+            const int64_t n = col0 + t_row + (T / 2) * h;
             b_ok[h] = !kEdge || n < p.N;
             b_ptr[h] = Bb + (b_ok[h] ? n : 0) * p.ldb + kbeg + t_kc * 4;
         }
@@ -242,7 +262,7 @@ ffma_gemm_kernel(const GemmArgs p) {
 
     // rows along K -> registers (zero outside the matrix and outside [kbeg, kend))
     auto fetch_t = [&](int t, const bool (&ok)[2], const float *const (&ptr)[2], float4 (&r)[2]) {
-        const int64_t koff = int64_t(t) * kBK;
+        const int64_t koff = int64_t(t) * BK;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const float *src = ptr[h] + koff;
@@ -262,29 +282,29 @@ ffma_gemm_kernel(const GemmArgs p) {
         }
     };
     // registers -> tile rows k..k+3, transposed and swizzled
-    auto stash_t = [&](float (*T)[kBM], const float4 (&r)[2]) {
+    auto stash_t = [&](float (*S)[T], const float4 (&r)[2]) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int x = t_row + 64 * h;
+            const int x = t_row + (T / 2) * h;
             const int k = t_kc * 4;
-            T[k + 0][tcol<true>(k, x)] = r[h].x;
-            T[k + 1][tcol<true>(k, x)] = r[h].y;
-            T[k + 2][tcol<true>(k, x)] = r[h].z;
-            T[k + 3][tcol<true>(k, x)] = r[h].w;
+            S[k + 0][tcol<true, KG, SH>(k, x)] = r[h].x;
+            S[k + 1][tcol<true, KG, SH>(k, x)] = r[h].y;
+            S[k + 2][tcol<true, KG, SH>(k, x)] = r[h].z;
+            S[k + 3][tcol<true, KG, SH>(k, x)] = r[h].w;
         }
     };
     // rows along M/N -> tile, async copies (zero-filled outside); `lim` is M or N
-    auto copy_c = [&](int t, float (*T)[kBM], const float *base, int64_t ld, int64_t x0,
+    auto copy_c = [&](int t, float (*S)[T], const float *base, int64_t ld, int64_t x0,
                       int64_t lim, const float *dummy) {
-        const int64_t koff = int64_t(t) * kBK;
+        const int64_t koff = int64_t(t) * BK;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const float *src = base + (koff + 8 * h) * ld;
-            float *dst = &T[c_row + 8 * h][c_col];
+            const float *src = base + (koff + TC::kCopyRows * h) * ld;
+            float *dst = &S[c_row + TC::kCopyRows * h][c_col];
             if constexpr (!kEdge) {
                 cp_async16(dst, src, 16);
             } else {
-                const int64_t k = kbeg + koff + c_row + 8 * h;
+                const int64_t k = kbeg + koff + c_row + TC::kCopyRows * h;
                 const int64_t c = x0 + c_col;
                 const bool k_ok = k < kend;
                 if constexpr (kVec) {
@@ -333,22 +353,24 @@ ffma_gemm_kernel(const GemmArgs p) {
         if (more) issue(t + 1, page ^ 1);
 
         float4 af[2][2], bf[2][2];
-        af[0][0] = *reinterpret_cast<const float4 *>(&As[page][0][tcol<kSwzA>(0, tm * 4)]);
-        af[0][1] = *reinterpret_cast<const float4 *>(&As[page][0][tcol<kSwzA>(0, 64 + tm * 4)]);
-        bf[0][0] = *reinterpret_cast<const float4 *>(&Bs[page][0][tcol<kSwzB>(0, tn * 4)]);
-        bf[0][1] = *reinterpret_cast<const float4 *>(&Bs[page][0][tcol<kSwzB>(0, 64 + tn * 4)]);
+        af[0][0] = *reinterpret_cast<const float4 *>(&As[page][0][tcol<kSwzA, KG, SH>(0, tm * 4)]);
+        af[0][1] = *reinterpret_cast<const float4 *>(
+            &As[page][0][tcol<kSwzA, KG, SH>(0, T / 2 + tm * 4)]);
+        bf[0][0] = *reinterpret_cast<const float4 *>(&Bs[page][0][tcol<kSwzB, KG, SH>(0, tn * 4)]);
+        bf[0][1] = *reinterpret_cast<const float4 *>(
+            &Bs[page][0][tcol<kSwzB, KG, SH>(0, T / 2 + tn * 4)]);
 #pragma unroll
-        for (int kk = 0; kk < kBK; ++kk) {
+        for (int kk = 0; kk < BK; ++kk) {
             const int cur = kk & 1;
-            if (kk + 1 < kBK) {
+            if (kk + 1 < BK) {
                 af[cur ^ 1][0] = *reinterpret_cast<const float4 *>(
-                    &As[page][kk + 1][tcol<kSwzA>(kk + 1, tm * 4)]);
+                    &As[page][kk + 1][tcol<kSwzA, KG, SH>(kk + 1, tm * 4)]);
                 af[cur ^ 1][1] = *reinterpret_cast<const float4 *>(
-                    &As[page][kk + 1][tcol<kSwzA>(kk + 1, 64 + tm * 4)]);
+                    &As[page][kk + 1][tcol<kSwzA, KG, SH>(kk + 1, T / 2 + tm * 4)]);
                 bf[cur ^ 1][0] = *reinterpret_cast<const float4 *>(
-                    &Bs[page][kk + 1][tcol<kSwzB>(kk + 1, tn * 4)]);
+                    &Bs[page][kk + 1][tcol<kSwzB, KG, SH>(kk + 1, tn * 4)]);
                 bf[cur ^ 1][1] = *reinterpret_cast<const float4 *>(
-                    &Bs[page][kk + 1][tcol<kSwzB>(kk + 1, 64 + tn * 4)]);
+                    &Bs[page][kk + 1][tcol<kSwzB, KG, SH>(kk + 1, T / 2 + tn * 4)]);
             }
             const float a[8] = {af[cur][0].x, af[cur][0].y, af[cur][0].z, af[cur][0].w,
                                 af[cur][1].x, af[cur][1].y, af[cur][1].z, af[cur][1].w};
@@ -395,20 +417,20 @@ ffma_gemm_kernel(const GemmArgs p) {
 
     // ---- split-K: last CTA of the tile reduces the partials in order ----
     if constexpr (kSplit) {
-        const WorkItem w = work_item(p, blockIdx.x);
+        const WorkItem w = work_item(p, blockIdx.x, T);
         if (w.nsplit > 1) {
             const int S = w.nsplit;
             const int split = w.split;
             const int64_t pid = blockIdx.x;
             float4 *part = reinterpret_cast<float4 *>(p.partials);
             // slots of this tile's ranges are consecutive, starting at pid - split
-            const size_t tile_base = size_t(pid - split - p.part_base) * 16 * kThreads;
-            float4 *mine = part + tile_base + size_t(split) * 16 * kThreads;
+            const size_t tile_base = size_t(pid - split - p.part_base) * 16 * NT;
+            float4 *mine = part + tile_base + size_t(split) * 16 * NT;
             unsigned *counter = p.counters + (w.tile - p.split_base);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int i = j >> 1, h = j & 1;
-                __stcg(mine + j * kThreads + tid,
+                __stcg(mine + j * NT + tid,
                        make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
                                    acc[i][2 * h + 1].y));
             }
@@ -431,7 +453,7 @@ ffma_gemm_kernel(const GemmArgs p) {
                 float4 tot = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                 for (int s = 0; s < S; ++s) {
                     const float4 v =
-                        __ldcg(part + tile_base + size_t(s) * 16 * kThreads + j * kThreads + tid);
+                        __ldcg(part + tile_base + size_t(s) * 16 * NT + j * NT + tid);
                     tot.x += v.x;
                     tot.y += v.y;
                     tot.z += v.z;
@@ -447,17 +469,17 @@ ffma_gemm_kernel(const GemmArgs p) {
     // ---- epilogue: C = act(alpha * acc (+ beta * C_old) (+ bias)) ----
     const float alpha = p.alpha, beta = p.beta;
     float *Cb = p.C;
-    if (kExt && p.batch > 1) Cb += work_item(p, blockIdx.x).batch * p.strideC;
+    if (kExt && p.batch > 1) Cb += work_item(p, blockIdx.x, T).batch * p.strideC;
     const float *bias = kExt ? p.bias : nullptr;
     const int act = kExt ? p.act : kActNone;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int64_t row = row0 + (i < 4 ? tm * 4 + i : 64 + tm * 4 + (i - 4));
+        const int64_t row = row0 + (i < 4 ? tm * 4 + i : T / 2 + tm * 4 + (i - 4));
         if (kEdge && row >= p.M) continue;
         float *crow = Cb + row * p.ldc;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int64_t col = col0 + h * 64 + tn * 4;
+            const int64_t col = col0 + h * (T / 2) + tn * 4;
             float v[4] = {alpha * acc[i][2 * h].x, alpha * acc[i][2 * h].y,
                           alpha * acc[i][2 * h + 1].x, alpha * acc[i][2 * h + 1].y};
             float *cp = crow + col;
@@ -497,31 +519,35 @@ ffma_gemm_kernel(const GemmArgs p) {
     }
 }
 
-template <bool kPacked, bool kVec, bool kEdge, bool kSplit, bool kTransA, bool kTransB,
-          bool kExt>
+template <int kTile, bool kPacked, bool kVec, bool kEdge, bool kSplit, bool kTransA,
+          bool kTransB, bool kExt>
 cudaError_t launch_variant(const GemmArgs &a, cudaStream_t stream) {
     const int64_t tiles = int64_t(a.tiles_m) * a.tiles_n * a.batch;
     const dim3 grid(unsigned(a.tail_start * a.split_k + (tiles - a.tail_start) * a.tail_split),
                     1, 1);
-    ffma_gemm_kernel<kPacked, kVec, kEdge, kSplit, kTransA, kTransB, kExt>
-        <<<grid, kThreads, 0, stream>>>(a);
+    ffma_gemm_kernel<kTile, kPacked, kVec, kEdge, kSplit, kTransA, kTransB, kExt>
+        <<<grid, TileCfg<kTile>::kThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
-// All (vec, edge, split) variants of one layout and issue form.
-template <bool kPacked, bool kTransA, bool kTransB, bool kExt>
+// All (vec, edge, split) variants of one tile, layout and issue form.
+template <int kTile, bool kPacked, bool kTransA, bool kTransB, bool kExt>
 cudaError_t launch_layout(const GemmArgs &a, bool vec, bool edge, cudaStream_t stream) {
     const bool split = a.split_k > 1 || a.tail_split > 1;
     if (!edge) {
         // full tiles are only planned on the vector path
-        return split ? launch_variant<kPacked, true, false, true, kTransA, kTransB, kExt>(a, stream)
-                     : launch_variant<kPacked, true, false, false, kTransA, kTransB, kExt>(a, stream);
+        return split
+                   ? launch_variant<kTile, kPacked, true, false, true, kTransA, kTransB, kExt>(a, stream)
+                   : launch_variant<kTile, kPacked, true, false, false, kTransA, kTransB, kExt>(
+                         a, stream);
     }
     if (vec)
-        return split ? launch_variant<kPacked, true, true, true, kTransA, kTransB, kExt>(a, stream)
-                     : launch_variant<kPacked, true, true, false, kTransA, kTransB, kExt>(a, stream);
-    return split ? launch_variant<kPacked, false, true, true, kTransA, kTransB, kExt>(a, stream)
-                 : launch_variant<kPacked, false, true, false, kTransA, kTransB, kExt>(a, stream);
+        return split
+                   ? launch_variant<kTile, kPacked, true, true, true, kTransA, kTransB, kExt>(a, stream)
+                   : launch_variant<kTile, kPacked, true, true, false, kTransA, kTransB, kExt>(a, stream);
+    return split
+               ? launch_variant<kTile, kPacked, false, true, true, kTransA, kTransB, kExt>(a, stream)
+               : launch_variant<kTile, kPacked, false, true, false, kTransA, kTransB, kExt>(a, stream);
 }
 
 }  // namespace ffma

@@ -75,7 +75,8 @@ sgemm_status check_sizes(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
     if (ldb < (N > 1 ? N : 1)) return SGEMM_ERR_INVALID_ARG;
     if (ldc < (N > 1 ? N : 1)) return SGEMM_ERR_INVALID_ARG;
     // the tile grid is launched as one 1-D grid dimension
-    if (ceil_div(M, kBM) * ceil_div(N, kBN) > int64_t(INT32_MAX)) return SGEMM_ERR_INVALID_ARG;
+    if (ceil_div(M, kSmallTile) * ceil_div(N, kSmallTile) > int64_t(INT32_MAX))
+        return SGEMM_ERR_INVALID_ARG;
     return SGEMM_OK;
 }
 
@@ -83,28 +84,29 @@ sgemm_status check_sizes(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
 // waves * k_per_split, plus a per-CTA cost for writing and re-reading the
 // partial tiles.  Only considered when the tile grid fills less than one wave
 // of resident CTAs.
-int choose_split(int64_t tiles, int64_t K, int sms, int64_t *k_per_split) {
-    const int64_t slots = int64_t(sms) * kCtasPerSm;
-    const int64_t kslices = ceil_div(K, kBK);
+int choose_split(int64_t tiles, int64_t K, int sms, int64_t *k_per_split, int bk = kBK,
+                 int cps = kCtasPerSm) {
+    const int64_t slots = int64_t(sms) * cps;
+    const int64_t kslices = ceil_div(K, bk);
     int best = 1;
-    int64_t best_kps = kslices * kBK;
+    int64_t best_kps = kslices * bk;
     if (const char *force = std::getenv("SGEMM_FORCE_SPLIT")) {
         int s = std::atoi(force);
         if (s >= 1) {
             if (s > kMaxSplit) s = kMaxSplit;
-            int64_t kps = ceil_div(kslices, s) * kBK;
+            int64_t kps = ceil_div(kslices, s) * bk;
             int eff = int(ceil_div(K, kps > 0 ? kps : 1));
             if (eff < 1) eff = 1;
-            if (eff > 1 && tiles > kMaxSplitTiles) eff = 1, kps = kslices * kBK;
-            *k_per_split = eff > 1 ? kps : kslices * kBK;
+            if (eff > 1 && tiles > kMaxSplitTiles) eff = 1, kps = kslices * bk;
+            *k_per_split = eff > 1 ? kps : kslices * bk;
             return eff;
         }
     }
     if (tiles < slots && tiles <= kMaxSplitTiles && K >= 2 * 128) {
         double best_cost = double(ceil_div(tiles, slots)) * double(best_kps);
         for (int s = 2; s <= kMaxSplit; ++s) {
-            const int64_t kps = ceil_div(kslices, s) * kBK;
-            if (kps < 128) break;  // keep at least 8 K slices per partition
+            const int64_t kps = ceil_div(kslices, s) * bk;
+            if (kps < 128) break;  // keep at least 128 of K per partition
             const int eff = int(ceil_div(K, kps));
             const int64_t ctas = tiles * eff;
             const double cost = double(ceil_div(ctas, slots)) * (double(kps) + 8.0 * eff + 32.0);
@@ -145,11 +147,31 @@ void choose_tail(int64_t tiles, int64_t K, int sms, int64_t *tail_start, int *ta
     *tail_kps = kps;
 }
 
-size_t split_workspace(int64_t tiles, int split_k, int64_t tail_start, int tail_split) {
-    if (split_k > 1) return kCounterBytes + size_t(tiles) * split_k * kBM * kBN * sizeof(float);
-    if (tail_split > 1)
-        return kCounterBytes + size_t(tiles - tail_start) * tail_split * kBM * kBN * sizeof(float);
+size_t split_workspace(int64_t tiles, int split_k, int64_t tail_start, int tail_split,
+                       int tile = kBM) {
+    const size_t per = size_t(tile) * tile * sizeof(float);
+    if (split_k > 1) return kCounterBytes + size_t(tiles) * split_k * per;
+    if (tail_split > 1) return kCounterBytes + size_t(tiles - tail_start) * tail_split * per;
     return 0;
+}
+
+// CTA tile for a shape.  64-wide tiles when 128-wide ones would waste 40 % or
+// more of their area on padding (N = 64 attention products), or would fill
+// under half the SMs while K is too short (<= 768) for split-K to make up
+// for it; 128 otherwise.  Measured on GB300 (TFLOP/s, 64 against 128): 256^3
+// 1.33 / 1.14, 1023x777x513 17.8 / 15.7, but 1024^3 28.9 / 31.5,
+// 1024x768x3072 37.8 / 41.9, 1024x1024x16384 40.6 / 47.0.
+// SGEMM_FORCE_TILE=64/128 overrides the choice for sweeps.
+int choose_tile(int64_t M, int64_t N, int64_t K, int64_t batch, int sms) {
+    if (const char *force = std::getenv("SGEMM_FORCE_TILE")) {
+        const int t = std::atoi(force);
+        if (t == 64 || t == 128) return t;
+    }
+    const int64_t per_batch = ceil_div(M, 128) * ceil_div(N, 128);
+    const double used = double(M) * double(N) / (double(per_batch) * 128.0 * 128.0);
+    if (used < 0.6) return kSmallTile;
+    if (2 * per_batch * batch < sms && K <= 768) return kSmallTile;
+    return 128;
 }
 
 // Kernel the planner names: the scalar-FMA kernel unless SGEMM_FORCE_KERNEL
@@ -165,38 +187,41 @@ int32_t default_kernel() {
     return kKernelFfma128;
 }
 
-// Tiling and split choice for `batch` problems of M x N x K; `vec` says
-// whether 16-byte vector access is legal for every operand.
 void plan_core(int64_t M, int64_t N, int64_t K, int64_t batch, bool vec, int sms,
                gemm_plan_t *out) {
     gemm_plan_t p;
     std::memset(&p, 0, sizeof(p));
+    const int tile = choose_tile(M, N, K, batch, sms);
+    const int bk = tile / 8;
+    const int cps = tile == kSmallTile ? kSmallCtasPerSm : kCtasPerSm;
     p.mode = SGEMM_MODE_FFMA;
-    p.kernel = default_kernel();
-    p.bm = kBM;
-    p.bn = kBN;
-    p.bk = kBK;
-    p.threads = kThreads;
+    p.kernel = tile == kSmallTile ? kKernelFfma128 : default_kernel();
+    p.bm = tile;
+    p.bn = tile;
+    p.bk = bk;
+    p.threads = (tile / 8) * (tile / 8);
     p.vec = vec ? 1 : 0;
-    p.tiles_m = ceil_div(M, kBM);
-    p.tiles_n = ceil_div(N, kBN);
+    p.tiles_m = ceil_div(M, tile);
+    p.tiles_n = ceil_div(N, tile);
     const int64_t tiles = p.tiles_m * p.tiles_n * batch;
     int64_t kps = 0;
-    p.split_k = (M > 0 && N > 0 && K > 0 && batch > 0) ? choose_split(tiles, K, sms, &kps) : 1;
-    if (p.split_k == 1) kps = ceil_div(K, kBK) * kBK;
-    p.k_per_split = kps > 0 ? kps : kBK;
+    p.split_k = (M > 0 && N > 0 && K > 0 && batch > 0)
+                    ? choose_split(tiles, K, sms, &kps, bk, cps)
+                    : 1;
+    if (p.split_k == 1) kps = ceil_div(K, bk) * bk;
+    p.k_per_split = kps > 0 ? kps : bk;
     int tail_split = 1;
     p.tail_start = tiles;
     p.tail_k_per_split = p.k_per_split;
-    if (p.split_k == 1 && M > 0 && N > 0 && K > 0)
+    if (tile == 128 && p.split_k == 1 && M > 0 && N > 0 && K > 0)
         choose_tail(tiles, K, sms, &p.tail_start, &tail_split, &p.tail_k_per_split);
     p.tail_split = tail_split;
-    const bool full = (M % kBM == 0) && (N % kBN == 0) && (K % kBK == 0) &&
+    const bool full = (M % tile == 0) && (N % tile == 0) && (K % bk == 0) &&
                       (p.split_k == 1 || K % p.k_per_split == 0) &&
                       (p.tail_split == 1 || K % p.tail_k_per_split == 0);
     p.edge = (p.vec && full) ? 0 : 1;
     p.grid_ctas = p.tail_start * p.split_k + (tiles - p.tail_start) * p.tail_split;
-    p.workspace_bytes = split_workspace(tiles, p.split_k, p.tail_start, p.tail_split);
+    p.workspace_bytes = split_workspace(tiles, p.split_k, p.tail_start, p.tail_split, tile);
     *out = p;
 }
 
@@ -289,7 +314,7 @@ sgemm_status run(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K, float
         a.counters = static_cast<unsigned *>(workspace);
         a.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + kCounterBytes);
     }
-    e = launch_ffma(a, plan.kernel, plan.vec != 0, plan.edge != 0, false, false, stream);
+    e = launch_ffma(a, plan.kernel, plan.bm, plan.vec != 0, plan.edge != 0, false, false, stream);
     return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
 }
 
@@ -297,16 +322,20 @@ bool plan_matches(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int64_t
                   int64_t ldb, int64_t ldc, const void *A, const void *B, const void *C) {
     if (p.mode != SGEMM_MODE_FFMA) return false;
     if (p.kernel != kKernelFfma128 && p.kernel != kKernelFfma2x128) return false;
-    if (p.bm != kBM || p.bn != kBN || p.bk != kBK || p.threads != kThreads) return false;
-    if (p.tiles_m != ceil_div(M, kBM) || p.tiles_n != ceil_div(N, kBN)) return false;
+    const int t = p.bm;
+    if ((t != 128 && t != kSmallTile) || p.bn != t || p.bk != t / 8 ||
+        p.threads != (t / 8) * (t / 8))
+        return false;
+    if (t == kSmallTile && p.kernel != kKernelFfma128) return false;
+    if (p.tiles_m != ceil_div(M, t) || p.tiles_n != ceil_div(N, t)) return false;
     const int64_t tiles = p.tiles_m * p.tiles_n;
     if (p.split_k < 1 || p.split_k > kMaxSplit) return false;
     if (p.tail_split < 1 || p.tail_split > kMaxSplit) return false;
     if (p.tail_start < 0 || p.tail_start > tiles) return false;
     if (p.split_k > 1 && (p.tail_start != tiles || tiles > kMaxSplitTiles)) return false;
-    if (p.tail_split > 1 && tiles - p.tail_start > kMaxSplitTiles) return false;
-    if (p.k_per_split <= 0 || p.k_per_split % kBK != 0) return false;
-    if (p.tail_k_per_split <= 0 || p.tail_k_per_split % kBK != 0) return false;
+    if (p.tail_split > 1 && (t != 128 || tiles - p.tail_start > kMaxSplitTiles)) return false;
+    if (p.k_per_split <= 0 || p.k_per_split % p.bk != 0) return false;
+    if (p.tail_k_per_split <= 0 || p.tail_k_per_split % p.bk != 0) return false;
     if (K > 0 && ceil_div(K, p.k_per_split) != p.split_k) return false;
     if (K > 0 && p.tail_start < tiles && ceil_div(K, p.tail_k_per_split) != p.tail_split)
         return false;
@@ -317,11 +346,11 @@ bool plan_matches(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int64_t
     if (p.vec && !vec_ok) return false;
     if (!p.edge) {
         if (!p.vec) return false;
-        if (M % kBM || N % kBN || K % kBK || (p.split_k > 1 && K % p.k_per_split) ||
+        if (M % t || N % t || K % p.bk || (p.split_k > 1 && K % p.k_per_split) ||
             (p.tail_split > 1 && K % p.tail_k_per_split))
             return false;
     }
-    const size_t need = split_workspace(tiles, p.split_k, p.tail_start, p.tail_split);
+    const size_t need = split_workspace(tiles, p.split_k, p.tail_start, p.tail_split, t);
     return p.workspace_bytes == need;
 }
 
@@ -581,7 +610,7 @@ extern "C" sgemm_status sgemm_ex(int32_t op_a, int32_t op_b, int64_t M, int64_t 
     // the outputs of different batches may not overlap
     if (batch > 1 && stride_c < (M > 0 ? (M - 1) * ldc + N : 0)) return SGEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0 || batch == 0) return SGEMM_OK;
-    if (ceil_div(M, kBM) * ceil_div(N, kBN) > int64_t(INT32_MAX) / batch)
+    if (ceil_div(M, kSmallTile) * ceil_div(N, kSmallTile) > int64_t(INT32_MAX) / batch)
         return SGEMM_ERR_INVALID_ARG;
     if (!C) return SGEMM_ERR_INVALID_ARG;
     if (K > 0 && alpha != 0.0f && (!A || !B)) return SGEMM_ERR_INVALID_ARG;
@@ -638,7 +667,7 @@ extern "C" sgemm_status sgemm_ex(int32_t op_a, int32_t op_b, int64_t M, int64_t 
         a.counters = static_cast<unsigned *>(ws);
         a.partials = reinterpret_cast<float *>(static_cast<char *>(ws) + kCounterBytes);
     }
-    e = launch_ffma(a, plan.kernel, plan.vec != 0, plan.edge != 0, ta, tb, st);
+    e = launch_ffma(a, plan.kernel, plan.bm, plan.vec != 0, plan.edge != 0, ta, tb, st);
     return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
 }
 

@@ -9,13 +9,17 @@
 
 namespace sgemm_impl {
 
-// CTA tile of the fp32 FFMA kernel: 128 x 128 outputs, K slices of 16,
-// 256 threads, each thread owns an 8 x 8 block of accumulators.
+// CTA tiles of the fp32 FFMA kernel: T x T outputs, K slices of T/8,
+// (T/8)^2 threads, each owning an 8 x 8 block of accumulators.  T = 128 is
+// the main tile (2 resident CTAs per SM); T = 64 is for grids that 128-wide
+// tiles cannot fill (8 per SM).
 constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kBK = 16;
 constexpr int kThreads = 256;
-constexpr int kCtasPerSm = 2;   // resident CTAs per SM the kernel is built for
+constexpr int kCtasPerSm = 2;   // resident 128-tile CTAs per SM
+constexpr int kSmallTile = 64;
+constexpr int kSmallCtasPerSm = 8;
 constexpr int kGroupM = 8;      // tile rows per raster group (L2 locality)
 
 // Split-K workspace layout: [tile counters: kCounterBytes][partials].  The
@@ -71,12 +75,13 @@ enum KernelId : int32_t {
 };
 
 // op(A) = A^T when trans_a (A stored K x M), op(B) = B^T when trans_b.
-cudaError_t launch_ffma(const GemmArgs &a, int kernel, bool vec, bool edge, bool trans_a,
-                        bool trans_b, cudaStream_t stream);
+// `tile` is 128 or 64 (the plan's bm).
+cudaError_t launch_ffma(const GemmArgs &a, int kernel, int tile, bool vec, bool edge,
+                        bool trans_a, bool trans_b, cudaStream_t stream);
 // the transposed layouts, one translation unit each
-cudaError_t launch_ffma_nt(const GemmArgs &a, bool vec, bool edge, cudaStream_t stream);
-cudaError_t launch_ffma_tn(const GemmArgs &a, bool vec, bool edge, cudaStream_t stream);
-cudaError_t launch_ffma_tt(const GemmArgs &a, bool vec, bool edge, cudaStream_t stream);
+cudaError_t launch_ffma_nt(const GemmArgs &a, int tile, bool vec, bool edge, cudaStream_t stream);
+cudaError_t launch_ffma_tn(const GemmArgs &a, int tile, bool vec, bool edge, cudaStream_t stream);
+cudaError_t launch_ffma_tt(const GemmArgs &a, int tile, bool vec, bool edge, cudaStream_t stream);
 cudaError_t launch_scale(float *C, int64_t M, int64_t N, int64_t ldc, float beta,
                          cudaStream_t stream);
 cudaError_t launch_epilogue_only(float *C, int64_t M, int64_t N, int64_t ldc, int64_t strideC,

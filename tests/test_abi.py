@@ -140,7 +140,25 @@ def test_plan_tail_split_is_opt_in(lib, monkeypatch):
 def test_plan_ragged_shape_takes_the_checked_scalar_path(lib):
     p = plan(1023, 777, 513, lda=513, ldb=777, ldc=777)
     assert p.vec == 0 and p.edge == 1
-    assert p.tiles_m == 8 and p.tiles_n == 7
+    # 8 x 7 = 56 tiles of 128 would fill under half of 152 SMs: 64-wide tiles
+    assert (p.bm, p.bn, p.bk, p.threads) == (64, 64, 8, 64)
+    assert p.tiles_m == 16 and p.tiles_n == 13
+
+
+def test_plan_tile_choice(lib, monkeypatch):
+    assert plan(8192, 8192, 8192).bm == 128
+    assert plan(1024, 2304, 768).bm == 128        # 144 tiles of 128
+    assert plan(1024, 768, 3072).bm == 128        # 48 tiles of 128, but K is long
+    assert plan(1024, 1024, 16384).bm == 128
+    assert plan(1023, 777, 513).bm == 64          # 56 tiles, short K
+    assert plan(1024, 64, 1024).bm == 64          # a 128-wide tile would be half padding
+    assert plan(256, 256, 256).bm == 64
+    assert plan(256, 256, 256, sms=4).bm == 128   # a small GPU is filled by 4 tiles
+    monkeypatch.setenv("SGEMM_FORCE_TILE", "128")
+    assert plan(256, 256, 256).bm == 128
+    monkeypatch.setenv("SGEMM_FORCE_TILE", "64")
+    q = plan(8192, 8192, 8192)
+    assert q.bm == 64 and q.tiles_m == 128 and q.threads == 64 and q.edge == 0
 
 
 def test_plan_misaligned_pointer_disables_vector_loads(lib):
@@ -149,7 +167,8 @@ def test_plan_misaligned_pointer_disables_vector_loads(lib):
     assert plan(256, 256, 256, C=4104).vec == 0
 
 
-def test_plan_split_k_fills_the_gpu_when_tiles_are_few(lib):
+def test_plan_split_k_fills_the_gpu_when_tiles_are_few(lib, monkeypatch):
+    monkeypatch.setenv("SGEMM_FORCE_TILE", "128")
     p = plan(1024, 1024, 16384)          # 64 tiles, long K
     assert p.split_k > 1
     assert p.k_per_split % p.bk == 0
@@ -159,6 +178,11 @@ def test_plan_split_k_fills_the_gpu_when_tiles_are_few(lib):
     assert p.workspace_bytes == sg.WORKSPACE_COUNTER_BYTES + 64 * p.split_k * 128 * 128 * 4
     # MLP-down: 48 tiles, K = 3072
     assert plan(1024, 768, 3072).split_k > 1
+    monkeypatch.setenv("SGEMM_FORCE_TILE", "64")
+    q = plan(1024, 1024, 16384)          # 64-wide tiles: 256 of them, still split along K
+    tiles = q.tiles_m * q.tiles_n
+    assert q.bm == 64 and tiles == 256 and q.split_k > 1
+    assert q.workspace_bytes == sg.WORKSPACE_COUNTER_BYTES + tiles * q.split_k * 64 * 64 * 4
     # a full wave of tiles is never split
     assert plan(8192, 8192, 8192).split_k == 1
     assert plan(4096, 4096, 4096).split_k == 1
@@ -174,7 +198,8 @@ def test_plan_depends_on_sm_count(lib):
     assert big.split_k >= 1
 
 
-def test_sgemm_with_plan_rejects_mismatched_plan_and_small_workspace(lib):
+def test_sgemm_with_plan_rejects_mismatched_plan_and_small_workspace(lib, monkeypatch):
+    monkeypatch.setenv("SGEMM_FORCE_TILE", "128")
     p = plan(1024, 1024, 16384)
     assert p.split_k > 1
     # workspace too small -> SGEMM_ERR_WORKSPACE (checked before the device)
@@ -193,6 +218,7 @@ def test_sgemm_with_plan_rejects_mismatched_plan_and_small_workspace(lib):
 
 
 def test_forced_split_override(lib, monkeypatch):
+    monkeypatch.setenv("SGEMM_FORCE_TILE", "128")
     monkeypatch.setenv("SGEMM_FORCE_SPLIT", "4")
     p = plan(512, 512, 1024)
     assert p.split_k == 4 and p.k_per_split == 256
@@ -201,6 +227,7 @@ def test_forced_split_override(lib, monkeypatch):
 
 
 def test_forced_kernel_override(lib, monkeypatch):
+    monkeypatch.setenv("SGEMM_FORCE_TILE", "128")
     monkeypatch.setenv("SGEMM_FORCE_KERNEL", "0")
     assert plan(256, 256, 256).kernel == 0
     monkeypatch.setenv("SGEMM_FORCE_KERNEL", "1")

@@ -202,10 +202,11 @@ def test_empty_shapes_are_no_ops(sg):
     assert bool((c == 3.0).all())
 
 
-@pytest.mark.parametrize("kernel", ["0", "1"])
+@pytest.mark.parametrize("kernel,tile", [("0", "128"), ("1", "128"), ("0", "64")])
 @pytest.mark.parametrize("split", ["1", "2", "3", "7"])
-def test_forced_kernel_and_split(sg, monkeypatch, kernel, split):
+def test_forced_kernel_and_split(sg, monkeypatch, kernel, tile, split):
     monkeypatch.setenv("SGEMM_FORCE_KERNEL", kernel)
+    monkeypatch.setenv("SGEMM_FORCE_TILE", tile)
     monkeypatch.setenv("SGEMM_FORCE_SPLIT", split)
     p = workloads.make(300, 260, 1000, seed=31, beta=0.5, c0_dist="uniform")
     run_and_check(sg, p)
@@ -234,7 +235,16 @@ def test_tail_split_parity(sg, monkeypatch, M, N, K, dist, lds):
     run_and_check(sg, p, exact=dist == "int4")
 
 
+@pytest.mark.parametrize("tile", ["64", "128"])
+@pytest.mark.parametrize("name", ["square1024ab", "ragged", "gpt2_qkv", "square256_int"])
+def test_forced_tile(sg, monkeypatch, tile, name):
+    monkeypatch.setenv("SGEMM_FORCE_TILE", tile)
+    p = workloads.workload(name)
+    run_and_check(sg, p, exact=p.meta["dist"] == "int4")
+
+
 def test_both_kernels_bit_identical(sg, monkeypatch):
+    monkeypatch.setenv("SGEMM_FORCE_TILE", "128")
     outs = []
     for kernel in ("0", "1"):
         monkeypatch.setenv("SGEMM_FORCE_KERNEL", kernel)
