@@ -92,6 +92,9 @@ class GemmPlan(ctypes.Structure):
         ("workspace_bytes", ctypes.c_size_t),
         ("tail_start", ctypes.c_int64),
         ("tail_k_per_split", ctypes.c_int64),
+        ("transpose_a", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("a_t_ld", ctypes.c_int64),
     ]
 
     def as_dict(self) -> dict:

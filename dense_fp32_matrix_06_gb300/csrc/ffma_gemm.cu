@@ -24,6 +24,26 @@ __global__ void scale_kernel(float *C, int64_t M, int64_t N, int64_t ldc, float 
     }
 }
 
+// At[k * ldt + m] = A[m * lda + k] for the first K columns of the first M
+// rows: 32 x 32 tiles through padded shared memory, so both the reads (along
+// k) and the writes (along m) are coalesced.  Feeds the product that reads A
+// one k-row at a time (see the planner's transpose_a).
+__global__ void transpose_kernel(const float *__restrict__ A, int64_t M, int64_t K, int64_t lda,
+                                 float *__restrict__ At, int64_t ldt) {
+    __shared__ float tile[32][33];
+    const int64_t m0 = int64_t(blockIdx.y) * 32, k0 = int64_t(blockIdx.x) * 32;
+    const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8
+    for (int i = ty; i < 32; i += 8) {
+        const int64_t m = m0 + i, k = k0 + tx;
+        tile[i][tx] = (m < M && k < K) ? A[m * lda + k] : 0.0f;
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+        const int64_t k = k0 + i, m = m0 + tx;
+        if (k < K && m < M) At[k * ldt + m] = tile[tx][i];
+    }
+}
+
 // C_b = act(beta * C_b + bias) for the K == 0 / alpha == 0 case of the
 // batched, fused-epilogue call (beta == 0 does not read C).
 __global__ void epilogue_only_kernel(float *C, int64_t M, int64_t N, int64_t ldc,
@@ -97,6 +117,13 @@ cudaError_t launch_ffma(const GemmArgs &a, int kernel, int tile, bool vec, bool 
     return kernel == kKernelFfma2x128
                ? ffma::launch_layout<128, true, false, false, false>(a, vec, edge, stream)
                : ffma::launch_layout<128, false, false, false, false>(a, vec, edge, stream);
+}
+
+cudaError_t launch_transpose(const float *A, int64_t M, int64_t K, int64_t lda, float *At,
+                             int64_t ldt, cudaStream_t stream) {
+    const dim3 grid(unsigned((K + 31) / 32), unsigned((M + 31) / 32));
+    transpose_kernel<<<grid, dim3(32, 8), 0, stream>>>(A, M, K, lda, At, ldt);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_scale(float *C, int64_t M, int64_t N, int64_t ldc, float beta,

@@ -82,6 +82,9 @@ cudaError_t launch_ffma(const GemmArgs &a, int kernel, int tile, bool vec, bool 
 cudaError_t launch_ffma_nt(const GemmArgs &a, int tile, bool vec, bool edge, cudaStream_t stream);
 cudaError_t launch_ffma_tn(const GemmArgs &a, int tile, bool vec, bool edge, cudaStream_t stream);
 cudaError_t launch_ffma_tt(const GemmArgs &a, int tile, bool vec, bool edge, cudaStream_t stream);
+// At = A^T (K x M, row stride ldt); M <= 65535 * 32.
+cudaError_t launch_transpose(const float *A, int64_t M, int64_t K, int64_t lda, float *At,
+                             int64_t ldt, cudaStream_t stream);
 cudaError_t launch_scale(float *C, int64_t M, int64_t N, int64_t ldc, float beta,
                          cudaStream_t stream);
 cudaError_t launch_epilogue_only(float *C, int64_t M, int64_t N, int64_t ldc, int64_t strideC,

@@ -103,6 +103,11 @@ typedef struct {
                               when there is none.  Only the last, partly filled wave
                               of tiles is split, so it ends sooner */
     int64_t tail_k_per_split; /* K extent of one tail partition */
+    int32_t transpose_a;   /* 1: A is first transposed into the workspace (K x M, row
+                              stride a_t_ld) and the product runs with A read as a
+                              row-per-k operand, which is faster for large grids */
+    int32_t reserved;
+    int64_t a_t_ld;        /* row stride of the transposed copy (floats) */
 } gemm_plan_t;
 
 /*

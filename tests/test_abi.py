@@ -115,7 +115,25 @@ def test_plan_full_tiles_take_the_unchecked_vector_path(lib):
     assert p.tiles_m == 64 and p.tiles_n == 64
     assert p.vec == 1 and p.edge == 0
     assert p.split_k == 1 and p.tail_split == 1 and p.tail_start == 4096
-    assert p.grid_ctas == 4096 and p.workspace_bytes == 0
+    assert p.grid_ctas == 4096
+    # A is transposed into the workspace first (K x M after the counter block)
+    assert p.transpose_a == 1 and p.a_t_ld == 8192
+    assert p.workspace_bytes == sg.WORKSPACE_COUNTER_BYTES + 8192 * 8192 * 4
+
+
+def test_plan_transpose_choice(lib, monkeypatch):
+    assert plan(2048, 2048, 2048).transpose_a == 1
+    assert plan(8192, 8192, 64).transpose_a == 0         # K too short to pay for the pass
+    assert plan(1024, 1024, 1024).transpose_a == 0        # split-K plan
+    assert plan(4096, 512, 4096).transpose_a == 0         # N < 1024
+    assert plan(2048, 2048, 2048, A=4100).transpose_a == 0   # not vector-aligned
+    monkeypatch.setenv("SGEMM_FORCE_TRANSPOSE_A", "0")
+    q = plan(8192, 8192, 8192)
+    assert q.transpose_a == 0 and q.workspace_bytes == 0
+    monkeypatch.setenv("SGEMM_FORCE_TRANSPOSE_A", "1")
+    r = plan(1023 * 2, 4096, 515, lda=516)
+    assert r.transpose_a == 1 and r.a_t_ld == 2048 and r.edge == 1
+    assert r.workspace_bytes == sg.WORKSPACE_COUNTER_BYTES + (515 * 2048 * 4 + 255) // 256 * 256
 
 
 def test_plan_tail_split_is_opt_in(lib, monkeypatch):
@@ -134,7 +152,7 @@ def test_plan_tail_split_is_opt_in(lib, monkeypatch):
     assert r.tail_split == 1 or r.tail_k_per_split >= 16
     monkeypatch.setenv("SGEMM_FORCE_TAIL", "0")
     t = plan(8192, 8192, 8192)
-    assert t.tail_split == 1 and t.workspace_bytes == 0 and t.grid_ctas == 4096
+    assert t.tail_split == 1 and t.grid_ctas == 4096
 
 
 def test_plan_ragged_shape_takes_the_checked_scalar_path(lib):

@@ -243,6 +243,46 @@ def test_forced_tile(sg, monkeypatch, tile, name):
     run_and_check(sg, p, exact=p.meta["dist"] == "int4")
 
 
+@pytest.mark.parametrize("force", ["0", "1"])
+@pytest.mark.parametrize("M,N,K,lds,dist", [
+    (2048, 1024, 512, None, "uniform"),
+    (2046, 1030, 515, (516, 1032, 1036), "uniform"),     # ragged: bounds-checked tiles
+    (1024, 1536, 768, None, "int4"),
+])
+def test_transposed_a_path(sg, monkeypatch, force, M, N, K, lds, dist):
+    monkeypatch.setenv("SGEMM_FORCE_TRANSPOSE_A", force)
+    monkeypatch.setenv("SGEMM_FORCE_SPLIT", "1")
+    monkeypatch.setenv("SGEMM_FORCE_TILE", "128")
+    lda, ldb, ldc = lds if lds else (None, None, None)
+    p = workloads.make(M, N, K, dist=dist, seed=61, lda=lda, ldb=ldb, ldc=ldc,
+                       alpha=1.5 if dist == "int4" else 0.75, beta=0.5,
+                       c0_dist="int4" if dist == "int4" else "uniform")
+    plan = sg.gemm_plan_for_sms(p.M, p.N, p.K, p.lda, p.ldb, p.ldc)
+    assert plan.transpose_a == int(force)
+    run_and_check(sg, p, exact=dist == "int4")
+
+
+def test_transposed_a_with_caller_workspace(sg, monkeypatch):
+    import torch
+    p = workloads.workload("square2048")
+    A = torch.from_numpy(p.A).cuda()
+    B = torch.from_numpy(p.B).cuda()
+    C = torch.empty((p.M, p.N), device="cuda")
+    plan = sg.plan_for(A, B, C)
+    assert plan.transpose_a == 1
+    ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    sg.sgemm_with_plan(plan, A, B, C, 1.0, 0.0, ws)
+    torch.cuda.synchronize()
+    ii, jj = workloads.sample_indices(p.M, p.N, 2000, seed=5)
+    ref = oracle.sgemm_entries(p.M, p.N, p.K, 1.0, p.A, p.B, 0.0, None, ii, jj)
+    got = C.cpu().numpy()[ii, jj]
+    den = p.K * float(np.abs(p.A).max()) * float(np.abs(p.B).max())
+    assert float(np.abs(got.astype(np.float64) - ref).max()) / den <= TOL_FFMA
+    with pytest.raises(sg.SgemmError) as e:
+        sg.sgemm_with_plan(plan, A, B, C, 1.0, 0.0, ws[:1 << 20])
+    assert e.value.status == 7
+
+
 def test_both_kernels_bit_identical(sg, monkeypatch):
     monkeypatch.setenv("SGEMM_FORCE_TILE", "128")
     outs = []
