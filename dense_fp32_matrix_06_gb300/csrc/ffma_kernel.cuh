@@ -116,15 +116,22 @@ __device__ __forceinline__ int tcol(int k, int x) {
 // (M) x 8 (N) threads.  With K slices of T/8 every thread stages exactly two
 // float4 of each operand per slice, whatever T is.  T = 128 is the main
 // tile; T = 64 serves grids too small to fill the GPU with 128-wide tiles.
-template <int T>
+// BK may be raised above T/8 (to 32 at T = 128) when both operands arrive
+// by row copies: fewer barriers and less loop overhead per FMA.  Operands
+// staged through registers need BK = T/8.
+template <int T, int BK = T / 8>
 struct TileCfg {
     static constexpr int kT = T;
-    static constexpr int kBK = T / 8;
+    static constexpr int kBK = BK;
     static constexpr int kThreads = (T / 8) * (T / 8);
     static constexpr int kWarpsN = T / 64;              // warps along N
     static constexpr int kKG = kBK / 4;                 // 4-wide k groups per slice
     static constexpr int kShift = kKG == 4 ? 3 : 4;     // log2(32 / kKG)
     static constexpr int kCopyRows = T / 16;            // tile rows per copy pass
+    static constexpr int kCopyPasses = BK / kCopyRows;
+    // two pages of T x BK for each operand; above 48 KiB they are dynamic
+    static constexpr int kSmemBytes = 2 * 2 * BK * T * 4;
+    static constexpr bool kDynSmem = kSmemBytes > 48 * 1024 - 64;
     static constexpr int kMinBlocks = T == 128 ? 2 : 8; // resident CTAs per SM
     static_assert(T == 128 || T == 64, "tile is 128 or 64");
 };
@@ -180,18 +187,29 @@ __device__ __forceinline__ WorkItem work_item(const GemmArgs &p, int64_t pid, in
 // kExt: batches, bias and activation are compiled in (sgemm_ex); the plain
 // product (sgemm) is built without them, which leaves it more registers.
 template <int kTile, bool kPacked, bool kVec, bool kEdge, bool kSplit, bool kTransA,
-          bool kTransB, bool kExt>
-__global__ void __launch_bounds__(TileCfg<kTile>::kThreads, TileCfg<kTile>::kMinBlocks)
+          bool kTransB, bool kExt, int kBKT = kTile / 8>
+__global__ void __launch_bounds__(TileCfg<kTile, kBKT>::kThreads,
+                                  TileCfg<kTile, kBKT>::kMinBlocks)
 ffma_gemm_kernel(const GemmArgs p) {
-    using TC = TileCfg<kTile>;
+    using TC = TileCfg<kTile, kBKT>;
     constexpr int T = TC::kT, BK = TC::kBK, NT = TC::kThreads, KG = TC::kKG, SH = TC::kShift;
+    static_assert(BK == T / 8 || (kTransA && !kTransB),
+                  "register-staged operands need K slices of T/8");
     // A tile: As[k][m]; swizzled when filled by transposing stores (A not transposed)
     // B tile: Bs[k][n]; swizzled when filled by transposing stores (B transposed)
     constexpr bool kSwzA = !kTransA;
     constexpr bool kSwzB = kTransB;
-    __shared__ __align__(16) float As[2][BK][T];
-    __shared__ __align__(16) float Bs[2][BK][T];
+    // Static tile pages (a one-row stand-in when the tiles are too large for
+    // static shared memory and live in the dynamic block instead).
+    constexpr int kStaticBK = TC::kDynSmem ? 1 : BK;
+    __shared__ __align__(16) float sa[2][kStaticBK][T];
+    __shared__ __align__(16) float sb[2][kStaticBK][T];
     __shared__ int s_last;
+    extern __shared__ __align__(16) float dyn_smem[];
+    float (&As)[2][BK][T] = *reinterpret_cast<float(*)[2][BK][T]>(
+        TC::kDynSmem ? dyn_smem : &sa[0][0][0]);
+    float (&Bs)[2][BK][T] = *reinterpret_cast<float(*)[2][BK][T]>(
+        TC::kDynSmem ? dyn_smem + 2 * BK * T : &sb[0][0][0]);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -298,7 +316,7 @@ ffma_gemm_kernel(const GemmArgs p) {
                       int64_t lim, const float *dummy) {
         const int64_t koff = int64_t(t) * BK;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < TC::kCopyPasses; ++h) {
             const float *src = base + (koff + TC::kCopyRows * h) * ld;
             float *dst = &S[c_row + TC::kCopyRows * h][c_col];
             if constexpr (!kEdge) {
@@ -520,13 +538,22 @@ ffma_gemm_kernel(const GemmArgs p) {
 }
 
 template <int kTile, bool kPacked, bool kVec, bool kEdge, bool kSplit, bool kTransA,
-          bool kTransB, bool kExt>
+          bool kTransB, bool kExt, int kBKT = kTile / 8>
 cudaError_t launch_variant(const GemmArgs &a, cudaStream_t stream) {
+    using TC = TileCfg<kTile, kBKT>;
+    auto kernel = ffma_gemm_kernel<kTile, kPacked, kVec, kEdge, kSplit, kTransA, kTransB, kExt,
+                                   kBKT>;
+    int dyn = 0;
+    if constexpr (TC::kDynSmem) {
+        dyn = TC::kSmemBytes;
+        const cudaError_t e =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+        if (e != cudaSuccess) return e;
+    }
     const int64_t tiles = int64_t(a.tiles_m) * a.tiles_n * a.batch;
     const dim3 grid(unsigned(a.tail_start * a.split_k + (tiles - a.tail_start) * a.tail_split),
                     1, 1);
-    ffma_gemm_kernel<kTile, kPacked, kVec, kEdge, kSplit, kTransA, kTransB, kExt>
-        <<<grid, TileCfg<kTile>::kThreads, 0, stream>>>(a);
+    kernel<<<grid, TC::kThreads, dyn, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -232,14 +232,17 @@ void plan_core(int64_t M, int64_t N, int64_t K, int64_t batch, bool vec, int sms
 // on GB300 (TFLOP/s, A as given / A^T given): 8192^3 60.75 / 63.53,
 // 4096^3 58.5 / 60.9, 2048^3 49.2 / 52.1.  A transpose pass costs
 // 8*M*K bytes of HBM traffic, about 35/N of the product's time at the fp32
-// rate, so it pays for full-grid 128-wide plans with N >= 1024 and K >= 256
-// (with the pass included: 8192^3 60.7 -> 62.9, 4096^3 58.4 -> 59.5,
-// 2048^3 48.7 -> 49.1; at K = 64 it loses, 47.5 -> 45.4).  The copy lives in
-// the workspace (K x M floats after the counter block).
+// rate, so it pays for 128-wide plans of at least two waves of tiles with
+// N >= 1024 and K >= 256.  With the pass, and the product in K slices of 32
+// (both operands are then row copies): 8192^3 60.7 -> 64.5 TFLOP/s, 4096^3
+// 58.4 -> 61.4; it loses at K = 64 (47.5 -> 45.4) and for 2048^3 (256 tiles,
+// under one wave).  The copy lives in the workspace (K x M floats after the
+// counter block).
 // SGEMM_FORCE_TRANSPOSE_A=0/1 overrides the choice for sweeps.
-bool choose_transpose_a(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K) {
+bool choose_transpose_a(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int sms) {
     bool want = p.bm == 128 && p.split_k == 1 && p.tail_split == 1 && p.vec && N >= 1024 &&
-                K >= 256 && M <= int64_t(65535) * 32;
+                K >= 256 && M <= int64_t(65535) * 32 &&
+                p.tiles_m * p.tiles_n >= int64_t(2) * kCtasPerSm * sms;
     if (const char *force = std::getenv("SGEMM_FORCE_TRANSPOSE_A")) {
         const int f = std::atoi(force);
         if (f == 0) want = false;
@@ -261,9 +264,14 @@ sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb
     const bool vec = lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0 && aligned16(A) &&
                      aligned16(B) && aligned16(C);
     plan_core(M, N, K, 1, vec, sms, out);
-    if (allow_transpose && M > 0 && N > 0 && K > 0 && choose_transpose_a(*out, M, N, K)) {
+    if (allow_transpose && M > 0 && N > 0 && K > 0 && choose_transpose_a(*out, M, N, K, sms)) {
+        // the product then runs with both operands copied by rows, in K slices of 32
         out->transpose_a = 1;
         out->workspace_bytes = transpose_workspace(M, K, &out->a_t_ld);
+        out->bk = kWideBK;
+        out->k_per_split = ceil_div(K, kWideBK) * kWideBK;
+        out->tail_k_per_split = out->k_per_split;
+        out->edge = (out->vec && M % 128 == 0 && N % 128 == 0 && K % kWideBK == 0) ? 0 : 1;
     }
     return SGEMM_OK;
 }
@@ -354,8 +362,7 @@ sgemm_status run(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K, float
         if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
         a.A = at;
         a.lda = plan.a_t_ld;
-        e = launch_ffma(a, plan.kernel, plan.bm, plan.vec != 0, plan.edge != 0, true, false,
-                        stream);
+        e = launch_ffma_tn_wide(a, plan.vec != 0, plan.edge != 0, stream);
         return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
     }
     e = launch_ffma(a, plan.kernel, plan.bm, plan.vec != 0, plan.edge != 0, false, false, stream);
@@ -367,9 +374,9 @@ bool plan_matches(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int64_t
     if (p.mode != SGEMM_MODE_FFMA) return false;
     if (p.kernel != kKernelFfma128 && p.kernel != kKernelFfma2x128) return false;
     const int t = p.bm;
-    if ((t != 128 && t != kSmallTile) || p.bn != t || p.bk != t / 8 ||
-        p.threads != (t / 8) * (t / 8))
+    if ((t != 128 && t != kSmallTile) || p.bn != t || p.threads != (t / 8) * (t / 8))
         return false;
+    if (p.bk != (p.transpose_a ? kWideBK : t / 8)) return false;
     if (t == kSmallTile && p.kernel != kKernelFfma128) return false;
     if (p.tiles_m != ceil_div(M, t) || p.tiles_n != ceil_div(N, t)) return false;
     const int64_t tiles = p.tiles_m * p.tiles_n;

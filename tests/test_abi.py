@@ -111,7 +111,8 @@ def plan(M, N, K, lda=None, ldb=None, ldc=None, A=0, B=0, C=0, sms=152):
 
 def test_plan_full_tiles_take_the_unchecked_vector_path(lib):
     p = plan(8192, 8192, 8192)
-    assert (p.bm, p.bn, p.bk, p.threads) == (128, 128, 16, 256)
+    # K slices of 32: after the transpose both operands are row copies
+    assert (p.bm, p.bn, p.bk, p.threads) == (128, 128, 32, 256)
     assert p.tiles_m == 64 and p.tiles_n == 64
     assert p.vec == 1 and p.edge == 0
     assert p.split_k == 1 and p.tail_split == 1 and p.tail_start == 4096
@@ -122,17 +123,18 @@ def test_plan_full_tiles_take_the_unchecked_vector_path(lib):
 
 
 def test_plan_transpose_choice(lib, monkeypatch):
-    assert plan(2048, 2048, 2048).transpose_a == 1
+    assert plan(4096, 4096, 4096).transpose_a == 1
+    assert plan(2048, 2048, 2048).transpose_a == 0        # under two waves of tiles
     assert plan(8192, 8192, 64).transpose_a == 0         # K too short to pay for the pass
     assert plan(1024, 1024, 1024).transpose_a == 0        # split-K plan
     assert plan(4096, 512, 4096).transpose_a == 0         # N < 1024
-    assert plan(2048, 2048, 2048, A=4100).transpose_a == 0   # not vector-aligned
+    assert plan(4096, 4096, 4096, A=4100).transpose_a == 0   # not vector-aligned
     monkeypatch.setenv("SGEMM_FORCE_TRANSPOSE_A", "0")
     q = plan(8192, 8192, 8192)
-    assert q.transpose_a == 0 and q.workspace_bytes == 0
+    assert q.transpose_a == 0 and q.workspace_bytes == 0 and q.bk == 16
     monkeypatch.setenv("SGEMM_FORCE_TRANSPOSE_A", "1")
     r = plan(1023 * 2, 4096, 515, lda=516)
-    assert r.transpose_a == 1 and r.a_t_ld == 2048 and r.edge == 1
+    assert r.transpose_a == 1 and r.a_t_ld == 2048 and r.edge == 1 and r.bk == 32
     assert r.workspace_bytes == sg.WORKSPACE_COUNTER_BYTES + (515 * 2048 * 4 + 255) // 256 * 256
 
 

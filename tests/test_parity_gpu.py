@@ -264,7 +264,7 @@ def test_transposed_a_path(sg, monkeypatch, force, M, N, K, lds, dist):
 
 def test_transposed_a_with_caller_workspace(sg, monkeypatch):
     import torch
-    p = workloads.workload("square2048")
+    p = workloads.workload("square4096")
     A = torch.from_numpy(p.A).cuda()
     B = torch.from_numpy(p.B).cuda()
     C = torch.empty((p.M, p.N), device="cuda")
