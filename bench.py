@@ -47,7 +47,8 @@ UNIT = "TFLOP/s"
 FMA_PER_SM_PER_CLK = 128      # fp32 FMA lanes per SM (4 sub-partitions x 32)
 L2_BYTES = 129 * 1000 * 1000
 KERNEL_SOURCES = [os.path.join(ROOT, "dense_fp32_matrix_06_gb300", "csrc", f)
-                  for f in ("ffma_kernel.cuh", "ffma_gemm.cu", "sgemm_internal.h")]
+                  for f in ("ffma_kernel.cuh", "ffma_gemm.cu", "ffma_gemm_tn.cu",
+                            "sgemm_internal.h")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -279,7 +280,8 @@ def run_ours(args):
     sh = stream.cuda_stream
     plan = sg.gemm_plan(p.M, p.N, p.K, p.lda, p.ldb, p.ldc, A.data_ptr(), B.data_ptr(),
                         C.data_ptr())
-    launches_per_gemm = 1
+    # one kernel per GEMM, plus the transpose pass when the plan copies A first
+    launches_per_gemm = 1 + int(plan.transpose_a)
 
     def step():
         sg.sgemm_ptr(p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
@@ -326,7 +328,10 @@ def run_ours(args):
     traffic = committed_traffic(plan.kernel, p.name, flops)
     roofline = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 3),
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                "kernel": f"ffma_gemm_kernel (plan kernel {plan.kernel})",
+                "kernel": ("ffma_gemm_kernel<128, op(A)=A^T copy, K slice 32> after "
+                           "transpose_kernel" if plan.transpose_a else
+                           f"ffma_gemm_kernel (plan kernel {plan.kernel})"),
+                "timed": "each sgemm call (all of its launches) with CUDA events",
                 "peak_source": f"{sms} SMs x {FMA_PER_SM_PER_CLK} FMA/clk x 2 x {mhz:.0f} MHz "
                                f"({peak_src})",
                 "algorithmic_flops_per_launch": flops,
