@@ -16,14 +16,21 @@ cudaError_t launch_ffma_tn(const GemmArgs &a, int tile, bool vec, bool edge,
 // copies, so the slice is not tied to the tile).  Measured on GB300 against
 // K slices of 16: 8192^3 65.2 against 63.6 TFLOP/s for the product alone.
 cudaError_t launch_ffma_tn_wide(const GemmArgs &a, bool vec, bool edge, cudaStream_t stream) {
+    const bool split = a.split_k > 1;
     if (!edge)
-        return ffma::launch_variant<128, false, true, false, false, true, false, false, kWideBK>(
-            a, stream);
+        return split ? ffma::launch_variant<128, false, true, false, true, true, false, false,
+                                            kWideBK>(a, stream)
+                     : ffma::launch_variant<128, false, true, false, false, true, false, false,
+                                            kWideBK>(a, stream);
     if (vec)
-        return ffma::launch_variant<128, false, true, true, false, true, false, false, kWideBK>(
-            a, stream);
-    return ffma::launch_variant<128, false, false, true, false, true, false, false, kWideBK>(
-        a, stream);
+        return split ? ffma::launch_variant<128, false, true, true, true, true, false, false,
+                                            kWideBK>(a, stream)
+                     : ffma::launch_variant<128, false, true, true, false, true, false, false,
+                                            kWideBK>(a, stream);
+    return split ? ffma::launch_variant<128, false, false, true, true, true, false, false,
+                                        kWideBK>(a, stream)
+                 : ffma::launch_variant<128, false, false, true, false, true, false, false,
+                                        kWideBK>(a, stream);
 }
 
 }  // namespace sgemm_impl

@@ -237,25 +237,36 @@ void plan_core(int64_t M, int64_t N, int64_t K, int64_t batch, bool vec, int sms
 // (both operands are then row copies): 8192^3 60.7 -> 64.5 TFLOP/s, 4096^3
 // 58.4 -> 61.4; it loses at K = 64 (47.5 -> 45.4) and for 2048^3 (256 tiles,
 // under one wave).  The copy lives in the workspace (K x M floats after the
-// counter block).
+// counter block).  Split-K plans can take it too (partials before the copy),
+// but measured it loses there (GPT-2 QKV 41.8 -> 38.6, 1024^3 31.5 -> 28.5),
+// so only the override selects it for them.
 // SGEMM_FORCE_TRANSPOSE_A=0/1 overrides the choice for sweeps.
 bool choose_transpose_a(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int sms) {
-    bool want = p.bm == 128 && p.split_k == 1 && p.tail_split == 1 && p.vec && N >= 1024 &&
-                K >= 256 && M <= int64_t(65535) * 32 &&
+    const bool able = p.bm == 128 && p.tail_split == 1 && p.vec && K >= 1 &&
+                      M <= int64_t(65535) * 32;
+    bool want = able && p.split_k == 1 && N >= 1024 && K >= 256 &&
                 p.tiles_m * p.tiles_n >= int64_t(2) * kCtasPerSm * sms;
     if (const char *force = std::getenv("SGEMM_FORCE_TRANSPOSE_A")) {
         const int f = std::atoi(force);
         if (f == 0) want = false;
-        if (f == 1)
-            want = p.bm == 128 && p.split_k == 1 && p.tail_split == 1 && p.vec && K >= 1 &&
-                   M <= int64_t(65535) * 32;
+        if (f == 1) want = able;
     }
     return want;
 }
 
-size_t transpose_workspace(int64_t M, int64_t K, int64_t *ld) {
+size_t transpose_bytes(int64_t M, int64_t K, int64_t *ld) {
     *ld = (M + 3) / 4 * 4;
-    return kCounterBytes + (size_t(K) * size_t(*ld) * sizeof(float) + 255) / 256 * 256;
+    return (size_t(K) * size_t(*ld) * sizeof(float) + 255) / 256 * 256;
+}
+
+// Workspace of a transposing plan: [counters][split-K partials][A^T].
+size_t transpose_workspace(const gemm_plan_t &p, int64_t M, int64_t K, int64_t *ld,
+                           size_t *at_offset) {
+    const int64_t tiles = p.tiles_m * p.tiles_n;
+    const size_t parts =
+        p.split_k > 1 ? size_t(tiles) * p.split_k * size_t(p.bm) * p.bm * sizeof(float) : 0;
+    *at_offset = kCounterBytes + parts;
+    return *at_offset + transpose_bytes(M, K, ld);
 }
 
 sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
@@ -266,12 +277,22 @@ sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb
     plan_core(M, N, K, 1, vec, sms, out);
     if (allow_transpose && M > 0 && N > 0 && K > 0 && choose_transpose_a(*out, M, N, K, sms)) {
         // the product then runs with both operands copied by rows, in K slices of 32
-        out->transpose_a = 1;
-        out->workspace_bytes = transpose_workspace(M, K, &out->a_t_ld);
-        out->bk = kWideBK;
-        out->k_per_split = ceil_div(K, kWideBK) * kWideBK;
-        out->tail_k_per_split = out->k_per_split;
-        out->edge = (out->vec && M % 128 == 0 && N % 128 == 0 && K % kWideBK == 0) ? 0 : 1;
+        gemm_plan_t &q = *out;
+        q.transpose_a = 1;
+        q.bk = kWideBK;
+        const int64_t tiles = q.tiles_m * q.tiles_n;
+        int64_t kps = 0;
+        q.split_k = choose_split(tiles, K, sms, &kps, kWideBK, kCtasPerSm);
+        q.k_per_split = q.split_k > 1 ? kps : ceil_div(K, kWideBK) * kWideBK;
+        q.tail_start = tiles;
+        q.tail_k_per_split = q.k_per_split;
+        q.grid_ctas = tiles * q.split_k;
+        q.edge = (q.vec && M % 128 == 0 && N % 128 == 0 && K % kWideBK == 0 &&
+                  (q.split_k == 1 || K % q.k_per_split == 0))
+                     ? 0
+                     : 1;
+        size_t at_offset = 0;
+        q.workspace_bytes = transpose_workspace(q, M, K, &q.a_t_ld, &at_offset);
     }
     return SGEMM_OK;
 }
@@ -357,7 +378,10 @@ sgemm_status run(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K, float
         a.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + kCounterBytes);
     }
     if (plan.transpose_a) {
-        float *at = reinterpret_cast<float *>(static_cast<char *>(workspace) + kCounterBytes);
+        int64_t ld = 0;
+        size_t at_offset = 0;
+        transpose_workspace(plan, M, K, &ld, &at_offset);
+        float *at = reinterpret_cast<float *>(static_cast<char *>(workspace) + at_offset);
         e = launch_transpose(A, M, K, lda, at, plan.a_t_ld, stream);
         if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
         a.A = at;
@@ -402,10 +426,11 @@ bool plan_matches(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int64_t
             return false;
     }
     if (p.transpose_a) {
-        if (t != 128 || p.split_k != 1 || p.tail_split != 1 || !p.vec) return false;
+        if (t != 128 || p.tail_split != 1 || !p.vec) return false;
         if (M > int64_t(65535) * 32) return false;
         int64_t ld = 0;
-        const size_t need = transpose_workspace(M, K, &ld);
+        size_t at_offset = 0;
+        const size_t need = transpose_workspace(p, M, K, &ld, &at_offset);
         return p.a_t_ld == ld && p.workspace_bytes == need;
     }
     const size_t need = split_workspace(tiles, p.split_k, p.tail_start, p.tail_split, t);

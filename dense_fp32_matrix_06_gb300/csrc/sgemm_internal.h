@@ -82,8 +82,8 @@ cudaError_t launch_ffma(const GemmArgs &a, int kernel, int tile, bool vec, bool 
 cudaError_t launch_ffma_nt(const GemmArgs &a, int tile, bool vec, bool edge, cudaStream_t stream);
 cudaError_t launch_ffma_tn(const GemmArgs &a, int tile, bool vec, bool edge, cudaStream_t stream);
 cudaError_t launch_ffma_tt(const GemmArgs &a, int tile, bool vec, bool edge, cudaStream_t stream);
-// op(A) = A^T, op(B) = B, 128-wide tiles, K slices of 32, no split-K, no
-// batch/bias/activation (the plain product on a transposed copy of A).
+// op(A) = A^T, op(B) = B, 128-wide tiles, K slices of 32, no batch/bias/
+// activation (the plain product on a transposed copy of A); split-K allowed.
 constexpr int kWideBK = 32;
 cudaError_t launch_ffma_tn_wide(const GemmArgs &a, bool vec, bool edge, cudaStream_t stream);
 // At = A^T (K x M, row stride ldt); M <= 65535 * 32.

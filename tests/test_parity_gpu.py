@@ -262,6 +262,19 @@ def test_transposed_a_path(sg, monkeypatch, force, M, N, K, lds, dist):
     run_and_check(sg, p, exact=dist == "int4")
 
 
+@pytest.mark.parametrize("split", ["2", "3"])
+def test_transposed_a_with_split_k(sg, monkeypatch, split):
+    monkeypatch.setenv("SGEMM_FORCE_TRANSPOSE_A", "1")
+    monkeypatch.setenv("SGEMM_FORCE_SPLIT", split)
+    monkeypatch.setenv("SGEMM_FORCE_TILE", "128")
+    p = workloads.make(512, 1024, 1000, seed=62, alpha=0.5, beta=-0.75, c0_dist="uniform")
+    plan = sg.gemm_plan_for_sms(p.M, p.N, p.K, p.lda, p.ldb, p.ldc)
+    assert plan.transpose_a == 1 and plan.split_k == int(split) and plan.bk == 32
+    run_and_check(sg, p)
+    q = workloads.make(384, 1152, 960, dist="int4", seed=63, alpha=1.5, beta=0.5, c0_dist="int4")
+    run_and_check(sg, q, exact=True)
+
+
 def test_transposed_a_with_caller_workspace(sg, monkeypatch):
     import torch
     p = workloads.workload("square4096")
