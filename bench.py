@@ -513,20 +513,20 @@ def run_tf32x3(sg, p, A, B, C, stream, args, dist, device):
     n_var = max(3, min(args.steps, 10))
     t_packed = timed(packed_call, n_var)
     old = os.environ.get("SGEMM_TF32X3_FUSE_A")
-    os.environ["SGEMM_TF32X3_FUSE_A"] = "1"
+    os.environ["SGEMM_TF32X3_FUSE_A"] = "0"
     try:
-        t_fused = timed(call, n_var)
+        t_prepass = timed(call, n_var)
     finally:
         if old is None:
             os.environ.pop("SGEMM_TF32X3_FUSE_A", None)
         else:
             os.environ["SGEMM_TF32X3_FUSE_A"] = old
     variants = {"packed_b": {"value": round(flops / t_packed / 1e12, 3),
-                             "note": "B split and transposed once (sgemm_tf32x3_pack_b); per call "
-                                     "A pre-pass + tensor kernel"},
-                "fused_a_opt_in": {"value": round(flops / t_fused / 1e12, 3),
-                                   "note": "A split in shared memory (SGEMM_TF32X3_FUSE_A=1); "
-                                           "slower, off by default"}}
+                             "note": "B split and transposed once (sgemm_tf32x3_pack_b); A split "
+                                     "in the kernel"},
+                "prepass_a": {"value": round(flops / t_prepass / 1e12, 3),
+                              "note": "A split by a pre-pass instead of in the kernel "
+                                      "(SGEMM_TF32X3_FUSE_A=0)"}}
     peak, src = tf32_peak_tflops()
     achieved = 3 * flops / per_call / 1e12
     return {"value": round(throughput(flops, args.steps, world, el), 3), "unit": UNIT,
@@ -535,10 +535,10 @@ def run_tf32x3(sg, p, A, B, C, stream, args, dist, device):
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
                          "peak": round(peak, 1), "unit": "TFLOP/s",
                          "frac": round(achieved / peak, 4), "traffic": None,
-                         "kernel": "tf32x3_mma_kernel<256,2> (+ split pre-pass)",
+                         "kernel": "tf32x3_fused_kernel<256,2> (+ B split/transpose pass)",
                          "peak_source": src,
                          "note": "achieved = 3 tf32 products x 2MNK over the whole call "
-                                 "(split pre-pass included)"},
+                                 "(B's split pass included)"},
             "variants": variants}
 
 

@@ -49,12 +49,15 @@ constexpr int kTcThreads = 128;
 // ---------------------------------------------------------------------------
 
 // Nearest TF32 value (ties to even) of a finite fp32 x; inf/NaN pass through.
+// Written with selects rather than early returns so that the many
+// conversions a thread does stay one basic block the compiler can interleave.
 __device__ __forceinline__ float tf32_round(float x) {
-    uint32_t u = __float_as_uint(x);
-    if ((u & 0x7f800000u) == 0x7f800000u) return x;
+    const uint32_t u = __float_as_uint(x);
     const uint32_t r = (u + 0x00000fffu + ((u >> 13) & 1u)) & 0xffffe000u;
-    if ((r & 0x7f800000u) == 0x7f800000u) return __uint_as_float(u & 0xffffe000u);
-    return __uint_as_float(r);
+    const bool special = (u & 0x7f800000u) == 0x7f800000u;   // inf or NaN: unchanged
+    const bool overflow = (r & 0x7f800000u) == 0x7f800000u;  // finite rounded to inf: truncate
+    const uint32_t t = overflow ? (u & 0xffffe000u) : r;
+    return __uint_as_float(special ? u : t);
 }
 
 __device__ __forceinline__ void split2(float x, float &hi, float &lo) {
@@ -134,6 +137,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "r"(bar), "r"(parity)
         : "memory");
     return ok != 0;
+}
+
+__device__ __forceinline__ float4 lds128(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, float4 v) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w)
+                 : "memory");
 }
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -508,11 +526,14 @@ template <int BN, int STAGES>
 struct FusedSmem {
     static constexpr int kABytes = kTcBM * kTcBK * 4;          // 16 KiB
     static constexpr int kBBytes = BN * kTcBK * 4;
-    static constexpr int kStageBytes = 2 * kABytes + 2 * kBBytes;
-    static constexpr int kTxBytes = kABytes + 2 * kBBytes;      // raw A + B_hi + B_lo
-    static constexpr int kBarOffset = STAGES * kStageBytes;
-    // full[STAGES], conv[STAGES], empty[STAGES], done, then the TMEM address slot
-    static constexpr int kBytes = kBarOffset + (3 * STAGES + 1) * 8 + 8;
+    static constexpr int kASlots = 3;                           // A ring: [A_hi][A_lo]
+    static constexpr int kASlotBytes = 2 * kABytes;
+    static constexpr int kBStageBytes = 2 * kBBytes;            // B ring: [B_hi][B_lo]
+    static constexpr int kBOffset = kASlots * kASlotBytes;
+    static constexpr int kBarOffset = kBOffset + STAGES * kBStageBytes;
+    // afull[A], aconv[A], aempty[A], bfull[S], bempty[S], done, then the TMEM slot
+    static constexpr int kNumBars = 3 * kASlots + 2 * STAGES + 1;
+    static constexpr int kBytes = kBarOffset + kNumBars * 8 + 8;
     static constexpr int kDynBytes = kBytes + 1024;
 };
 
@@ -522,21 +543,23 @@ tf32x3_fused_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b_hi,
                     const __grid_constant__ CUtensorMap map_b_lo, const TcArgs p) {
     using L = FusedSmem<BN, STAGES>;
+    constexpr int NA = L::kASlots;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
     const uint32_t bar0 = base + L::kBarOffset;
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto conv_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
-    const uint32_t done_bar = bar0 + 8u * (3 * STAGES);
-    uint32_t *tmem_slot =
-        reinterpret_cast<uint32_t *>(gbase + L::kBarOffset + (3 * STAGES + 1) * 8);
-    auto a_hi = [&](int s) { return base + s * L::kStageBytes; };
-    auto a_lo = [&](int s) { return base + s * L::kStageBytes + L::kABytes; };
-    auto b_hi = [&](int s) { return base + s * L::kStageBytes + 2 * L::kABytes; };
-    auto b_lo = [&](int s) { return base + s * L::kStageBytes + 2 * L::kABytes + L::kBBytes; };
+    auto afull_bar = [&](int r) { return bar0 + 8u * r; };
+    auto aconv_bar = [&](int r) { return bar0 + 8u * (NA + r); };
+    auto aempty_bar = [&](int r) { return bar0 + 8u * (2 * NA + r); };
+    auto bfull_bar = [&](int s) { return bar0 + 8u * (3 * NA + s); };
+    auto bempty_bar = [&](int s) { return bar0 + 8u * (3 * NA + STAGES + s); };
+    const uint32_t done_bar = bar0 + 8u * (3 * NA + 2 * STAGES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + L::kBarOffset + L::kNumBars * 8);
+    auto a_hi = [&](int r) { return base + r * L::kASlotBytes; };
+    auto a_lo = [&](int r) { return base + r * L::kASlotBytes + L::kABytes; };
+    auto b_hi = [&](int s) { return base + L::kBOffset + s * L::kBStageBytes; };
+    auto b_lo = [&](int s) { return base + L::kBOffset + s * L::kBStageBytes + L::kBBytes; };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -560,10 +583,14 @@ tf32x3_fused_kernel(const __grid_constant__ CUtensorMap map_a,
     const int nkb = max(0, min(nkb_all, kb0 + p.kb_per_split) - kb0);
 
     if (threadIdx.x == 0) {
+        for (int r = 0; r < NA; ++r) {
+            mbar_init(afull_bar(r), 1);
+            mbar_init(aconv_bar(r), kFusedThreads - 128);
+            mbar_init(aempty_bar(r), 1);
+        }
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(conv_bar(s), kFusedThreads - 128);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(bfull_bar(s), 1);
+            mbar_init(bempty_bar(s), 1);
         }
         mbar_init(done_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -581,20 +608,31 @@ tf32x3_fused_kernel(const __grid_constant__ CUtensorMap map_a,
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    int issued = 0;
+    int issued_b = 0, issued_a = 0;   // K blocks each producer issued
     if (warp == 0 && lane == 0) {
-        // ---- TMA producer: raw A into the A_lo slot, packed B_hi/B_lo ----
+        // ---- TMA producer of the packed B_hi / B_lo tiles ----
         if (!p.inject_stall) {
             for (int kb = 0; kb < nkb; ++kb) {
                 const int s = kb % STAGES;
                 const uint32_t use = uint32_t(kb / STAGES);
-                if (kb >= STAGES && !mbar_wait(empty_bar(s), (use & 1u) ^ 1u, p.limit_ns)) break;
-                mbar_expect_tx(full_bar(s), uint32_t(L::kTxBytes));
+                if (kb >= STAGES && !mbar_wait(bempty_bar(s), (use & 1u) ^ 1u, p.limit_ns)) break;
+                mbar_expect_tx(bfull_bar(s), uint32_t(2 * L::kBBytes));
                 const int kc = (kb0 + kb) * kTcBK;
-                tma_load_2d(a_lo(s), &map_a, kc, m0, full_bar(s));
-                tma_load_2d(b_hi(s), &map_b_hi, kc, n0, full_bar(s));
-                tma_load_2d(b_lo(s), &map_b_lo, kc, n0, full_bar(s));
-                issued = kb + 1;
+                tma_load_2d(b_hi(s), &map_b_hi, kc, n0, bfull_bar(s));
+                tma_load_2d(b_lo(s), &map_b_lo, kc, n0, bfull_bar(s));
+                issued_b = kb + 1;
+            }
+        }
+    } else if (warp == 2 && lane == 0) {
+        // ---- TMA producer of the raw fp32 A tiles, into the A_lo slot ----
+        if (!p.inject_stall) {
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int r = kb % NA;
+                const uint32_t use = uint32_t(kb / NA);
+                if (kb >= NA && !mbar_wait(aempty_bar(r), (use & 1u) ^ 1u, p.limit_ns)) break;
+                mbar_expect_tx(afull_bar(r), uint32_t(L::kABytes));
+                tma_load_2d(a_lo(r), &map_a, (kb0 + kb) * kTcBK, m0, afull_bar(r));
+                issued_a = kb + 1;
             }
         }
     } else if (warp == 1 && lane == 0) {
@@ -602,9 +640,10 @@ tf32x3_fused_kernel(const __grid_constant__ CUtensorMap map_a,
         constexpr uint32_t idesc = tf32_idesc(BN);
         bool ok = true;
         for (int kb = 0; kb < nkb && ok; ++kb) {
-            const int s = kb % STAGES;
-            const uint32_t use = uint32_t(kb / STAGES);
-            if (!mbar_wait(conv_bar(s), use & 1u, p.limit_ns)) {
+            const int s = kb % STAGES, r = kb % NA;
+            const uint32_t use = uint32_t(kb / STAGES), ause = uint32_t(kb / NA);
+            if (!mbar_wait(aconv_bar(r), ause & 1u, p.limit_ns) ||
+                !mbar_wait(bfull_bar(s), use & 1u, p.limit_ns)) {
                 ok = false;
                 break;
             }
@@ -612,40 +651,43 @@ tf32x3_fused_kernel(const __grid_constant__ CUtensorMap map_a,
 #pragma unroll
             for (int kk = 0; kk < kTcBK / 8; ++kk) {
                 const uint32_t koff = uint32_t(kk) * 32u;
-                const uint64_t ah = sw128_desc(a_hi(s) + koff), al = sw128_desc(a_lo(s) + koff);
+                const uint64_t ah = sw128_desc(a_hi(r) + koff), al = sw128_desc(a_lo(r) + koff);
                 const uint64_t bh = sw128_desc(b_hi(s) + koff), bl = sw128_desc(b_lo(s) + koff);
                 mma_tf32(tmem, al, bh, idesc, (kb | kk) != 0 ? 1u : 0u);
                 mma_tf32(tmem, ah, bl, idesc, 1u);
                 mma_tf32(tmem, ah, bh, idesc, 1u);
             }
-            mma_commit(empty_bar(s));
+            mma_commit(aempty_bar(r));   // both arrive once these MMAs have finished
+            mma_commit(bempty_bar(s));
         }
         s_mma_ok = ok ? 1 : 0;
         mma_commit(done_bar);
     } else if (warp >= 4) {
-        // ---- converters: split the raw A tile in place ----
+        // ---- converters: the raw tile in A_lo becomes A_lo in place, plus A_hi ----
         const int c = threadIdx.x - 128;
         for (int kb = 0; kb < nkb; ++kb) {
-            const int s = kb % STAGES;
-            const uint32_t use = uint32_t(kb / STAGES);
-            if (!mbar_wait(full_bar(s), use & 1u, p.limit_ns)) break;
-            float4 *lo = reinterpret_cast<float4 *>(gbase + (a_lo(s) - base));
-            float4 *hi = reinterpret_cast<float4 *>(gbase + (a_hi(s) - base));
+            const int r = kb % NA;
+            if (!mbar_wait(afull_bar(r), uint32_t(kb / NA) & 1u, p.limit_ns)) break;
+            // 128-bit shared accesses, consecutive across the 128 threads; each
+            // thread reads all its elements before writing any of them back
+            constexpr int kQ = L::kABytes / 16 / 128;
+            float4 x[kQ];
 #pragma unroll
-            for (int q = 0; q < L::kABytes / 16 / 128; ++q) {
-                const int i = c + 128 * q;
-                const float4 x = lo[i];
+            for (int q = 0; q < kQ; ++q) x[q] = lds128(a_lo(r) + 16u * uint32_t(c + 128 * q));
+#pragma unroll
+            for (int q = 0; q < kQ; ++q) {
                 float4 h, l;
-                split2(x.x, h.x, l.x);
-                split2(x.y, h.y, l.y);
-                split2(x.z, h.z, l.z);
-                split2(x.w, h.w, l.w);
-                hi[i] = h;
-                lo[i] = l;
+                split2(x[q].x, h.x, l.x);
+                split2(x[q].y, h.y, l.y);
+                split2(x[q].z, h.z, l.z);
+                split2(x[q].w, h.w, l.w);
+                const uint32_t off = 16u * uint32_t(c + 128 * q);
+                sts128(a_hi(r) + off, h);
+                sts128(a_lo(r) + off, l);
             }
             // make the generic-proxy writes visible to the tensor cores
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(conv_bar(s));
+            mbar_arrive(aconv_bar(r));
         }
     }
     __syncwarp();
@@ -758,9 +800,14 @@ tf32x3_fused_kernel(const __grid_constant__ CUtensorMap map_a,
     // ---- teardown ----
     tc_fence_before();
     __syncthreads();
+    // copies still in flight (only after an expired wait) land before exit
     if (warp == 0 && lane == 0) {
-        for (int kb = (issued > STAGES ? issued - STAGES : 0); kb < issued; ++kb)
-            mbar_wait(full_bar(kb % STAGES), uint32_t(kb / STAGES) & 1u, p.limit_ns);
+        for (int kb = (issued_b > STAGES ? issued_b - STAGES : 0); kb < issued_b; ++kb)
+            mbar_wait(bfull_bar(kb % STAGES), uint32_t(kb / STAGES) & 1u, p.limit_ns);
+    }
+    if (warp == 2 && lane == 0) {
+        for (int kb = (issued_a > NA ? issued_a - NA : 0); kb < issued_a; ++kb)
+            mbar_wait(afull_bar(kb % NA), uint32_t(kb / NA) & 1u, p.limit_ns);
     }
     if (warp == 1 && lane == 0 && !have) mbar_wait(done_bar, 0u, p.limit_ns);
     __syncthreads();
@@ -869,13 +916,17 @@ bool tf32x3_fusable_a(const float *A, int64_t lda) {
     return (reinterpret_cast<uintptr_t>(A) & 15u) == 0 && lda % 4 == 0;
 }
 
-// The in-smem split of A (tf32x3_fused_kernel) is opt-in: measured on GB300
-// it is slower than the pre-pass (8192^3: 114 against 259 TFLOP/s), because
-// with two 96 KiB stages the conversion sits between the TMA landing and the
-// MMA on the critical path, which the two-deep ring cannot hide.
+// A is split inside the kernel (tf32x3_fused_kernel) whenever TMA can read it
+// as stored; SGEMM_TF32X3_FUSE_A=0 forces the pre-pass instead.  Measured on
+// GB300 (TFLOP/s, pre-pass / in-kernel): 8192^3 259 / 287 (271 / 300 with B
+// packed once), 4096^3 201 / 231, 1024x1024x16384 112 / 138.  What made the
+// in-kernel split pay was the branch-free TF32 rounding: with early returns
+// the converters' 64 conversions per slice did not interleave and the kernel
+// ran at 40 % of these rates.
 bool tf32x3_use_fused_a(const float *A, int64_t lda) {
     const char *env = std::getenv("SGEMM_TF32X3_FUSE_A");
-    return env && std::atoi(env) != 0 && tf32x3_fusable_a(A, lda);
+    if (env && std::atoi(env) == 0) return false;
+    return tf32x3_fusable_a(A, lda);
 }
 
 size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, int split, bool fused,

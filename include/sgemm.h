@@ -212,11 +212,11 @@ sgemm_status sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
  * accumulation in tensor memory (tcgen05.mma kind::tf32, TMA-fed).
  * Accuracy: max|C - exact| / (K*max|A|*max|B| + |beta|*max|C0|) <= 1e-5;
  * exact on integer inputs whose partial sums stay below 2^24 (their lo
- * parts are zero).  Any alignment and leading dimension are accepted: a
- * pre-pass splits A and B (B transposed) into a library-owned workspace of
- * about 8*(M+N)*ceil(K/4)*4 bytes per (device, stream), grown with
- * stream-ordered allocation (see below for splitting A in the kernel
- * instead).  Grids smaller than half the GPU are split along K (partials in
+ * parts are zero).  Any alignment and leading dimension are accepted: B is
+ * split and transposed into a library-owned workspace per call, and A is
+ * split inside the kernel (or, when its layout does not allow TMA, in a
+ * pre-pass into the same workspace) -- at most 8*(M+N)*ceil(K/4)*4 bytes per
+ * (device, stream), grown with stream-ordered allocation.  Grids smaller than half the GPU are split along K (partials in
  * the same workspace).  M, N, K must be below 2^31.  Every device-side
  * wait gives up after 1 s: the kernel then stores nothing to C and records
  * the event, which sgemm_device_status reports.
@@ -229,12 +229,11 @@ sgemm_status sgemm_tf32x3(int64_t M, int64_t N, int64_t K, float alpha,
  * 3xTF32 with B packed once.  The tensor cores read both operands K-major,
  * and B is stored K x N (N-major), so sgemm_tf32x3 transposes and splits B
  * into TF32 hi/lo parts on every call; these calls let a B that is
- * multiplied many times (weights) be packed once.  A is split per call, in a
- * pre-pass (default) or, with SGEMM_TF32X3_FUSE_A=1 in the environment and
- * A 16-byte aligned with lda % 4 == 0, inside the kernel's shared-memory
- * stage (the raw fp32 tile arrives by TMA and is split in place; no HBM pass
- * over A).  The in-kernel split is measured slower on GB300 and so is off by
- * default.
+ * multiplied many times (weights) be packed once.  A is K-major as stored:
+ * when it is 16-byte aligned with lda % 4 == 0 its split happens inside the
+ * kernel's shared-memory stage (the raw fp32 tile arrives by TMA and is split
+ * in place, with no pass over A in HBM); otherwise, or with
+ * SGEMM_TF32X3_FUSE_A=0 in the environment, in a pre-pass.
  *
  * sgemm_tf32x3_packed_b_bytes -- size of the packed form of a K x N matrix
  *   (0 for K or N <= 0).

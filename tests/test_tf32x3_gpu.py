@@ -131,20 +131,23 @@ def test_forced_split(sg, monkeypatch, split):
     check(q, run(sg, q), exact=True)        # 10 K blocks: split 16 leaves empty ranges
 
 
+@pytest.mark.parametrize("fuse", ["0", "1"])
 @pytest.mark.parametrize("name", ["square1024ab", "ragged", "gpt2_mlp_down", "long_k",
                                   "square256_int"])
-def test_in_kernel_split_of_a(sg, monkeypatch, name):
-    """SGEMM_TF32X3_FUSE_A=1: A split in shared memory (when its stride allows TMA)."""
-    monkeypatch.setenv("SGEMM_TF32X3_FUSE_A", "1")
+def test_both_splits_of_a(sg, monkeypatch, name, fuse):
+    """A split in the kernel (default when its stride allows TMA) or by a pre-pass
+    (SGEMM_TF32X3_FUSE_A=0)."""
+    monkeypatch.setenv("SGEMM_TF32X3_FUSE_A", fuse)
     p = workloads.workload(name)
     check(p, run(sg, p), exact=p.meta["dist"] == "int4")
     q = workloads.make(200, 300, 72, dist="int4", seed=81, alpha=1.5, beta=0.5, c0_dist="int4")
     check(q, run(sg, q), exact=True)
 
 
-def test_in_kernel_split_bounded_waits(sg, monkeypatch):
+def test_prepass_split_bounded_waits(sg, monkeypatch):
+    """The same bounded-wait check on the pre-pass kernel."""
     import torch
-    monkeypatch.setenv("SGEMM_TF32X3_FUSE_A", "1")
+    monkeypatch.setenv("SGEMM_TF32X3_FUSE_A", "0")
     M, N, K = 256, 512, 128
     A = torch.ones((M, K), device="cuda")
     B = torch.ones((K, N), device="cuda")
