@@ -44,6 +44,54 @@ __global__ void transpose_kernel(const float *__restrict__ A, int64_t M, int64_t
     }
 }
 
+// The same with 64 x 64 tiles and 128-bit global accesses (A and At 16-byte
+// aligned, lda and ldt multiples of 4, ldt covering M rounded up to 4): each
+// of 256 threads loads four float4 along k and stores four float4 along m.
+// The shared tile is padded by one float per row; the column reads of the
+// store phase then see at most two-way bank conflicts.
+__global__ void __launch_bounds__(256) transpose64_kernel(const float *__restrict__ A, int64_t M,
+                                                          int64_t K, int64_t lda,
+                                                          float *__restrict__ At, int64_t ldt) {
+    __shared__ float tile[64][65];
+    const int64_t m0 = int64_t(blockIdx.y) * 64, k0 = int64_t(blockIdx.x) * 64;
+    const int t = threadIdx.x;
+    const int c4 = (t & 15) * 4;   // 4 consecutive columns of the tile
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = (t >> 4) + 16 * i;   // tile row (m)
+        const int64_t m = m0 + r, k = k0 + c4;
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (m < M) {
+            if (k + 3 < K) {
+                v = __ldg(reinterpret_cast<const float4 *>(A + m * lda + k));
+            } else {
+                const float *src = A + m * lda;
+                v.x = k + 0 < K ? src[k + 0] : 0.0f;
+                v.y = k + 1 < K ? src[k + 1] : 0.0f;
+                v.z = k + 2 < K ? src[k + 2] : 0.0f;
+                v.w = k + 3 < K ? src[k + 3] : 0.0f;
+            }
+        }
+        tile[r][c4 + 0] = v.x;
+        tile[r][c4 + 1] = v.y;
+        tile[r][c4 + 2] = v.z;
+        tile[r][c4 + 3] = v.w;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = (t >> 4) + 16 * i;   // tile column (k) = output row
+        const int64_t k = k0 + r, m = m0 + c4;
+        if (k < K && m < M) {
+            // m .. m+3 lie inside the row of At (ldt >= M rounded up to 4);
+            // entries past M are zeros from the tile
+            const float4 v = make_float4(tile[c4 + 0][r], tile[c4 + 1][r], tile[c4 + 2][r],
+                                         tile[c4 + 3][r]);
+            *reinterpret_cast<float4 *>(At + k * ldt + m) = v;
+        }
+    }
+}
+
 // C_b = act(beta * C_b + bias) for the K == 0 / alpha == 0 case of the
 // batched, fused-epilogue call (beta == 0 does not read C).
 __global__ void epilogue_only_kernel(float *C, int64_t M, int64_t N, int64_t ldc,
@@ -121,8 +169,16 @@ cudaError_t launch_ffma(const GemmArgs &a, int kernel, int tile, bool vec, bool 
 
 cudaError_t launch_transpose(const float *A, int64_t M, int64_t K, int64_t lda, float *At,
                              int64_t ldt, cudaStream_t stream) {
-    const dim3 grid(unsigned((K + 31) / 32), unsigned((M + 31) / 32));
-    transpose_kernel<<<grid, dim3(32, 8), 0, stream>>>(A, M, K, lda, At, ldt);
+    const bool vec = (reinterpret_cast<uintptr_t>(A) & 15u) == 0 &&
+                     (reinterpret_cast<uintptr_t>(At) & 15u) == 0 && lda % 4 == 0 &&
+                     ldt % 4 == 0 && ldt >= (M + 3) / 4 * 4;
+    if (vec) {
+        const dim3 grid(unsigned((K + 63) / 64), unsigned((M + 63) / 64));
+        transpose64_kernel<<<grid, 256, 0, stream>>>(A, M, K, lda, At, ldt);
+    } else {
+        const dim3 grid(unsigned((K + 31) / 32), unsigned((M + 31) / 32));
+        transpose_kernel<<<grid, dim3(32, 8), 0, stream>>>(A, M, K, lda, At, ldt);
+    }
     return cudaGetLastError();
 }
 

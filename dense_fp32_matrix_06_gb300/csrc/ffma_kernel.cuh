@@ -545,9 +545,10 @@ cudaError_t launch_variant(const GemmArgs &a, cudaStream_t stream) {
                                    kBKT>;
     int dyn = 0;
     if constexpr (TC::kDynSmem) {
+        static bool configured[64];
         dyn = TC::kSmemBytes;
         const cudaError_t e =
-            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+            set_smem_once(reinterpret_cast<const void *>(kernel), dyn, configured);
         if (e != cudaSuccess) return e;
     }
     const int64_t tiles = int64_t(a.tiles_m) * a.tiles_n * a.batch;

@@ -613,7 +613,7 @@ sgemm_status tf32x3_run(int64_t M, int64_t N, int64_t K, float alpha, const floa
     if (M == 0 || N == 0) return SGEMM_OK;
     if (!C) return SGEMM_ERR_INVALID_ARG;
     if (K > 0 && alpha != 0.0f && (!A || !B)) return SGEMM_ERR_INVALID_ARG;
-    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return SGEMM_ERR_INVALID_ARG;
+    if (M > INT32_MAX || N > INT32_MAX || K > kTf32x3MaxK) return SGEMM_ERR_INVALID_ARG;
     int dev = 0, sms = 0;
     s = current_device(&dev, &sms);
     if (s != SGEMM_OK) return s;
@@ -766,7 +766,7 @@ extern "C" size_t sgemm_tf32x3_packed_b_bytes(int64_t K, int64_t N) {
 
 extern "C" sgemm_status sgemm_tf32x3_pack_b(int64_t K, int64_t N, const float *B, int64_t ldb,
                                            void *packed, size_t packed_bytes, void *stream) {
-    if (K <= 0 || N <= 0 || K > INT32_MAX || N > INT32_MAX) return SGEMM_ERR_INVALID_ARG;
+    if (K <= 0 || N <= 0 || K > kTf32x3MaxK || N > INT32_MAX) return SGEMM_ERR_INVALID_ARG;
     if (ldb < N || !B || !packed) return SGEMM_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(packed) & 255u) != 0) return SGEMM_ERR_MISALIGNED;
     if (packed_bytes < tf32x3_packed_b_bytes(K, N)) return SGEMM_ERR_WORKSPACE;
@@ -779,7 +779,7 @@ extern "C" sgemm_status sgemm_tf32x3_pack_b(int64_t K, int64_t N, const float *B
 extern "C" sgemm_status sgemm_tf32x3_packed(int64_t M, int64_t N, int64_t K, float alpha,
                                            const float *A, int64_t lda, const void *packed_b,
                                            float beta, float *C, int64_t ldc, void *stream) {
-    if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+    if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > kTf32x3MaxK)
         return SGEMM_ERR_INVALID_ARG;
     if (lda < std::max<int64_t>(1, K) || ldc < std::max<int64_t>(1, N))
         return SGEMM_ERR_INVALID_ARG;

@@ -29,6 +29,19 @@ constexpr size_t kCounterBytes = 16384;
 constexpr int64_t kMaxSplitTiles = kCounterBytes / sizeof(unsigned);
 constexpr int kMaxSplit = 32;
 
+// Sets the dynamic shared memory limit of `kernel` on the current device once
+// (per kernel and device; `flags` is the caller's per-kernel table).  Setting
+// it twice from racing threads is harmless.
+inline cudaError_t set_smem_once(const void *kernel, int bytes, bool (&flags)[64]) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && flags[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && dev >= 0 && dev < 64) flags[dev] = true;
+    return e;
+}
+
 // Epilogue activations.
 constexpr int kActNone = 0;
 constexpr int kActGeluTanh = 1;
@@ -98,7 +111,9 @@ cudaError_t launch_ffma_probe(int64_t ctas, int64_t iters, bool packed, float *o
                               cudaStream_t stream);
 cudaError_t ffma_kernel_attributes(cudaFuncAttributes *attr);
 
-// 3xTF32 tensor-core mode (tf32x3_gemm.cu).
+// 3xTF32 tensor-core mode (tf32x3_gemm.cu).  K runs along grid dimension y
+// of the split passes (32 rows of K per block at most).
+constexpr int64_t kTf32x3MaxK = int64_t(65535) * 32;
 int tf32x3_choose_split(int64_t M, int64_t N, int64_t K, int sms);
 size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, int split, bool fused,
                               bool packed_b);

@@ -106,6 +106,64 @@ __global__ void split_transpose_kernel(const float *__restrict__ B, int64_t K, i
     }
 }
 
+// The same with 64 x 64 tiles and 128-bit global accesses, for B 16-byte
+// aligned with ldb % 4 == 0 (ldo is a multiple of 4 and the outputs are
+// 256-byte aligned): 256 threads each load four float4 along n and store four
+// float4 of each output along k.  Rows of the tiles are padded by one float.
+__global__ void __launch_bounds__(256)
+split_transpose64_kernel(const float *__restrict__ B, int64_t K, int64_t N, int64_t ldb,
+                         float *__restrict__ hiT, float *__restrict__ loT, int64_t ldo) {
+    __shared__ float th[64][65];
+    __shared__ float tl[64][65];
+    const int64_t k0 = int64_t(blockIdx.y) * 64, n0 = int64_t(blockIdx.x) * 64;
+    const int t = threadIdx.x;
+    const int c4 = (t & 15) * 4;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = (t >> 4) + 16 * i;   // tile row (k)
+        const int64_t k = k0 + r, n = n0 + c4;
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (k < K) {
+            if (n + 3 < N) {
+                v = __ldg(reinterpret_cast<const float4 *>(B + k * ldb + n));
+            } else {
+                const float *src = B + k * ldb;
+                v.x = n + 0 < N ? src[n + 0] : 0.0f;
+                v.y = n + 1 < N ? src[n + 1] : 0.0f;
+                v.z = n + 2 < N ? src[n + 2] : 0.0f;
+                v.w = n + 3 < N ? src[n + 3] : 0.0f;
+            }
+        }
+        float h, l;
+        split2(v.x, h, l);
+        th[r][c4 + 0] = h;
+        tl[r][c4 + 0] = l;
+        split2(v.y, h, l);
+        th[r][c4 + 1] = h;
+        tl[r][c4 + 1] = l;
+        split2(v.z, h, l);
+        th[r][c4 + 2] = h;
+        tl[r][c4 + 2] = l;
+        split2(v.w, h, l);
+        th[r][c4 + 3] = h;
+        tl[r][c4 + 3] = l;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = (t >> 4) + 16 * i;   // tile column (n) = output row
+        const int64_t n = n0 + r, k = k0 + c4;
+        if (n < N && k < K) {
+            // k .. k+3 stay inside the output row (ldo >= K rounded up to 4);
+            // entries past K are zeros
+            *reinterpret_cast<float4 *>(hiT + n * ldo + k) =
+                make_float4(th[c4][r], th[c4 + 1][r], th[c4 + 2][r], th[c4 + 3][r]);
+            *reinterpret_cast<float4 *>(loT + n * ldo + k) =
+                make_float4(tl[c4][r], tl[c4 + 1][r], tl[c4 + 2][r], tl[c4 + 3][r]);
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // PTX wrappers (mbarrier, TMA, tcgen05)
 // ---------------------------------------------------------------------------
@@ -862,8 +920,9 @@ cudaError_t launch_mma(const CUtensorMap &ah, const CUtensorMap &al, const CUten
                        const CUtensorMap &bl, const TcArgs &a, cudaStream_t stream) {
     using L = TcSmem<BN, STAGES>;
     // the attribute is per device; set it on every call (cheap, host-side)
-    cudaError_t e = cudaFuncSetAttribute(tf32x3_mma_kernel<BN, STAGES>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynBytes);
+    static bool configured[64];
+    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(tf32x3_mma_kernel<BN, STAGES>),
+                                  L::kDynBytes, configured);
     if (e != cudaSuccess) return e;
     const unsigned grid = unsigned(int64_t(a.tiles_m) * a.tiles_n * a.split);
     tf32x3_mma_kernel<BN, STAGES><<<grid, kTcThreads, L::kDynBytes, stream>>>(ah, al, bh, bl, a);
@@ -874,8 +933,9 @@ template <int BN, int STAGES>
 cudaError_t launch_fused(const CUtensorMap &a, const CUtensorMap &bh, const CUtensorMap &bl,
                          const TcArgs &args, cudaStream_t stream) {
     using L = FusedSmem<BN, STAGES>;
-    cudaError_t e = cudaFuncSetAttribute(tf32x3_fused_kernel<BN, STAGES>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynBytes);
+    static bool configured[64];
+    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(tf32x3_fused_kernel<BN, STAGES>),
+                                  L::kDynBytes, configured);
     if (e != cudaSuccess) return e;
     const unsigned grid = unsigned(int64_t(args.tiles_m) * args.tiles_n * args.split);
     tf32x3_fused_kernel<BN, STAGES><<<grid, kFusedThreads, L::kDynBytes, stream>>>(a, bh, bl, args);
@@ -945,8 +1005,13 @@ cudaError_t tf32x3_pack_b(int64_t K, int64_t N, const float *B, int64_t ldb, voi
     float *b_hi = static_cast<float *>(packed);
     float *b_lo = reinterpret_cast<float *>(static_cast<char *>(packed) +
                                             round256(size_t(N) * kp * 4));
-    const dim3 tgrid(unsigned((N + 31) / 32), unsigned((K + 31) / 32));
-    split_transpose_kernel<<<tgrid, dim3(32, 8), 0, stream>>>(B, K, N, ldb, b_hi, b_lo, kp);
+    if ((reinterpret_cast<uintptr_t>(B) & 15u) == 0 && ldb % 4 == 0) {
+        const dim3 grid(unsigned((N + 63) / 64), unsigned((K + 63) / 64));
+        split_transpose64_kernel<<<grid, 256, 0, stream>>>(B, K, N, ldb, b_hi, b_lo, kp);
+    } else {
+        const dim3 tgrid(unsigned((N + 31) / 32), unsigned((K + 31) / 32));
+        split_transpose_kernel<<<tgrid, dim3(32, 8), 0, stream>>>(B, K, N, ldb, b_hi, b_lo, kp);
+    }
     return cudaGetLastError();
 }
 
