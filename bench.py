@@ -602,7 +602,7 @@ def run_extras(sg, device, stream):
 def run_configs(sg, device, stream):
     """TFLOP/s of sgemm and sgemm_tf32x3 on every configured workload (inputs
     resident, CUDA events, median; workloads under 200 MB get the L2 flushed
-    between repetitions)."""
+    between repetitions), and of the CPU oracle on a sample of its rows."""
     import torch
     sh = stream.cuda_stream
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
@@ -635,6 +635,11 @@ def run_configs(sg, device, stream):
                 ts.append(e0.elapsed_time(e1) / 1e3)
             ts.sort()
             res[mode] = round(p.flops / ts[len(ts) // 2] / 1e12, 3)
+        # the CPU oracle on a bounded sample of rows of the same problem
+        rows = min(p.M, max(16, int(2e10 / max(2.0 * p.N * p.K, 1.0))))
+        dt, oflops, threads = oracle_rows_rate(p, rows, seed=3)
+        res["oracle"] = round(oflops / dt / 1e12, 5)
+        res["oracle_sample"] = f"{rows} of {p.M} rows, {threads} threads"
         res["shape"] = f"{p.M}x{p.N}x{p.K}"
         res["l2_flushed"] = small
         out[name] = res
