@@ -6,8 +6,10 @@
 // method's product C = alpha*A*B + beta*C.
 //
 // Design (prior art on the pages, re-derived for a 152-SM Blackwell part):
-//  * CTA tile 128 x 128, K slice 16, 256 threads, 8 x 8 accumulators per
-//    thread updated as outer products: for every k the thread reads 8 values
+//  * Square CTA tiles (TileCfg): 128 x 128 with 256 threads (the main tile)
+//    or 64 x 64 with 64 threads, K slices of T/8 -- or 32 when both operands
+//    arrive by row copies -- and 8 x 8 accumulators per thread
+//    updated as outer products: for every k the thread reads 8 values
 //    of column k of the A tile and 8 of row k of the B tile and does 64 FMAs
 //    (velog @levelstage "AutoMinepp4", section "행렬곱: by 벡터의 외적": the
 //    product is a sum of outer products, which keeps the accumulators in
@@ -20,7 +22,7 @@
 //    Measured on GB300 the packed form is slower: it holds the FMA pipe two
 //    cycles, so it saves issue slots but not pipe time, and the broadcast
 //    operand pairs push the kernel past its 128-register budget.
-//  * The 8 x 8 block is split into four 4 x 4 quadrants 64 rows / 64 columns
+//  * The 8 x 8 block is split into four 4 x 4 quadrants T/2 rows / columns
 //    apart, so one 128-bit shared load serves 4 rows (or columns) and the
 //    loads of a warp are conflict-free: a warp reads 4 distinct 16-byte A
 //    chunks (each broadcast to 8 lanes) and 8 distinct B chunks.
@@ -32,6 +34,8 @@
 //    keeps the stores conflict-free (velog @levelstage "AutoMinepp7",
 //    section "직사각형 타일링": chunks are fetched into registers before the
 //    compute and split into the other local-memory page after it).
+//  * The FMAs of a k step run in boustrophedon order (every two consecutive
+//    FMAs share a source operand), which measured faster than row order.
 //  * Two smem pages: slice t+1 is in flight (registers and async copies)
 //    while slice t is computed; one barrier per K slice ("Micro_gemm_4x4 -
 //    cuBLAS micro GEMM skeleton", section 8, double buffering, with the
