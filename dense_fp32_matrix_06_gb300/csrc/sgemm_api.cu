@@ -632,21 +632,17 @@ sgemm_status tf32x3_run(int64_t M, int64_t N, int64_t K, float alpha, const floa
         e = launch_scale(C, M, N, ldc, beta, st);
         return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
     }
-    int split = tf32x3_choose_split(M, N, K, sms);
-    if (const char *force = std::getenv("SGEMM_TF32X3_FORCE_SPLIT")) {
-        const int f = std::atoi(force);
-        if (f >= 1 && f <= 64) split = f;
-    }
+    const Tf32x3Plan plan = tf32x3_plan(M, N, K, sms);
     // The per-stream workspace starts with the split-K tile counters, which
     // stay zero between calls; the hi/lo operands and partials follow.
     void *ws = nullptr;
     s = library_workspace(
         dev, st,
-        kCounterBytes + tf32x3_workspace_bytes(M, N, K, split, tf32x3_use_fused_a(A, lda), false),
+        kCounterBytes + tf32x3_workspace_bytes(M, N, K, plan, tf32x3_use_fused_a(A, lda), false),
         &ws);
     if (s != SGEMM_OK) return s;
     e = launch_tf32x3(A, lda, B, ldb, C, ldc, M, N, K, alpha, beta,
-                      static_cast<char *>(ws) + kCounterBytes, static_cast<unsigned *>(ws), split,
+                      static_cast<char *>(ws) + kCounterBytes, static_cast<unsigned *>(ws), plan,
                       limit_ns, inject_stall, st);
     return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
 }
@@ -806,19 +802,15 @@ extern "C" sgemm_status sgemm_tf32x3_packed(int64_t M, int64_t N, int64_t K, flo
     if (!A || !packed_b) return SGEMM_ERR_INVALID_ARG;
     if (!tf32x3_fusable_a(A, lda) || (reinterpret_cast<uintptr_t>(packed_b) & 255u) != 0)
         return SGEMM_ERR_MISALIGNED;
-    int split = tf32x3_choose_split(M, N, K, sms);
-    if (const char *force = std::getenv("SGEMM_TF32X3_FORCE_SPLIT")) {
-        const int f = std::atoi(force);
-        if (f >= 1 && f <= 64) split = f;
-    }
+    const Tf32x3Plan plan = tf32x3_plan(M, N, K, sms);
     void *ws = nullptr;
     s = library_workspace(
         dev, st,
-        kCounterBytes + tf32x3_workspace_bytes(M, N, K, split, tf32x3_use_fused_a(A, lda), true),
+        kCounterBytes + tf32x3_workspace_bytes(M, N, K, plan, tf32x3_use_fused_a(A, lda), true),
         &ws);
     if (s != SGEMM_OK) return s;
     e = launch_tf32x3_packed(A, lda, packed_b, C, ldc, M, N, K, alpha, beta,
                              static_cast<char *>(ws) + kCounterBytes, static_cast<unsigned *>(ws),
-                             split, kWaitLimitNs, 0, st);
+                             plan, kWaitLimitNs, 0, st);
     return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
 }

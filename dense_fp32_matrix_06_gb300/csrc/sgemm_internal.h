@@ -114,8 +114,22 @@ cudaError_t ffma_kernel_attributes(cudaFuncAttributes *attr);
 // 3xTF32 tensor-core mode (tf32x3_gemm.cu).  K runs along grid dimension y
 // of the split passes (32 rows of K per block at most).
 constexpr int64_t kTf32x3MaxK = int64_t(65535) * 32;
-int tf32x3_choose_split(int64_t M, int64_t N, int64_t K, int sms);
-size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, int split, bool fused,
+// Work decomposition of a tensor-mode launch: either every tile cut into
+// `split` K ranges (small grids), or only the tiles from tail_start on (the
+// last, partly filled wave) cut into `tail_split` ranges.
+struct Tf32x3Plan {
+    int split = 1;
+    int tail_split = 1;
+    int64_t tiles = 0;
+    int64_t tail_start = 0;   // == tiles when no tail is cut
+    // partial tiles the workspace must hold
+    int64_t partial_slots() const {
+        return split > 1 ? tiles * split : (tail_split > 1 ? (tiles - tail_start) * tail_split : 0);
+    }
+    int64_t grid() const { return tail_start * split + (tiles - tail_start) * tail_split; }
+};
+Tf32x3Plan tf32x3_plan(int64_t M, int64_t N, int64_t K, int sms);
+size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, const Tf32x3Plan &plan, bool fused,
                               bool packed_b);
 size_t tf32x3_packed_b_bytes(int64_t K, int64_t N);
 bool tf32x3_fusable_a(const float *A, int64_t lda);
@@ -124,11 +138,13 @@ cudaError_t tf32x3_pack_b(int64_t K, int64_t N, const float *B, int64_t ldb, voi
                           cudaStream_t stream);
 cudaError_t launch_tf32x3_packed(const float *A, int64_t lda, const void *packed_b, float *C,
                                  int64_t ldc, int64_t M, int64_t N, int64_t K, float alpha,
-                                 float beta, void *workspace, unsigned *counters, int split,
+                                 float beta, void *workspace, unsigned *counters,
+                                 const Tf32x3Plan &plan,
                                  uint64_t limit_ns, int inject_stall, cudaStream_t stream);
 cudaError_t launch_tf32x3(const float *A, int64_t lda, const float *B, int64_t ldb, float *C,
                           int64_t ldc, int64_t M, int64_t N, int64_t K, float alpha, float beta,
-                          void *workspace, unsigned *counters, int split, uint64_t limit_ns,
+                          void *workspace, unsigned *counters, const Tf32x3Plan &plan,
+                          uint64_t limit_ns,
                           int inject_stall, cudaStream_t stream);
 // Reads and clears the mode's device error word (synchronises `stream`).
 cudaError_t tf32x3_read_error(unsigned *out, cudaStream_t stream);

@@ -310,13 +310,52 @@ struct TcArgs {
     int32_t tiles_m, tiles_n;
     uint64_t limit_ns;     // bound on every mbarrier wait
     int32_t inject_stall;  // 1: the producer issues nothing (exercises the bounded waits)
-    // split-K: tile t's K blocks are cut into `split` ranges of kb_per_split
-    // blocks; CTA pid computes range pid % split of tile pid / split
+    // Work decomposition: tiles [0, tail_start) are cut into `split` K ranges
+    // of kb_per_split blocks, tiles [tail_start, tiles) into `tail_split`
+    // ranges of tail_kb_per_split (only the last, partly filled wave of tiles
+    // is cut when split == 1).  The ranges of a tile are consecutive CTAs.
+    // Split tiles only: partial slot of CTA x is x - part_base, counter of
+    // tile t is counters[t - cnt_base].
     int32_t split;
     int32_t kb_per_split;
+    int32_t tail_start;
+    int32_t tail_split;
+    int32_t tail_kb_per_split;
+    int32_t part_base;
+    int32_t cnt_base;
     unsigned *counters;    // split > 1: one ticket per tile, zero on entry and exit
     float *partials;       // split > 1: tiles * split partial tiles of 128 x BN
 };
+
+// (tile, K range) of this CTA.
+struct TcWork {
+    int pid;          // tile
+    int sidx, ns;     // range index, ranges of the tile
+    int kbps;         // K blocks per range
+    int slot_first;   // partial slot of the tile's first range
+    int cnt;          // counter index
+};
+
+__device__ __forceinline__ TcWork tc_work(const TcArgs &p) {
+    TcWork w;
+    const int x = int(blockIdx.x);
+    const int lead = p.tail_start * p.split;
+    if (x < lead) {
+        w.pid = x / p.split;
+        w.sidx = x - w.pid * p.split;
+        w.ns = p.split;
+        w.kbps = p.kb_per_split;
+    } else {
+        const int j = x - lead;
+        w.pid = p.tail_start + j / p.tail_split;
+        w.sidx = j % p.tail_split;
+        w.ns = p.tail_split;
+        w.kbps = p.tail_kb_per_split;
+    }
+    w.slot_first = x - w.sidx - p.part_base;
+    w.cnt = w.pid - p.cnt_base;
+    return w;
+}
 
 template <int BN, int STAGES>
 struct TcSmem {
@@ -356,8 +395,9 @@ tf32x3_mma_kernel(const __grid_constant__ CUtensorMap map_a_hi,
     __shared__ unsigned s_ticket;
 
     // (tile, K range) of this CTA; grouped raster over 8 tile rows
-    const int pid = blockIdx.x / p.split;
-    const int split_idx = blockIdx.x - pid * p.split;
+    const TcWork work = tc_work(p);
+    const int pid = work.pid;
+    const int split_idx = work.sidx;
     const int per_group = 8 * p.tiles_n;
     const int group = pid / per_group;
     const int first_m = group * 8;
@@ -368,8 +408,8 @@ tf32x3_mma_kernel(const __grid_constant__ CUtensorMap map_a_hi,
     const int m0 = tile_m * kTcBM;
     const int n0 = tile_n * BN;
     const int nkb_all = int((p.K + kTcBK - 1) / kTcBK);
-    const int kb0 = split_idx * p.kb_per_split;
-    const int nkb = max(0, min(nkb_all, kb0 + p.kb_per_split) - kb0);   // K blocks of this CTA
+    const int kb0 = split_idx * work.kbps;
+    const int nkb = max(0, min(nkb_all, kb0 + work.kbps) - kb0);   // K blocks of this CTA
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -478,7 +518,7 @@ tf32x3_mma_kernel(const __grid_constant__ CUtensorMap map_a_hi,
         }
     };
 
-    if (p.split == 1) {
+    if (work.ns == 1) {
         if (__all_sync(0xffffffffu, clean)) {
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -490,7 +530,7 @@ tf32x3_mma_kernel(const __grid_constant__ CUtensorMap map_a_hi,
     } else {
         // partial tile of this K range: slot blockIdx.x, row-major 128 x BN
         const size_t slot = size_t(kTcBM) * BN;
-        float *part = p.partials + size_t(pid) * p.split * slot;
+        float *part = p.partials + size_t(work.slot_first) * slot;
         float *mine = part + size_t(split_idx) * slot + size_t(warp * 32 + lane) * BN;
         if (__all_sync(0xffffffffu, clean)) {
 #pragma unroll 1
@@ -514,13 +554,13 @@ tf32x3_mma_kernel(const __grid_constant__ CUtensorMap map_a_hi,
         // 0x10001, so the tile still completes (and rearms) but is not stored
         if (threadIdx.x == 0) {
             const unsigned add = clean ? 1u : 0x10001u;
-            const unsigned now = atomicAdd(p.counters + pid, add) + add;
+            const unsigned now = atomicAdd(p.counters + work.cnt, add) + add;
             s_ticket = now;
-            if ((now & 0xffffu) == unsigned(p.split)) p.counters[pid] = 0u;
+            if ((now & 0xffffu) == unsigned(work.ns)) p.counters[work.cnt] = 0u;
         }
         __syncthreads();
         const unsigned now = s_ticket;
-        if ((now & 0xffffu) == unsigned(p.split) && (now >> 16) == 0u && row_ok) {
+        if ((now & 0xffffu) == unsigned(work.ns) && (now >> 16) == 0u && row_ok) {
             __threadfence();
             const float *base = part + size_t(warp * 32 + lane) * BN;
 #pragma unroll 1
@@ -528,7 +568,7 @@ tf32x3_mma_kernel(const __grid_constant__ CUtensorMap map_a_hi,
                 float v[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-                for (int sidx = 0; sidx < p.split; ++sidx) {
+                for (int sidx = 0; sidx < work.ns; ++sidx) {
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const float4 x = __ldcg(reinterpret_cast<const float4 *>(
@@ -625,8 +665,9 @@ tf32x3_fused_kernel(const __grid_constant__ CUtensorMap map_a,
     __shared__ unsigned s_ticket;
 
     // (tile, K range) of this CTA; grouped raster over 8 tile rows
-    const int pid = blockIdx.x / p.split;
-    const int split_idx = blockIdx.x - pid * p.split;
+    const TcWork work = tc_work(p);
+    const int pid = work.pid;
+    const int split_idx = work.sidx;
     const int per_group = 8 * p.tiles_n;
     const int group = pid / per_group;
     const int first_m = group * 8;
@@ -637,8 +678,8 @@ tf32x3_fused_kernel(const __grid_constant__ CUtensorMap map_a,
     const int m0 = tile_m * kTcBM;
     const int n0 = tile_n * BN;
     const int nkb_all = int((p.K + kTcBK - 1) / kTcBK);
-    const int kb0 = split_idx * p.kb_per_split;
-    const int nkb = max(0, min(nkb_all, kb0 + p.kb_per_split) - kb0);
+    const int kb0 = split_idx * work.kbps;
+    const int nkb = max(0, min(nkb_all, kb0 + work.kbps) - kb0);
 
     if (threadIdx.x == 0) {
         for (int r = 0; r < NA; ++r) {
@@ -792,7 +833,7 @@ tf32x3_fused_kernel(const __grid_constant__ CUtensorMap map_a,
         }
     };
 
-    if (p.split == 1) {
+    if (work.ns == 1) {
         if (__all_sync(0xffffffffu, clean)) {
 #pragma unroll 1
             for (int c0 = cbeg; c0 < cbeg + BN / 2; c0 += 32) {
@@ -803,7 +844,7 @@ tf32x3_fused_kernel(const __grid_constant__ CUtensorMap map_a,
         }
     } else {
         const size_t slot = size_t(kTcBM) * BN;
-        float *part = p.partials + size_t(pid) * p.split * slot;
+        float *part = p.partials + size_t(work.slot_first) * slot;
         float *mine = part + size_t(split_idx) * slot + size_t(lrow) * BN;
         if (__all_sync(0xffffffffu, clean)) {
 #pragma unroll 1
@@ -825,13 +866,13 @@ tf32x3_fused_kernel(const __grid_constant__ CUtensorMap map_a,
         __syncthreads();
         if (threadIdx.x == 0) {
             const unsigned add = clean ? 1u : 0x10001u;
-            const unsigned now = atomicAdd(p.counters + pid, add) + add;
+            const unsigned now = atomicAdd(p.counters + work.cnt, add) + add;
             s_ticket = now;
-            if ((now & 0xffffu) == unsigned(p.split)) p.counters[pid] = 0u;
+            if ((now & 0xffffu) == unsigned(work.ns)) p.counters[work.cnt] = 0u;
         }
         __syncthreads();
         const unsigned now = s_ticket;
-        if ((now & 0xffffu) == unsigned(p.split) && (now >> 16) == 0u && row_ok) {
+        if ((now & 0xffffu) == unsigned(work.ns) && (now >> 16) == 0u && row_ok) {
             __threadfence();
             const float *rowp = part + size_t(lrow) * BN;
 #pragma unroll 1
@@ -839,7 +880,7 @@ tf32x3_fused_kernel(const __grid_constant__ CUtensorMap map_a,
                 float v[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-                for (int sidx = 0; sidx < p.split; ++sidx) {
+                for (int sidx = 0; sidx < work.ns; ++sidx) {
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const float4 x = __ldcg(reinterpret_cast<const float4 *>(
@@ -924,7 +965,9 @@ cudaError_t launch_mma(const CUtensorMap &ah, const CUtensorMap &al, const CUten
     cudaError_t e = set_smem_once(reinterpret_cast<const void *>(tf32x3_mma_kernel<BN, STAGES>),
                                   L::kDynBytes, configured);
     if (e != cudaSuccess) return e;
-    const unsigned grid = unsigned(int64_t(a.tiles_m) * a.tiles_n * a.split);
+    const int64_t tiles = int64_t(a.tiles_m) * a.tiles_n;
+    const unsigned grid = unsigned(int64_t(a.tail_start) * a.split +
+                                   (tiles - a.tail_start) * a.tail_split);
     tf32x3_mma_kernel<BN, STAGES><<<grid, kTcThreads, L::kDynBytes, stream>>>(ah, al, bh, bl, a);
     return cudaGetLastError();
 }
@@ -937,7 +980,9 @@ cudaError_t launch_fused(const CUtensorMap &a, const CUtensorMap &bh, const CUte
     cudaError_t e = set_smem_once(reinterpret_cast<const void *>(tf32x3_fused_kernel<BN, STAGES>),
                                   L::kDynBytes, configured);
     if (e != cudaSuccess) return e;
-    const unsigned grid = unsigned(int64_t(args.tiles_m) * args.tiles_n * args.split);
+    const int64_t tiles = int64_t(args.tiles_m) * args.tiles_n;
+    const unsigned grid = unsigned(int64_t(args.tail_start) * args.split +
+                                   (tiles - args.tail_start) * args.tail_split);
     tf32x3_fused_kernel<BN, STAGES><<<grid, kFusedThreads, L::kDynBytes, stream>>>(a, bh, bl, args);
     return cudaGetLastError();
 }
@@ -958,13 +1003,39 @@ size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 // most half the SMs and every range kept >= 24 K blocks (768 of K) --
 // 1024x1024x16384: 51 -> 111 TFLOP/s at 4 ranges, 1024x768x3072: 40 -> 54 at
 // 3-4 -- and lost everywhere else (1024^3, GPT-2 QKV/MLP-up, 2048^3, 4096^3).
-int tf32x3_choose_split(int64_t M, int64_t N, int64_t K, int sms) {
+Tf32x3Plan tf32x3_plan(int64_t M, int64_t N, int64_t K, int sms) {
+    Tf32x3Plan plan;
     const int64_t tiles = ((M + kTcBM - 1) / kTcBM) * ((N + kTcBN - 1) / kTcBN);
     const int64_t nkb = (K + kTcBK - 1) / kTcBK;
-    if (sms <= 0 || tiles > kMaxSplitTiles || 2 * tiles > sms) return 1;
-    int64_t s = std::min<int64_t>(sms / tiles, nkb / 24);
-    s = std::min<int64_t>(s, 16);
-    return s > 1 ? int(s) : 1;
+    plan.tiles = tiles;
+    plan.tail_start = tiles;
+    if (sms <= 0) return plan;
+    if (const char *force = std::getenv("SGEMM_TF32X3_FORCE_SPLIT")) {
+        const int f = std::atoi(force);
+        if (f >= 1 && f <= 64 && tiles <= kMaxSplitTiles) {
+            plan.split = f;
+            return plan;
+        }
+    }
+    if (tiles <= kMaxSplitTiles && 2 * tiles <= sms) {
+        int64_t sp = std::min<int64_t>(sms / tiles, nkb / 24);
+        sp = std::min<int64_t>(sp, 16);
+        plan.split = sp > 1 ? int(sp) : 1;
+        return plan;
+    }
+    // Tail: with one CTA per SM, a last wave of tiles that fills at most half
+    // the SMs idles the rest for a whole tile's time; cut just those tiles
+    // into K ranges (all of them still fitting in one wave).
+    // SGEMM_TF32X3_FORCE_TAIL=0 disables it, =s forces s ranges.
+    const int64_t rem = tiles % sms;
+    int want = 0;
+    if (rem > 0 && 2 * rem <= sms) want = int(std::min<int64_t>(sms / rem, 4));
+    if (const char *force = std::getenv("SGEMM_TF32X3_FORCE_TAIL")) want = std::atoi(force);
+    if (tiles >= sms && rem > 0 && want >= 2 && rem * want <= sms && nkb >= 8 * want) {
+        plan.tail_start = tiles - rem;
+        plan.tail_split = want;
+    }
+    return plan;
 }
 
 size_t tf32x3_packed_b_bytes(int64_t K, int64_t N) {
@@ -989,13 +1060,12 @@ bool tf32x3_use_fused_a(const float *A, int64_t lda) {
     return tf32x3_fusable_a(A, lda);
 }
 
-size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, int split, bool fused,
-                              bool packed_b) {
+size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, const Tf32x3Plan &plan,
+                              bool fused, bool packed_b) {
     const int64_t kp = (K + 3) / 4 * 4;
     const size_t a = fused ? 0 : 2 * round256(size_t(M) * kp * 4);
     const size_t b = packed_b ? 0 : tf32x3_packed_b_bytes(K, N);
-    const int64_t tiles = ((M + kTcBM - 1) / kTcBM) * ((N + kTcBN - 1) / kTcBN);
-    const size_t parts = split > 1 ? size_t(tiles) * split * kTcBM * kTcBN * 4 : 0;
+    const size_t parts = size_t(plan.partial_slots()) * kTcBM * kTcBN * 4;
     return a + b + parts;
 }
 
@@ -1018,8 +1088,8 @@ cudaError_t tf32x3_pack_b(int64_t K, int64_t N, const float *B, int64_t ldb, voi
 namespace {
 
 TcArgs make_args(float *C, int64_t ldc, int64_t M, int64_t N, int64_t K, float alpha,
-                 float beta, unsigned *counters, float *parts, int split, uint64_t limit_ns,
-                 int inject_stall) {
+                 float beta, unsigned *counters, float *parts, const Tf32x3Plan &plan,
+                 uint64_t limit_ns, int inject_stall) {
     TcArgs a;
     a.C = C;
     a.M = M;
@@ -1033,8 +1103,14 @@ TcArgs make_args(float *C, int64_t ldc, int64_t M, int64_t N, int64_t K, float a
     a.limit_ns = limit_ns;
     a.inject_stall = inject_stall;
     const int64_t nkb = (K + kTcBK - 1) / kTcBK;
-    a.split = split > 1 ? split : 1;
+    a.split = plan.split > 1 ? plan.split : 1;
     a.kb_per_split = int32_t((nkb + a.split - 1) / a.split);
+    a.tail_start = int32_t(plan.tail_start);
+    a.tail_split = plan.tail_split > 1 ? plan.tail_split : 1;
+    a.tail_kb_per_split = int32_t((nkb + a.tail_split - 1) / a.tail_split);
+    // partial slots / counters only for split tiles
+    a.part_base = a.split > 1 ? 0 : a.tail_start;
+    a.cnt_base = a.split > 1 ? 0 : a.tail_start;
     a.counters = counters;
     a.partials = parts;
     return a;
@@ -1046,8 +1122,9 @@ TcArgs make_args(float *C, int64_t ldc, int64_t M, int64_t N, int64_t K, float a
 // is split in shared memory) followed by the split-K partials.
 cudaError_t launch_tf32x3_packed(const float *A, int64_t lda, const void *packed_b, float *C,
                                  int64_t ldc, int64_t M, int64_t N, int64_t K, float alpha,
-                                 float beta, void *workspace, unsigned *counters, int split,
-                                 uint64_t limit_ns, int inject_stall, cudaStream_t stream) {
+                                 float beta, void *workspace, unsigned *counters,
+                                 const Tf32x3Plan &plan, uint64_t limit_ns, int inject_stall,
+                                 cudaStream_t stream) {
     const int64_t kp = (K + 3) / 4 * 4;
     const float *b_hi = static_cast<const float *>(packed_b);
     const float *b_lo = reinterpret_cast<const float *>(static_cast<const char *>(packed_b) +
@@ -1060,7 +1137,7 @@ cudaError_t launch_tf32x3_packed(const float *A, int64_t lda, const void *packed
             !encode_kmajor(&bh, b_hi, N, K, kp, kTcBN) || !encode_kmajor(&bl, b_lo, N, K, kp, kTcBN))
             return cudaErrorInvalidValue;
         const TcArgs a = make_args(C, ldc, M, N, K, alpha, beta, counters,
-                                   reinterpret_cast<float *>(w), split, limit_ns, inject_stall);
+                                   reinterpret_cast<float *>(w), plan, limit_ns, inject_stall);
         return launch_fused<kTcBN, kTcStages>(am, bh, bl, a, stream);
     }
     const size_t abytes = round256(size_t(M) * kp * 4);
@@ -1076,15 +1153,15 @@ cudaError_t launch_tf32x3_packed(const float *A, int64_t lda, const void *packed
     if (!encode_kmajor(&ah, a_hi, M, K, kp, kTcBM) || !encode_kmajor(&al, a_lo, M, K, kp, kTcBM) ||
         !encode_kmajor(&bh, b_hi, N, K, kp, kTcBN) || !encode_kmajor(&bl, b_lo, N, K, kp, kTcBN))
         return cudaErrorInvalidValue;
-    const TcArgs a = make_args(C, ldc, M, N, K, alpha, beta, counters, parts, split, limit_ns,
+    const TcArgs a = make_args(C, ldc, M, N, K, alpha, beta, counters, parts, plan, limit_ns,
                                inject_stall);
     return launch_mma<kTcBN, kTcStages>(ah, al, bh, bl, a, stream);
 }
 
 cudaError_t launch_tf32x3(const float *A, int64_t lda, const float *B, int64_t ldb, float *C,
                           int64_t ldc, int64_t M, int64_t N, int64_t K, float alpha, float beta,
-                          void *workspace, unsigned *counters, int split, uint64_t limit_ns,
-                          int inject_stall, cudaStream_t stream) {
+                          void *workspace, unsigned *counters, const Tf32x3Plan &plan,
+                          uint64_t limit_ns, int inject_stall, cudaStream_t stream) {
     constexpr int BN = kTcBN, STAGES = kTcStages;
     const int64_t kp = (K + 3) / 4 * 4;
     char *w = static_cast<char *>(workspace);
@@ -1093,7 +1170,7 @@ cudaError_t launch_tf32x3(const float *A, int64_t lda, const float *B, int64_t l
         cudaError_t e = tf32x3_pack_b(K, N, B, ldb, w, stream);
         if (e != cudaSuccess) return e;
         return launch_tf32x3_packed(A, lda, w, C, ldc, M, N, K, alpha, beta,
-                                    w + tf32x3_packed_b_bytes(K, N), counters, split, limit_ns,
+                                    w + tf32x3_packed_b_bytes(K, N), counters, plan, limit_ns,
                                     inject_stall, stream);
     }
     // both operands split (and B transposed) in a pre-pass
@@ -1117,7 +1194,7 @@ cudaError_t launch_tf32x3(const float *A, int64_t lda, const float *B, int64_t l
     if (!encode_kmajor(&ah, a_hi, M, K, kp, kTcBM) || !encode_kmajor(&al, a_lo, M, K, kp, kTcBM) ||
         !encode_kmajor(&bh, b_hi, N, K, kp, BN) || !encode_kmajor(&bl, b_lo, N, K, kp, BN))
         return cudaErrorInvalidValue;
-    const TcArgs a = make_args(C, ldc, M, N, K, alpha, beta, counters, parts, split, limit_ns,
+    const TcArgs a = make_args(C, ldc, M, N, K, alpha, beta, counters, parts, plan, limit_ns,
                                inject_stall);
     return launch_mma<BN, STAGES>(ah, al, bh, bl, a, stream);
 }

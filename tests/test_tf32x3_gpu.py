@@ -160,6 +160,18 @@ def test_prepass_split_bounded_waits(sg, monkeypatch):
     assert sg.device_status(stream) == 0
 
 
+@pytest.mark.parametrize("tail", ["0", "2", "3"])
+def test_tail_split(sg, monkeypatch, tail):
+    """Only the last, partly filled wave of tiles cut along K (2048 x 2560: 160
+    tiles of 128 x 256, 8 of them past the first wave on 152 SMs)."""
+    monkeypatch.setenv("SGEMM_TF32X3_FORCE_TAIL", tail)
+    p = workloads.make(2048, 2560, 1000, seed=91, alpha=0.75, beta=0.5, c0_dist="uniform")
+    check(p, run(sg, p), exact=False)
+    q = workloads.make(2048, 2560, 800, dist="int4", seed=92, alpha=1.5, beta=0.5,
+                       c0_dist="int4")
+    check(q, run(sg, q), exact=True)
+
+
 def test_split_plans_for_small_grids(sg):
     # these run with more K ranges than tiles; parity at full size
     for name in ("long_k", "gpt2_mlp_down", "square1024ab"):
