@@ -237,24 +237,23 @@ void plan_core(int64_t M, int64_t N, int64_t K, int64_t batch, bool vec, int sms
 // Transposing A first.  The kernel stages an operand whose stored rows run
 // along K (A as given) through registers and transposing shared stores, and
 // copies one whose rows run along M (A^T) straight in with cp.async, which
-// leaves it 8 registers and ~10 instructions per K slice lighter.  Measured
-// on GB300 (TFLOP/s, A as given / A^T given): 8192^3 60.75 / 63.53,
-// 4096^3 58.5 / 60.9, 2048^3 49.2 / 52.1.  A transpose pass costs
-// 8*M*K bytes of HBM traffic, about 35/N of the product's time at the fp32
-// rate, so it pays for 128-wide plans of at least two waves of tiles with
-// N >= 1024 and K >= 256.  With the pass, and the product in K slices of 32
-// (both operands are then row copies): 8192^3 60.7 -> 64.5 TFLOP/s, 4096^3
-// 58.4 -> 61.4; it loses at K = 64 (47.5 -> 45.4) and for 2048^3 (256 tiles,
-// under one wave).  The copy lives in the workspace (K x M floats after the
-// counter block).  Split-K plans can take it too (partials before the copy),
-// but measured it loses there (GPT-2 QKV 41.8 -> 38.6, 1024^3 31.5 -> 28.5),
-// so only the override selects it for them.
+// leaves it 8 registers and ~10 instructions per K slice lighter, and lets
+// the product run in K slices of 32 through a three-page ring.  A transpose
+// pass costs 8*M*K bytes of HBM traffic, about 35/N of the product's time.
+// Measured on GB300 (TFLOP/s, without / with the pass): 8192^3 60.7 / 65.8,
+// 4096^3 58.4 / 62.4, 2048^3 48.7 / 50.9, 1024x1024x16384 (split-K) 47.0 /
+// 49.2; it loses for K = 64 (47.5 / 46.7), for GPT-2 QKV (144 tiles, under
+// one per SM: 43.9 / 43.4) and for split-K plans with short K (1024^3 31.5 /
+// 29.3, MLP-up 39.8 / 38.2).  Hence: N >= 1024, K >= 256, and either no
+// split with at least one tile per SM, or split-K with K >= 8192.  The copy
+// lives in the workspace after the counters and any split-K partials.
 // SGEMM_FORCE_TRANSPOSE_A=0/1 overrides the choice for sweeps.
 bool choose_transpose_a(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int sms) {
     const bool able = p.bm == 128 && p.tail_split == 1 && p.vec && K >= 1 &&
                       M <= int64_t(65535) * 32;
-    bool want = able && p.split_k == 1 && N >= 1024 && K >= 256 &&
-                p.tiles_m * p.tiles_n >= int64_t(2) * kCtasPerSm * sms;
+    const int64_t tiles = p.tiles_m * p.tiles_n;
+    bool want = able && N >= 1024 && K >= 256 &&
+                ((p.split_k == 1 && tiles >= sms) || (p.split_k > 1 && K >= 8192));
     if (const char *force = std::getenv("SGEMM_FORCE_TRANSPOSE_A")) {
         const int f = std::atoi(force);
         if (f == 0) want = false;

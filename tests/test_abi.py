@@ -124,9 +124,11 @@ def test_plan_full_tiles_take_the_unchecked_vector_path(lib):
 
 def test_plan_transpose_choice(lib, monkeypatch):
     assert plan(4096, 4096, 4096).transpose_a == 1
-    assert plan(2048, 2048, 2048).transpose_a == 0        # under two waves of tiles
+    assert plan(2048, 2048, 2048).transpose_a == 1        # 256 tiles, at least one per SM
+    assert plan(1024, 2304, 768).transpose_a == 0         # 144 tiles, under one per SM
+    assert plan(1024, 1024, 16384).transpose_a == 1       # split-K with long K
     assert plan(8192, 8192, 64).transpose_a == 0         # K too short to pay for the pass
-    assert plan(1024, 1024, 1024).transpose_a == 0        # split-K plan
+    assert plan(1024, 1024, 1024).transpose_a == 0        # split-K plan, short K
     assert plan(4096, 512, 4096).transpose_a == 0         # N < 1024
     assert plan(4096, 4096, 4096, A=4100).transpose_a == 0   # not vector-aligned
     monkeypatch.setenv("SGEMM_FORCE_TRANSPOSE_A", "0")
@@ -189,6 +191,7 @@ def test_plan_misaligned_pointer_disables_vector_loads(lib):
 
 def test_plan_split_k_fills_the_gpu_when_tiles_are_few(lib, monkeypatch):
     monkeypatch.setenv("SGEMM_FORCE_TILE", "128")
+    monkeypatch.setenv("SGEMM_FORCE_TRANSPOSE_A", "0")   # split-K bookkeeping only
     p = plan(1024, 1024, 16384)          # 64 tiles, long K
     assert p.split_k > 1
     assert p.k_per_split % p.bk == 0

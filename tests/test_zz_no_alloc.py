@@ -48,8 +48,20 @@ def test_noalloc_matches_sgemm_on_two_calls(sg, name):
     p = workloads.workload(name)
     A, B, C0 = _device_problem(p)
     stream = torch.cuda.current_stream().cuda_stream
-    plan = sg.gemm_plan(p.M, p.N, p.K, p.lda, p.ldb, p.ldc, A.data_ptr(), B.data_ptr(),
-                        C0.data_ptr())
+    # sgemm_noalloc never plans a transposed copy of A (it would need M x K
+    # floats of scratch), so its split-K scratch is that of the plan without it
+    import os
+    old = os.environ.get("SGEMM_FORCE_TRANSPOSE_A")
+    os.environ["SGEMM_FORCE_TRANSPOSE_A"] = "0"
+    try:
+        plan = sg.gemm_plan(p.M, p.N, p.K, p.lda, p.ldb, p.ldc, A.data_ptr(), B.data_ptr(),
+                            C0.data_ptr())
+    finally:
+        if old is None:
+            del os.environ["SGEMM_FORCE_TRANSPOSE_A"]
+        else:
+            os.environ["SGEMM_FORCE_TRANSPOSE_A"] = old
+    assert plan.transpose_a == 0
     assert plan.workspace_bytes <= sg.NOALLOC_SCRATCH_BYTES
 
     C_ref = C0.clone()
