@@ -341,8 +341,10 @@ def run_ours(args):
         roofline["frac_at_measured_clock"] = round(achieved / peak_at_clock, 4)
 
     probe = None
-    if args.probe:
+    if not args.no_probe:
         probe = ffma_probe(sg, device, sms)
+        roofline["probe_tflops"] = probe["scalar"]
+        roofline["frac_vs_probe"] = round(achieved / probe["scalar"], 4)
 
     tc = None
     if not args.no_tf32x3:
@@ -352,7 +354,8 @@ def run_ours(args):
     per_config = None
     if not args.no_extras and rank == 0:
         extras = run_extras(sg, device, stream)
-        per_config = run_configs(sg, device, stream)
+        per_config = run_configs(sg, device, stream, peak,
+                                 probe["scalar"] if probe else None)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -368,7 +371,7 @@ def run_ours(args):
             "config": {"workload": describe(p), "M": p.M, "N": p.N, "K": p.K,
                        "l2": f"inputs larger than L2 ({(p.A.nbytes + p.B.nbytes) >> 20} MiB of "
                              f"A+B > 129 MB L2); no flush between steps",
-                       "plan": {k: v for k, v in plan.as_dict().items() if k != "reserved"},
+                       "plan": plan.as_dict(),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "e2e": e2e, "gpu_launches": args.steps * launches_per_gemm,
             "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks,
@@ -602,13 +605,48 @@ def run_extras(sg, device, stream):
     return out
 
 
-def run_configs(sg, device, stream):
-    """TFLOP/s of sgemm and sgemm_tf32x3 on every configured workload (inputs
+def hbm_peak_gbs() -> tuple[float, str]:
+    """Measured HBM copy bandwidth (MEASURED_PEAKS.json), else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "MEASURED_PEAKS.json hbm_gbs"
+    except (OSError, ValueError, KeyError):
+        return 6800.0, "fallback 6.8 TB/s"
+
+
+def algorithmic_bytes(p: workloads.Problem) -> int:
+    """Minimum HBM traffic of one GEMM: read A and B once, write C once, and
+    read C once more when beta != 0."""
+    return 4 * (p.M * p.K + p.K * p.N + p.M * p.N * (2 if p.beta != 0 else 1))
+
+
+def roofline_entry(flops: float, nbytes: float, seconds: float, peak_tflops: float,
+                   hbm_gbs: float) -> dict:
+    """Roofline of one timed call: the bound is the slower of the compute peak
+    and HBM bandwidth for the call's algorithmic bytes; frac = that time over
+    the measured time."""
+    t_alu = flops / (peak_tflops * 1e12)
+    t_hbm = nbytes / (hbm_gbs * 1e9)
+    return {"bound": "hbm" if t_hbm > t_alu else "alu",
+            "frac": round(max(t_alu, t_hbm) / seconds, 4),
+            "hbm_gbs": round(nbytes / seconds / 1e9, 1)}
+
+
+def run_configs(sg, device, stream, peak_tflops: float, probe_tflops: float | None):
+    """Every configured workload: TFLOP/s of sgemm and sgemm_tf32x3 (inputs
     resident, CUDA events, median; workloads under 200 MB get the L2 flushed
-    between repetitions), and of the CPU oracle on a sample of its rows."""
+    between repetitions) with each one's roofline fraction, and the CPU oracle
+    on a sample of the workload's rows.
+
+    FFMA roofline: the slower of the fp32 FMA peak (`peak_tflops`) and HBM
+    bandwidth for the algorithmic bytes.  Tensor mode: the tf32 tensor peak
+    over the three products it computes (2MNK of effective work per 3*2MNK of
+    tf32 work), or HBM, whichever is slower."""
     import torch
     sh = stream.cuda_stream
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    bw, _ = hbm_peak_gbs()
+    tf32_peak, _ = tf32_peak_tflops()
     out = {}
     for name in workloads.WORKLOADS:
         p = workloads.workload(name)
@@ -616,7 +654,10 @@ def run_configs(sg, device, stream):
         B = torch.from_numpy(p.B).to(device)
         C = torch.from_numpy(p.C0).to(device)
         small = p.A.nbytes + p.B.nbytes + p.C0.nbytes < 200 << 20
-        res = {}
+        nbytes = algorithmic_bytes(p)
+        res = {"shape": f"{p.M}x{p.N}x{p.K}", "alpha": p.alpha, "beta": p.beta,
+               "algorithmic_flops": int(p.flops), "algorithmic_bytes": int(nbytes),
+               "flop_per_byte": round(p.flops / nbytes, 1)}
         for mode, fn in (("ffma", sg.sgemm_ptr), ("tf32x3", sg.sgemm_tf32x3_ptr)):
             def call():
                 fn(p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
@@ -637,13 +678,24 @@ def run_configs(sg, device, stream):
                 torch.cuda.synchronize(device)
                 ts.append(e0.elapsed_time(e1) / 1e3)
             ts.sort()
-            res[mode] = round(p.flops / ts[len(ts) // 2] / 1e12, 3)
+            med = ts[len(ts) // 2]
+            res[mode] = round(p.flops / med / 1e12, 3)
+            res[f"{mode}_ms"] = round(med * 1e3, 4)
+            if mode == "ffma":
+                r = roofline_entry(p.flops, nbytes, med, peak_tflops, bw)
+                res.update(r)
+                if probe_tflops:
+                    t_probe = max(p.flops / (probe_tflops * 1e12), nbytes / (bw * 1e9))
+                    res["frac_vs_probe"] = round(t_probe / med, 4)
+            else:
+                r = roofline_entry(p.flops, nbytes, med, tf32_peak / 3.0, bw)
+                res["tf32x3_bound"] = "hbm" if r["bound"] == "hbm" else "tensor"
+                res["tf32x3_frac"] = r["frac"]
         # the CPU oracle on a bounded sample of rows of the same problem
         rows = min(p.M, max(16, int(2e10 / max(2.0 * p.N * p.K, 1.0))))
         dt, oflops, threads = oracle_rows_rate(p, rows, seed=3)
         res["oracle"] = round(oflops / dt / 1e12, 5)
         res["oracle_sample"] = f"{rows} of {p.M} rows, {threads} threads"
-        res["shape"] = f"{p.M}x{p.N}x{p.K}"
         res["l2_flushed"] = small
         out[name] = res
         del A, B, C
@@ -724,7 +776,8 @@ def parse(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
-    ap.add_argument("--probe", action="store_true", help="also time the fp32 FMA probe")
+    ap.add_argument("--no-probe", action="store_true",
+                    help="skip the fp32 FMA probe (the attainable FMA rate)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the batched / transposed / fused-epilogue sgemm_ex cases")
     ap.add_argument("--no-tf32x3", action="store_true",

@@ -53,7 +53,25 @@ EXPORTED_SYMBOLS = (
     "sgemm_tf32x3_packed_b_bytes",
     "sgemm_tf32x3_pack_b",
     "sgemm_tf32x3_packed",
+    "sgemm_set_tuning",
+    "sgemm_get_tuning",
 )
+# sgemm_tuning_knob
+TUNING_KNOBS = {
+    "split_k": 0,
+    "tail_split": 1,
+    "tile": 2,
+    "kernel": 3,
+    "transpose_a": 4,
+    "ffma_ext": 5,
+    "tf32x3_split": 6,
+    "tf32x3_tail": 7,
+    "tf32x3_fuse_a": 8,
+    "workspace_limit_mib": 9,
+    "schedule": 10,
+    "sk_min_slices": 11,
+    "sk_grid": 12,
+}
 OP_N, OP_T = 0, 1
 ACT_NONE, ACT_GELU_TANH = 0, 1
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -93,8 +111,11 @@ class GemmPlan(ctypes.Structure):
         ("tail_start", ctypes.c_int64),
         ("tail_k_per_split", ctypes.c_int64),
         ("transpose_a", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("stages", ctypes.c_int32),
         ("a_t_ld", ctypes.c_int64),
+        ("schedule", ctypes.c_int32),
+        ("dp_rounds", ctypes.c_int32),
+        ("sk_iters", ctypes.c_int64),
     ]
 
     def as_dict(self) -> dict:
@@ -165,6 +186,10 @@ def load_library() -> ctypes.CDLL:
         lib.sgemm_tf32x3_stall_selftest.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp,
                                                     _i64, _i64, _vp]
         lib.sgemm_tf32x3_stall_selftest.restype = ctypes.c_int
+        lib.sgemm_set_tuning.argtypes = [ctypes.c_int32, ctypes.c_int32]
+        lib.sgemm_set_tuning.restype = ctypes.c_int
+        lib.sgemm_get_tuning.argtypes = [ctypes.c_int32]
+        lib.sgemm_get_tuning.restype = ctypes.c_int32
         _lib = lib
         return lib
 
@@ -292,6 +317,41 @@ def ffma_probe(ctas: int, iters: int, out_ptr: int, packed: bool = True, stream:
     """sgemm_ffma_probe(): FLOPs = ctas * 256 * iters * 128."""
     _check(load_library().sgemm_ffma_probe(ctas, iters, 1 if packed else 0, out_ptr or None,
                                            stream or None), "sgemm_ffma_probe")
+
+
+def set_tuning(knob: str, value: int | None) -> None:
+    """sgemm_set_tuning(): override one planner choice (None = the planner's)."""
+    _check(load_library().sgemm_set_tuning(TUNING_KNOBS[knob], -1 if value is None else value),
+           f"sgemm_set_tuning({knob})")
+
+
+def get_tuning(knob: str) -> int | None:
+    """sgemm_get_tuning(): the knob's override, or None when the planner decides."""
+    v = int(load_library().sgemm_get_tuning(TUNING_KNOBS[knob]))
+    return None if v == -1 else v
+
+
+class tuning:
+    """Context manager: ``with tuning(split_k=4, tile=128): ...`` sets knobs
+    for the duration of the block and restores their previous values."""
+
+    def __init__(self, **knobs: int | None):
+        for k in knobs:
+            if k not in TUNING_KNOBS:
+                raise KeyError(f"unknown tuning knob {k!r}")
+        self.knobs = knobs
+        self.saved: dict[str, int | None] = {}
+
+    def __enter__(self):
+        for k, v in self.knobs.items():
+            self.saved[k] = get_tuning(k)
+            set_tuning(k, v)
+        return self
+
+    def __exit__(self, *exc):
+        for k, v in self.saved.items():
+            set_tuning(k, v)
+        return False
 
 
 # --------------------------------------------------------------------------

@@ -4,7 +4,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <cstdlib>
 
 #include "ffma_kernel.cuh"
 #include "sgemm_internal.h"
@@ -156,10 +155,11 @@ cudaError_t launch_ffma(const GemmArgs &a, int kernel, int tile, bool vec, bool 
     // split-K (8192^3: 60.8 against 60.0 TFLOP/s) and for bounds-checked
     // vector split-K (1024x1024x16384: 47.0 against 45.4); the plain build
     // for full-tile split-K (GPT-2 QKV 41.8 against 39.9, 1024^3 31.5
-    // against 29.7).  SGEMM_FFMA_EXT=0/1 overrides the choice for sweeps.
+    // against 29.7).  The tuning knob kKnobFfmaExt (0/1) overrides the
+    // choice for sweeps.
     const bool split = a.split_k > 1 || a.tail_split > 1;
     bool pick_ext = (!edge && !split) || (edge && vec && split);
-    if (const char *force = std::getenv("SGEMM_FFMA_EXT")) pick_ext = std::atoi(force) != 0;
+    if (const int force = tuning(kKnobFfmaExt); force >= 0) pick_ext = force != 0;
     if (ext || (kernel != kKernelFfma2x128 && pick_ext))
         return ffma::launch_layout<128, false, false, false, true>(a, vec, edge, stream);
     return kernel == kKernelFfma2x128

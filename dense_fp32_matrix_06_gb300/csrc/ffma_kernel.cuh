@@ -505,21 +505,32 @@ ffma_gemm_kernel(const GemmArgs p) {
             // every partial, this CTA's own included, is read back from the
             // workspace (each thread reads only what it wrote itself or what
             // the fence and ticket made visible), so the sum order is the
-            // same whichever CTA arrives last
+            // same whichever CTA arrives last.  Half a tile at a time with a
+            // partial's eight loads in flight together: 2S L2 round trips
+            // rather than 16S.
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int i = j >> 1, h = j & 1;
-                float4 tot = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                for (int s = 0; s < S; ++s) {
-                    const float4 v =
-                        __ldcg(part + tile_base + size_t(s) * 16 * NT + j * NT + tid);
-                    tot.x += v.x;
-                    tot.y += v.y;
-                    tot.z += v.z;
-                    tot.w += v.w;
+            for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                for (int j = 8 * half; j < 8 * half + 8; ++j) {
+                    const int i = j >> 1, h = j & 1;
+                    acc[i][2 * h] = make_float2(0.0f, 0.0f);
+                    acc[i][2 * h + 1] = make_float2(0.0f, 0.0f);
                 }
-                acc[i][2 * h] = make_float2(tot.x, tot.y);
-                acc[i][2 * h + 1] = make_float2(tot.z, tot.w);
+                for (int s = 0; s < S; ++s) {
+                    float4 v[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        v[j] = __ldcg(part + tile_base + size_t(s) * 16 * NT +
+                                      (8 * half + j) * NT + tid);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int i = (8 * half + j) >> 1, h = j & 1;
+                        acc[i][2 * h].x += v[j].x;
+                        acc[i][2 * h].y += v[j].y;
+                        acc[i][2 * h + 1].x += v[j].z;
+                        acc[i][2 * h + 1].y += v[j].w;
+                    }
+                }
             }
             if (tid == 0) *counter = 0u;
         }

@@ -10,7 +10,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <cstdlib>
 #include <algorithm>
 #include <cstring>
 #include <mutex>
@@ -90,10 +89,9 @@ int choose_split(int64_t tiles, int64_t K, int sms, int64_t *k_per_split, int bk
     const int64_t kslices = ceil_div(K, bk);
     int best = 1;
     int64_t best_kps = kslices * bk;
-    if (const char *force = std::getenv("SGEMM_FORCE_SPLIT")) {
-        int s = std::atoi(force);
+    {
+        const int s = tuning(kKnobSplit);
         if (s >= 1) {
-            if (s > kMaxSplit) s = kMaxSplit;
             int64_t kps = ceil_div(kslices, s) * bk;
             int eff = int(ceil_div(K, kps > 0 ? kps : 1));
             if (eff < 1) eff = 1;
@@ -130,7 +128,7 @@ int choose_split(int64_t tiles, int64_t K, int sms, int64_t *k_per_split, int bk
     return best;
 }
 
-// Tail split (opt-in, SGEMM_FORCE_TAIL=s with s >= 2): cut only the tiles of
+// Tail split (opt-in, tuning knob kKnobTail = s with s >= 2): cut only the tiles of
 // the last, partly filled wave of resident CTAs into s K ranges.  Off by
 // default: measured on GB300 it gains nothing (8192^3: 59.26 TFLOP/s either
 // way; 4096^3: 56.35 with, 56.93 without), because with two CTAs per SM a
@@ -143,8 +141,7 @@ void choose_tail(int64_t tiles, int64_t K, int sms, int64_t *tail_start, int *ta
     *tail_start = tiles;
     *tail_split = 1;
     *tail_kps = kslices * kBK;
-    const char *force = std::getenv("SGEMM_FORCE_TAIL");
-    const int want = force ? std::atoi(force) : 0;
+    const int want = tuning(kKnobTail);
     if (want < 2 || tiles < slots) return;
     const int64_t rem = tiles % slots;
     if (rem == 0 || rem > kMaxSplitTiles) return;
@@ -170,10 +167,10 @@ size_t split_workspace(int64_t tiles, int split_k, int64_t tail_start, int tail_
 // for it; 128 otherwise.  Measured on GB300 (TFLOP/s, 64 against 128): 256^3
 // 1.33 / 1.14, 1023x777x513 17.8 / 15.7, but 1024^3 28.9 / 31.5,
 // 1024x768x3072 37.8 / 41.9, 1024x1024x16384 40.6 / 47.0.
-// SGEMM_FORCE_TILE=64/128 overrides the choice for sweeps.
+// The tuning knob kKnobTile (64/128) overrides the choice for sweeps.
 int choose_tile(int64_t M, int64_t N, int64_t K, int64_t batch, int sms) {
-    if (const char *force = std::getenv("SGEMM_FORCE_TILE")) {
-        const int t = std::atoi(force);
+    {
+        const int t = tuning(kKnobTile);
         if (t == 64 || t == 128) return t;
     }
     const int64_t per_batch = ceil_div(M, 128) * ceil_div(N, 128);
@@ -183,21 +180,86 @@ int choose_tile(int64_t M, int64_t N, int64_t K, int64_t batch, int sms) {
     return 128;
 }
 
-// Kernel the planner names: the scalar-FMA kernel unless SGEMM_FORCE_KERNEL
-// (0 = scalar, 1 = packed) asks otherwise; the override exists for sweeps.
+// Kernel the planner names: the scalar-FMA kernel unless the tuning knob
+// kKnobKernel (0 = scalar, 1 = packed) asks otherwise; it exists for sweeps.
 // Measured on GB300 at 8192^3: scalar 59.0 TFLOP/s, packed 54.0 (a packed FMA
 // holds the FMA pipe for two cycles, so it saves issue slots but not pipe
 // time, and its broadcast operand pairs push the kernel past 128 registers).
 int32_t default_kernel() {
-    if (const char *force = std::getenv("SGEMM_FORCE_KERNEL")) {
-        const int k = std::atoi(force);
-        if (k == kKernelFfma128 || k == kKernelFfma2x128) return k;
-    }
+    const int k = tuning(kKnobKernel);
+    if (k == kKernelFfma128 || k == kKernelFfma2x128) return k;
     return kKernelFfma128;
 }
 
+// ---- persistent stream-K schedule ----
+constexpr int kSkMinSlicesDefault = 8; // fewest K slices in one CTA's run
+constexpr int64_t kSkMaxK = int64_t(1) << 30;   // the kernel counts K in 32-bit integers
+
+int64_t sk_slots(int tile, int sms) {
+    return int64_t(sms) * (tile == kSmallTile ? kSmallCtasPerSm : kCtasPerSm);
+}
+
+// Turns plan `p` (tile, tiles_m, tiles_n already set) into a stream-K plan
+// for `tiles` tiles of ceil(K / bk) slices on `sms` SMs.  With two waves of
+// tiles or more, whole-K tiles go round-robin to every resident CTA until
+// at most two waves' worth are left (all of them when the tiles fill whole
+// waves); the K slices of what is left, or of every tile of a smaller grid,
+// are split into G equal runs, G being the resident CTA count, or fewer so
+// that a run keeps at least kKnobSkMinSlices slices and a tile is shared by
+// at most kSkMaxContrib runs.
+void plan_stream_k(gemm_plan_t &p, int64_t tiles, int64_t K, int sms, bool direct) {
+    const int tile = p.bm;
+    const int bk = sk_config_bk(tile, direct);
+    const int64_t kt = ceil_div(K, bk);
+    const int64_t S = sk_slots(tile, sms);
+    int64_t dp_rounds = 0, sk_tiles = tiles, G = S;
+    if (tiles >= 2 * S) {
+        dp_rounds = tiles / S - (tiles % S ? 1 : 0);
+        sk_tiles = tiles - dp_rounds * S;
+    } else {
+        const int32_t knob = tuning(kKnobSkMinSlices);
+        const int64_t min_sl = knob > 0 ? knob : kSkMinSlicesDefault;
+        G = std::min<int64_t>(S, std::max<int64_t>(1, tiles * kt / min_sl));
+        G = std::min<int64_t>(G, tiles * kSkMaxContrib);
+        if (const int32_t force = tuning(kKnobSkGrid); force > 0)
+            G = std::min<int64_t>({int64_t(force), tiles * kt, tiles * kSkMaxContrib});
+    }
+    p.schedule = 1;
+    p.dp_rounds = int32_t(dp_rounds);
+    p.sk_iters = sk_tiles * kt;
+    p.grid_ctas = G;
+    p.bk = bk;
+    p.stages = sk_config_pages(tile, direct);
+    p.split_k = 1;
+    p.tail_split = 1;
+    p.tail_start = tiles;
+    p.k_per_split = kt * bk;
+    p.tail_k_per_split = p.k_per_split;
+    p.edge = 1;   // every tile is bounds-checked (the checks cost a few instructions a slice)
+    p.workspace_bytes =
+        p.sk_iters > 0 ? kCounterBytes + size_t(2 * G) * tile * tile * sizeof(float) : 0;
+}
+
+// Persistent stream-K or one CTA per (tile, K range).  Measured on GB300
+// (microseconds, L2 flushed, stream-K / split-K planned as above): the
+// stream-K kernel wins where the grid is far from a whole wave and the K
+// ranges are long or the problem tiny -- 256^3 on 64-wide tiles 17.1 / 19.2,
+// 1024x1024x16384 (64 tiles of 128) 672 / 709 -- and loses where split-K
+// already balances the GPU (1024^3 78.5 / 66.2, 1023x777x513 49.8 / 41.6,
+// GPT-2 QKV 90.9 / 82.6, 2048^3 344.7 / 338.6): its main loop issues more
+// instructions and stalls more in dispatch than the split-K kernel's, which
+// eats what the even split gains.  The tuning knob kKnobSchedule overrides.
+bool choose_stream_k(int tile, int64_t tiles, int64_t K, int sms) {
+    const int32_t force = tuning(kKnobSchedule);
+    if (force == 0 || force == 1) return force == 1;
+    if (tile == kSmallTile) return 4 * tiles < sms;
+    return 2 * tiles <= sms && K >= 8192;
+}
+
+// `direct`: both operands reach the kernel by direct copies (op(A) = A^T and
+// op(B) = B), which lets a stream-K plan take the longer K slice.
 void plan_core(int64_t M, int64_t N, int64_t K, int64_t batch, bool vec, int sms,
-               gemm_plan_t *out) {
+               gemm_plan_t *out, bool direct = false) {
     gemm_plan_t p;
     std::memset(&p, 0, sizeof(p));
     const int tile = choose_tile(M, N, K, batch, sms);
@@ -209,6 +271,7 @@ void plan_core(int64_t M, int64_t N, int64_t K, int64_t batch, bool vec, int sms
     p.bn = tile;
     p.bk = bk;
     p.threads = (tile / 8) * (tile / 8);
+    p.stages = 2;
     p.vec = vec ? 1 : 0;
     p.tiles_m = ceil_div(M, tile);
     p.tiles_n = ceil_div(N, tile);
@@ -231,6 +294,9 @@ void plan_core(int64_t M, int64_t N, int64_t K, int64_t batch, bool vec, int sms
     p.edge = (p.vec && full) ? 0 : 1;
     p.grid_ctas = p.tail_start * p.split_k + (tiles - p.tail_start) * p.tail_split;
     p.workspace_bytes = split_workspace(tiles, p.split_k, p.tail_start, p.tail_split, tile);
+    if (M > 0 && N > 0 && K > 0 && batch > 0 && K <= kSkMaxK &&
+        choose_stream_k(tile, tiles, K, sms))
+        plan_stream_k(p, tiles, K, sms, direct);
     *out = p;
 }
 
@@ -247,18 +313,17 @@ void plan_core(int64_t M, int64_t N, int64_t K, int64_t batch, bool vec, int sms
 // 29.3, MLP-up 39.8 / 38.2).  Hence: N >= 1024, K >= 256, and either no
 // split with at least one tile per SM, or split-K with K >= 8192.  The copy
 // lives in the workspace after the counters and any split-K partials.
-// SGEMM_FORCE_TRANSPOSE_A=0/1 overrides the choice for sweeps.
+// The tuning knob kKnobTransposeA (0/1) overrides the choice for sweeps.
 bool choose_transpose_a(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int sms) {
     const bool able = p.bm == 128 && p.tail_split == 1 && p.vec && K >= 1 &&
                       M <= int64_t(65535) * 32;
     const int64_t tiles = p.tiles_m * p.tiles_n;
+    const bool k_split = p.split_k > 1 || p.schedule == 1;
     bool want = able && N >= 1024 && K >= 256 &&
-                ((p.split_k == 1 && tiles >= sms) || (p.split_k > 1 && K >= 8192));
-    if (const char *force = std::getenv("SGEMM_FORCE_TRANSPOSE_A")) {
-        const int f = std::atoi(force);
-        if (f == 0) want = false;
-        if (f == 1) want = able;
-    }
+                ((!k_split && tiles >= sms) || (k_split && K >= 8192));
+    const int f = tuning(kKnobTransposeA);
+    if (f == 0) want = false;
+    if (f == 1) want = able;
     return want;
 }
 
@@ -271,8 +336,10 @@ size_t transpose_bytes(int64_t M, int64_t K, int64_t *ld) {
 size_t transpose_workspace(const gemm_plan_t &p, int64_t M, int64_t K, int64_t *ld,
                            size_t *at_offset) {
     const int64_t tiles = p.tiles_m * p.tiles_n;
-    const size_t parts =
-        p.split_k > 1 ? size_t(tiles) * p.split_k * size_t(p.bm) * p.bm * sizeof(float) : 0;
+    const size_t tile_bytes = size_t(p.bm) * p.bm * sizeof(float);
+    const size_t parts = p.schedule == 1 ? (p.sk_iters > 0 ? size_t(2 * p.grid_ctas) * tile_bytes : 0)
+                         : p.split_k > 1 ? size_t(tiles) * p.split_k * tile_bytes
+                                         : 0;
     *at_offset = kCounterBytes + parts;
     return *at_offset + transpose_bytes(M, K, ld);
 }
@@ -287,7 +354,14 @@ sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb
         // the product then runs with both operands copied by rows, in K slices of 32
         gemm_plan_t &q = *out;
         q.transpose_a = 1;
+        if (q.schedule == 1) {
+            plan_stream_k(q, q.tiles_m * q.tiles_n, K, sms, true);
+            size_t at_offset = 0;
+            q.workspace_bytes = transpose_workspace(q, M, K, &q.a_t_ld, &at_offset);
+            return SGEMM_OK;
+        }
         q.bk = kWideBK;
+        q.stages = 3;
         const int64_t tiles = q.tiles_m * q.tiles_n;
         int64_t kps = 0;
         q.split_k = choose_split(tiles, K, sms, &kps, kWideBK, kCtasPerSm);
@@ -324,11 +398,21 @@ sgemm_status library_workspace(int dev, cudaStream_t stream, size_t bytes, void 
         *out = w->ptr;
         return SGEMM_OK;
     }
+    // An optional cap (tuning knob kKnobWorkspaceLimitMiB) bounds what the
+    // library may hold per (device, stream); a request above it fails as an
+    // allocation failure would.
+    const int32_t cap = tuning(kKnobWorkspaceLimitMiB);
+    const size_t limit = cap >= 0 ? size_t(cap) << 20 : SIZE_MAX;
+    if (bytes > limit) return cuda_fail(cudaErrorMemoryAllocation, SGEMM_ERR_ALLOC);
     size_t want = bytes + bytes / 4;
     want = (want + 0xFFFFF) & ~size_t(0xFFFFF);
+    if (want > limit) want = bytes;
     void *p = nullptr;
     cudaError_t e = cudaMallocAsync(&p, want, stream);
-    if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_ALLOC);
+    if (e != cudaSuccess) {
+        cudaGetLastError();   // a later launch check must not see this error
+        return cuda_fail(e, SGEMM_ERR_ALLOC);
+    }
     e = cudaMemsetAsync(p, 0, kCounterBytes, stream);
     if (e != cudaSuccess) {
         cudaFreeAsync(p, stream);
@@ -343,6 +427,42 @@ sgemm_status library_workspace(int dev, cudaStream_t stream, size_t bytes, void 
     }
     *out = p;
     return SGEMM_OK;
+}
+
+// Launch arguments of a stream-K plan, from the operand fields of `a`.
+SkArgs sk_args(const gemm_plan_t &plan, const GemmArgs &a, void *workspace) {
+    SkArgs k;
+    k.A = a.A;
+    k.B = a.B;
+    k.C = a.C;
+    k.M = a.M;
+    k.N = a.N;
+    k.K = a.K;
+    k.lda = a.lda;
+    k.ldb = a.ldb;
+    k.ldc = a.ldc;
+    k.alpha = a.alpha;
+    k.beta = a.beta;
+    k.batch = a.batch;
+    k.strideA = a.strideA;
+    k.strideB = a.strideB;
+    k.strideC = a.strideC;
+    k.bias = a.bias;
+    k.act = a.act;
+    k.tiles_m = int32_t(plan.tiles_m);
+    k.tiles_n = int32_t(plan.tiles_n);
+    k.kt = int32_t(ceil_div(a.K, plan.bk));
+    k.dp_rounds = plan.dp_rounds;
+    k.grid = int32_t(plan.grid_ctas);
+    k.tiles = plan.tiles_m * plan.tiles_n * a.batch;
+    k.sk_iters = plan.sk_iters;
+    k.counters = nullptr;
+    k.partials = nullptr;
+    if (plan.sk_iters > 0) {
+        k.counters = static_cast<unsigned *>(workspace);
+        k.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + kCounterBytes);
+    }
+    return k;
 }
 
 sgemm_status run(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K, float alpha,
@@ -394,7 +514,17 @@ sgemm_status run(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K, float
         if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
         a.A = at;
         a.lda = plan.a_t_ld;
-        e = launch_ffma_tn_wide(a, plan.vec != 0, plan.edge != 0, stream);
+        if (plan.schedule == 1)
+            e = launch_ffma_sk(sk_args(plan, a, workspace), plan.bm, plan.bk, plan.stages,
+                               plan.vec != 0, true, false, false, stream);
+        else
+            e = launch_ffma_tn_wide(a, plan.vec != 0, plan.edge != 0, stream);
+        return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
+    }
+    if (plan.schedule == 1) {
+        const SkArgs k = sk_args(plan, a, workspace);
+        e = launch_ffma_sk(k, plan.bm, plan.bk, plan.stages, plan.vec != 0, false, false, false,
+                           stream);
         return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
     }
     e = launch_ffma(a, plan.kernel, plan.bm, plan.vec != 0, plan.edge != 0, false, false, stream);
@@ -408,10 +538,48 @@ bool plan_matches(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int64_t
     const int t = p.bm;
     if ((t != 128 && t != kSmallTile) || p.bn != t || p.threads != (t / 8) * (t / 8))
         return false;
-    if (p.bk != (p.transpose_a ? kWideBK : t / 8)) return false;
     if (t == kSmallTile && p.kernel != kKernelFfma128) return false;
     if (p.tiles_m != ceil_div(M, t) || p.tiles_n != ceil_div(N, t)) return false;
     const int64_t tiles = p.tiles_m * p.tiles_n;
+    if (p.schedule != 0 && p.schedule != 1) return false;
+    if (p.schedule == 1) {
+        // stream-K: whole-K rounds, then every run non-empty, every tile
+        // shared by few enough runs, counters and partials inside the workspace
+        const bool direct = p.transpose_a != 0;
+        if (p.bk != sk_config_bk(t, direct) || p.stages != sk_config_pages(t, direct) ||
+            p.edge != 1)
+            return false;
+        if (p.split_k != 1 || p.tail_split != 1 || p.tail_start != tiles) return false;
+        if (K <= 0) return p.sk_iters == 0 && p.dp_rounds == 0;
+        if (K > kSkMaxK) return false;
+        const int64_t kt = ceil_div(K, p.bk);
+        if (p.k_per_split != kt * p.bk || p.tail_k_per_split != p.k_per_split) return false;
+        const int64_t G = p.grid_ctas;
+        if (G < 1 || G > INT32_MAX || p.dp_rounds < 0) return false;
+        const int64_t dp_tiles = int64_t(p.dp_rounds) * G;
+        if (dp_tiles > tiles) return false;
+        const int64_t sk_tiles = tiles - dp_tiles;
+        if (p.sk_iters != sk_tiles * kt) return false;
+        if (sk_tiles > 0 && (G > p.sk_iters || sk_tiles > kMaxSplitTiles ||
+                             G > sk_tiles * kSkMaxContrib))
+            return false;
+        if (p.vec && !(lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0 && aligned16(A) &&
+                       aligned16(B) && aligned16(C)))
+            return false;
+        if (p.transpose_a) {
+            if (t != 128 || !p.vec || M > int64_t(65535) * 32) return false;
+            int64_t ld = 0;
+            size_t at_offset = 0;
+            const size_t need = transpose_workspace(p, M, K, &ld, &at_offset);
+            return p.a_t_ld == ld && p.workspace_bytes == need;
+        }
+        const size_t need =
+            p.sk_iters > 0 ? kCounterBytes + size_t(2 * G) * t * t * sizeof(float) : 0;
+        return p.workspace_bytes == need;
+    }
+    if (p.dp_rounds != 0 || p.sk_iters != 0) return false;
+    if (p.bk != (p.transpose_a ? kWideBK : t / 8)) return false;
+    if (p.stages != (p.transpose_a ? 3 : 2)) return false;
     if (p.split_k < 1 || p.split_k > kMaxSplit) return false;
     if (p.tail_split < 1 || p.tail_split > kMaxSplit) return false;
     if (p.tail_start < 0 || p.tail_start > tiles) return false;
@@ -487,7 +655,19 @@ sgemm_status sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
     void *ws = nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (plan.workspace_bytes > 0 && K > 0 && alpha != 0.0f) {
+        const int last_error = g_last_cuda_error;
         s = library_workspace(dev, st, plan.workspace_bytes, &ws);
+        if (s == SGEMM_ERR_ALLOC && plan.transpose_a) {
+            // The transposed copy of A only makes the product faster; without
+            // room for it, run the plan that reads A as stored (split-K
+            // partials at most).
+            s = plan_impl(M, N, K, lda, ldb, ldc, A, B, C, sms, &plan, false);
+            if (s != SGEMM_OK) return s;
+            ws = nullptr;
+            s = plan.workspace_bytes > 0 ? library_workspace(dev, st, plan.workspace_bytes, &ws)
+                                         : SGEMM_OK;
+            if (s == SGEMM_OK) g_last_cuda_error = last_error;
+        }
         if (s != SGEMM_OK) return s;
     }
     return run(plan, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, ws, st);
@@ -598,8 +778,11 @@ extern "C" sgemm_status sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alp
         if (s != SGEMM_OK) return s;
         // The buffer keeps whatever the previous call left; the tile counters
         // must start at zero, so clear the ones this launch uses.
-        const int64_t split_tiles = plan.split_k > 1 ? plan.tiles_m * plan.tiles_n
-                                                     : plan.tiles_m * plan.tiles_n - plan.tail_start;
+        const int64_t tiles = plan.tiles_m * plan.tiles_n;
+        const int64_t split_tiles =
+            plan.schedule == 1 ? tiles - int64_t(plan.dp_rounds) * plan.grid_ctas
+            : plan.split_k > 1 ? tiles
+                               : tiles - plan.tail_start;
         const size_t counter_bytes = size_t(split_tiles) * sizeof(unsigned);
         const cudaError_t e = cudaMemsetAsync(ws, 0, counter_bytes, st);
         if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
@@ -715,7 +898,7 @@ extern "C" sgemm_status sgemm_ex(int32_t op_a, int32_t op_b, int64_t M, int64_t 
                      stride_b % 4 == 0 && stride_c % 4 == 0 && aligned16(A) && aligned16(B) &&
                      aligned16(C) && aligned16(bias);
     gemm_plan_t plan;
-    plan_core(M, N, K, batch, vec, sms, &plan);
+    plan_core(M, N, K, batch, vec, sms, &plan, ta && !tb);
     if (ta || tb) plan.kernel = kKernelFfma128;   // the packed form exists for op N, N only
     void *ws = nullptr;
     if (plan.workspace_bytes > 0) {
@@ -754,6 +937,12 @@ extern "C" sgemm_status sgemm_ex(int32_t op_a, int32_t op_b, int64_t M, int64_t 
     if (plan.workspace_bytes > 0) {
         a.counters = static_cast<unsigned *>(ws);
         a.partials = reinterpret_cast<float *>(static_cast<char *>(ws) + kCounterBytes);
+    }
+    if (plan.schedule == 1) {
+        const bool ext = batch > 1 || bias != nullptr || act != SGEMM_ACT_NONE;
+        e = launch_ffma_sk(sk_args(plan, a, ws), plan.bm, plan.bk, plan.stages, plan.vec != 0,
+                           ta, tb, ext, st);
+        return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
     }
     e = launch_ffma(a, plan.kernel, plan.bm, plan.vec != 0, plan.edge != 0, ta, tb, st);
     return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);

@@ -32,15 +32,42 @@ constexpr int kMaxSplit = 32;
 // Sets the dynamic shared memory limit of `kernel` on the current device once
 // (per kernel and device; `flags` is the caller's per-kernel table).  Setting
 // it twice from racing threads is harmless.
-inline cudaError_t set_smem_once(const void *kernel, int bytes, bool (&flags)[64]) {
+// With `max_carveout` the kernel also asks for the largest shared-memory
+// carveout, so that the CTAs a persistent grid counts on fit on every SM.
+inline cudaError_t set_smem_once(const void *kernel, int bytes, bool (&flags)[64],
+                                 bool max_carveout = false) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64 && flags[dev]) return cudaSuccess;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && max_carveout)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 int(cudaSharedmemCarveoutMaxShared));
     if (e == cudaSuccess && dev >= 0 && dev < 64) flags[dev] = true;
     return e;
 }
+
+// Planner and dispatch overrides (tuning.cu; C ABI sgemm_set_tuning).  Each
+// knob starts from an environment variable read once at library load; -1
+// means the planner decides.  The order matches sgemm_tuning_knob.
+enum Knob : int32_t {
+    kKnobSplit = 0,          // split-K ranges of every tile (1..kMaxSplit)
+    kKnobTail = 1,           // K ranges of the last partial wave (0/1 off, 2..)
+    kKnobTile = 2,           // CTA tile 64 or 128
+    kKnobKernel = 3,         // 0 scalar FMA issue, 1 packed f32x2
+    kKnobTransposeA = 4,     // 0/1: transposed copy of A first
+    kKnobFfmaExt = 5,        // 0/1: plain or extended instantiation for plain products
+    kKnobTf32x3Split = 6,    // tensor mode: K ranges of every tile
+    kKnobTf32x3Tail = 7,     // tensor mode: K ranges of the last partial wave
+    kKnobTf32x3FuseA = 8,    // tensor mode: 0 forces the pre-pass split of A
+    kKnobWorkspaceLimitMiB = 9,  // cap on each library-owned workspace
+    kKnobSchedule = 10,      // 0 one CTA per (tile, K range), 1 persistent stream-K
+    kKnobSkMinSlices = 11,   // stream-K: fewest K slices per CTA run
+    kKnobSkGrid = 12,        // stream-K: resident CTAs (grids of under two waves)
+    kKnobCount = 13
+};
+int32_t tuning(Knob k);
 
 // Epilogue activations.
 constexpr int kActNone = 0;
@@ -86,6 +113,59 @@ enum KernelId : int32_t {
     kKernelFfma128 = 0,    // scalar fma.rn.f32
     kKernelFfma2x128 = 1,  // packed fma.rn.f32x2 (two FMAs per instruction)
 };
+
+// ---- persistent stream-K kernel (ffma_sk_kernel.cuh) ----
+// G = gridDim.x CTAs stay resident and share the work evenly: first
+// `dp_rounds` rounds of whole-K tiles handed out round-robin (tile r*G + g
+// to CTA g), then the K slices of the remaining tiles, cut into G equal
+// contiguous runs over (tile, slice) order.  A tile whose slices several
+// CTAs share is summed in a fixed order by the last of them to finish.
+struct SkArgs {
+    const float *A;
+    const float *B;
+    float *C;
+    int64_t M, N, K;
+    int64_t lda, ldb, ldc;
+    float alpha, beta;
+    int64_t batch;
+    int64_t strideA, strideB, strideC;
+    const float *bias;
+    int32_t act;
+    int32_t tiles_m, tiles_n;
+    int32_t kt;           // K slices per tile
+    int32_t dp_rounds;    // whole-K rounds: tiles [0, dp_rounds * G)
+    int32_t grid;         // G, the CTAs launched (every stream-K run non-empty: G <= sk_iters)
+    int64_t tiles;        // over all batches (batch-major)
+    int64_t sk_iters;     // slices of tiles [dp_rounds * G, tiles), spread over the G CTAs
+    unsigned *counters;   // one per stream-K tile; zero on entry and on exit
+    float *partials;      // 2 * G partial tiles
+};
+constexpr int kSkMaxContrib = 16;   // most CTAs that may share one tile's K slices
+// K slice and ring depth of the stream-K kernel for a tile: both operands
+// copied directly (op(A) = A^T, op(B) = B): K slices of T/4 in three pages;
+// otherwise (an operand staged through a raw page and transposed) K slices
+// of T/8 in four pages.
+constexpr int sk_config_bk(int tile, bool direct) {
+    return tile == 128 && direct ? 32 : tile / 8;
+}
+constexpr int sk_config_pages(int tile, bool direct) {
+    return tile == 128 && direct ? 3 : 4;
+}
+// op(A) = A^T when trans_a, op(B) = B^T when trans_b.
+cudaError_t launch_ffma_sk(const SkArgs &a, int tile, int bk, int pages, bool vec, bool trans_a,
+                           bool trans_b, bool ext, cudaStream_t stream);
+cudaError_t launch_ffma_sk_nn(const SkArgs &a, int tile, int bk, int pages, bool vec, bool ext,
+                              cudaStream_t stream);
+cudaError_t launch_ffma_sk_nt(const SkArgs &a, int tile, int bk, int pages, bool vec,
+                              cudaStream_t stream);
+cudaError_t launch_ffma_sk_tn(const SkArgs &a, int tile, int bk, int pages, bool vec, bool ext,
+                              cudaStream_t stream);
+cudaError_t launch_ffma_sk_tt(const SkArgs &a, int tile, int bk, int pages, bool vec,
+                              cudaStream_t stream);
+// dynamic shared memory of one CTA of the stream-K kernel
+constexpr int sk_smem_bytes(int tile, int bk, int pages, bool staged_a, bool staged_b) {
+    return (2 * pages + (staged_a ? 2 : 0) + (staged_b ? 2 : 0)) * tile * bk * 4;
+}
 
 // op(A) = A^T when trans_a (A stored K x M), op(B) = B^T when trans_b.
 // `tile` is 128 or 64 (the plan's bm).

@@ -1010,8 +1010,8 @@ Tf32x3Plan tf32x3_plan(int64_t M, int64_t N, int64_t K, int sms) {
     plan.tiles = tiles;
     plan.tail_start = tiles;
     if (sms <= 0) return plan;
-    if (const char *force = std::getenv("SGEMM_TF32X3_FORCE_SPLIT")) {
-        const int f = std::atoi(force);
+    {
+        const int f = tuning(kKnobTf32x3Split);
         if (f >= 1 && f <= 64 && tiles <= kMaxSplitTiles) {
             plan.split = f;
             return plan;
@@ -1026,11 +1026,11 @@ Tf32x3Plan tf32x3_plan(int64_t M, int64_t N, int64_t K, int sms) {
     // Tail: with one CTA per SM, a last wave of tiles that fills at most half
     // the SMs idles the rest for a whole tile's time; cut just those tiles
     // into K ranges (all of them still fitting in one wave).
-    // SGEMM_TF32X3_FORCE_TAIL=0 disables it, =s forces s ranges.
+    // The tuning knob kKnobTf32x3Tail = 0 disables it, = s forces s ranges.
     const int64_t rem = tiles % sms;
     int want = 0;
     if (rem > 0 && 2 * rem <= sms) want = int(std::min<int64_t>(sms / rem, 4));
-    if (const char *force = std::getenv("SGEMM_TF32X3_FORCE_TAIL")) want = std::atoi(force);
+    if (const int force = tuning(kKnobTf32x3Tail); force >= 0) want = force;
     if (tiles >= sms && rem > 0 && want >= 2 && rem * want <= sms && nkb >= 8 * want) {
         plan.tail_start = tiles - rem;
         plan.tail_split = want;
@@ -1048,15 +1048,14 @@ bool tf32x3_fusable_a(const float *A, int64_t lda) {
 }
 
 // A is split inside the kernel (tf32x3_fused_kernel) whenever TMA can read it
-// as stored; SGEMM_TF32X3_FUSE_A=0 forces the pre-pass instead.  Measured on
+// as stored; the tuning knob kKnobTf32x3FuseA = 0 forces the pre-pass instead.  Measured on
 // GB300 (TFLOP/s, pre-pass / in-kernel): 8192^3 259 / 287 (271 / 300 with B
 // packed once), 4096^3 201 / 231, 1024x1024x16384 112 / 138.  What made the
 // in-kernel split pay was the branch-free TF32 rounding: with early returns
 // the converters' 64 conversions per slice did not interleave and the kernel
 // ran at 40 % of these rates.
 bool tf32x3_use_fused_a(const float *A, int64_t lda) {
-    const char *env = std::getenv("SGEMM_TF32X3_FUSE_A");
-    if (env && std::atoi(env) == 0) return false;
+    if (tuning(kKnobTf32x3FuseA) == 0) return false;
     return tf32x3_fusable_a(A, lda);
 }
 

@@ -98,7 +98,10 @@ typedef struct {
     int64_t k_per_split;   /* K extent of one partition (a multiple of bk) */
     int64_t tiles_m, tiles_n;
     int64_t grid_ctas;     /* CTAs launched */
-    size_t workspace_bytes;/* device scratch the plan needs (0 without split tiles) */
+    size_t workspace_bytes;/* device scratch the plan needs: the split-K tile
+                              counters and partial tiles, and the transposed
+                              copy of A when transpose_a is set; 0 when it has
+                              neither */
     int64_t tail_start;    /* first tile (in launch order) of the tail region; tiles
                               when there is none.  Only the last, partly filled wave
                               of tiles is split, so it ends sooner */
@@ -106,8 +109,18 @@ typedef struct {
     int32_t transpose_a;   /* 1: A is first transposed into the workspace (K x M, row
                               stride a_t_ld) and the product runs with A read as a
                               row-per-k operand, which is faster for large grids */
-    int32_t reserved;
+    int32_t stages;        /* shared-memory pages in the K-slice ring: 2 (one
+                              slice in flight while one is computed), or 3
+                              (two in flight; K slices of 32, transpose_a) */
     int64_t a_t_ld;        /* row stride of the transposed copy (floats) */
+    int32_t schedule;      /* 0: one CTA per (tile, K range) as above; 1: persistent
+                              stream-K: grid_ctas CTAs stay resident, take whole-K
+                              tiles round-robin for dp_rounds rounds, then split the
+                              K slices of the remaining tiles into grid_ctas equal
+                              runs (split_k = tail_split = 1 then) */
+    int32_t dp_rounds;     /* stream-K: rounds of whole-K tiles */
+    int64_t sk_iters;      /* stream-K: K slices (of bk) of the tiles after the
+                              dp_rounds * grid_ctas whole-K ones */
 } gemm_plan_t;
 
 /*
@@ -136,10 +149,17 @@ sgemm_status gemm_plan_for_sms(int64_t M, int64_t N, int64_t K, int64_t lda, int
 
 /*
  * sgemm -- C = alpha*A*B + beta*C on `stream` (see the conventions above).
- * Plans the shape with gemm_plan.  When the plan needs workspace (split-K),
- * the library uses a buffer it owns, one per (device, stream), grown with
- * stream-ordered allocation and kept until exit; its first use on a stream
- * therefore allocates.  Returns SGEMM_OK or an error status.
+ * Plans the shape with gemm_plan.  When the plan needs workspace (split-K
+ * partials, or the transposed copy of A that large full-grid plans make
+ * first: 4*K*M bytes, about 256 MiB at M = K = 8192), the library uses a
+ * buffer it owns, one per (device, stream), grown with stream-ordered
+ * allocation (cudaMallocAsync, plus 25 % headroom) and kept until the
+ * process exits; the first call on a stream, and any call that needs more
+ * than the buffer holds, therefore allocates.  If that allocation fails for
+ * a plan with the transposed copy, sgemm falls back to the plan that reads A
+ * as stored (no copy; split-K scratch at most) and runs it.  Returns
+ * SGEMM_OK or an error status (SGEMM_ERR_ALLOC when even the fallback's
+ * scratch cannot be had).
  */
 sgemm_status sgemm(int64_t M, int64_t N, int64_t K, float alpha,
                    const float *A, int64_t lda, const float *B, int64_t ldb,
@@ -167,9 +187,14 @@ sgemm_status sgemm_with_plan(const gemm_plan_t *plan, int64_t M, int64_t N, int6
 #define SGEMM_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 
 /*
- * sgemm_noalloc -- the same C = alpha*A*B + beta*C as sgemm, same arguments,
- * same plan, same kernels and bit-identical results, for callers that must
- * not allocate device memory.  The pages have no counterpart to this call.
+ * sgemm_noalloc -- the same C = alpha*A*B + beta*C as sgemm, with the same
+ * arguments, for callers that must not allocate device memory.  The pages
+ * have no counterpart to this call.  It always runs the plan without the
+ * transposed copy of A (that copy would need M*K floats of scratch), so its
+ * results are bit-identical to sgemm's under that plan -- sgemm with the
+ * tuning knob SGEMM_TUNE_TRANSPOSE_A set to 0 -- and, for shapes where sgemm
+ * makes the copy, equal to sgemm's within the accuracy the conventions above
+ * state rather than bit for bit.
  *
  * Who needs it: code that runs where a cudaMalloc is not allowed or not
  * safe -- an application or framework that reserved the device memory up
@@ -233,8 +258,8 @@ sgemm_status sgemm_tf32x3(int64_t M, int64_t N, int64_t K, float alpha,
  * multiplied many times (weights) be packed once.  A is K-major as stored:
  * when it is 16-byte aligned with lda % 4 == 0 its split happens inside the
  * kernel's shared-memory stage (the raw fp32 tile arrives by TMA and is split
- * in place, with no pass over A in HBM); otherwise, or with
- * SGEMM_TF32X3_FUSE_A=0 in the environment, in a pre-pass.
+ * in place, with no pass over A in HBM); otherwise, or with the tuning knob
+ * SGEMM_TUNE_TF32X3_FUSE_A set to 0, in a pre-pass.
  *
  * sgemm_tf32x3_packed_b_bytes -- size of the packed form of a K x N matrix
  *   (0 for K or N <= 0).
@@ -308,6 +333,44 @@ sgemm_status sgemm_ex(int32_t op_a, int32_t op_b, int64_t M, int64_t N, int64_t 
                       const float *B, int64_t ldb, int64_t stride_b, float beta, float *C,
                       int64_t ldc, int64_t stride_c, int64_t batch, const float *bias,
                       int32_t act, void *stream);
+
+/*
+ * Tuning knobs: overrides of the planner's choices, for measurement sweeps
+ * and tests.  Each starts from the environment variable named beside it,
+ * read once when the library is loaded (never on the call path); after that
+ * only sgemm_set_tuning changes it.  The value -1 means "the planner
+ * decides" (the default).  Knobs are process-wide and take effect for plans
+ * made after the change; set them while no other host thread is planning.
+ */
+typedef enum {
+    SGEMM_TUNE_SPLIT_K = 0,       /* SGEMM_FORCE_SPLIT: K ranges per tile, 1..32 */
+    SGEMM_TUNE_TAIL_SPLIT = 1,    /* SGEMM_FORCE_TAIL: K ranges of the tiles of the
+                                     last partial wave, 0..32 (< 2: none) */
+    SGEMM_TUNE_TILE = 2,          /* SGEMM_FORCE_TILE: CTA tile 64 or 128 */
+    SGEMM_TUNE_KERNEL = 3,        /* SGEMM_FORCE_KERNEL: 0 scalar, 1 packed FMA issue */
+    SGEMM_TUNE_TRANSPOSE_A = 4,   /* SGEMM_FORCE_TRANSPOSE_A: 0 never, 1 whenever able */
+    SGEMM_TUNE_FFMA_EXT = 5,      /* SGEMM_FFMA_EXT: 0/1, which compiled build of the
+                                     FFMA kernel runs plain products */
+    SGEMM_TUNE_TF32X3_SPLIT = 6,  /* SGEMM_TF32X3_FORCE_SPLIT: tensor mode, 1..64 */
+    SGEMM_TUNE_TF32X3_TAIL = 7,   /* SGEMM_TF32X3_FORCE_TAIL: tensor mode, 0..64 */
+    SGEMM_TUNE_TF32X3_FUSE_A = 8, /* SGEMM_TF32X3_FUSE_A: 0 forces A's pre-pass split */
+    SGEMM_TUNE_WORKSPACE_LIMIT_MIB = 9, /* SGEMM_WORKSPACE_LIMIT_MIB: cap, in MiB, on each
+                                     library-owned workspace; a larger request fails
+                                     as a failed allocation would (SGEMM_ERR_ALLOC) */
+    SGEMM_TUNE_SCHEDULE = 10,     /* SGEMM_SCHEDULE: 0 one CTA per (tile, K range),
+                                     1 persistent stream-K (see gemm_plan_t.schedule) */
+    SGEMM_TUNE_SK_MIN_SLICES = 11, /* SGEMM_SK_MIN_SLICES: stream-K, fewest K slices in
+                                     one CTA's run (1..2^20) */
+    SGEMM_TUNE_SK_GRID = 12       /* SGEMM_SK_GRID: stream-K, CTAs of a grid of under two
+                                     waves of tiles (1..2^20) */
+} sgemm_tuning_knob;
+
+/* Sets a knob (value -1 restores the planner's choice).  Returns
+ * SGEMM_ERR_INVALID_ARG for an unknown knob or a value outside its range. */
+sgemm_status sgemm_set_tuning(int32_t knob, int32_t value);
+
+/* Current value of a knob (-1: the planner decides; -2: unknown knob). */
+int32_t sgemm_get_tuning(int32_t knob);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char *sgemm_status_string(sgemm_status status);

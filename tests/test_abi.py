@@ -4,6 +4,7 @@ input before anything would be launched; the planner's choices."""
 from __future__ import annotations
 
 import ctypes
+import sys
 import os
 import re
 import subprocess
@@ -122,7 +123,7 @@ def test_plan_full_tiles_take_the_unchecked_vector_path(lib):
     assert p.workspace_bytes == sg.WORKSPACE_COUNTER_BYTES + 8192 * 8192 * 4
 
 
-def test_plan_transpose_choice(lib, monkeypatch):
+def test_plan_transpose_choice(lib, tune):
     assert plan(4096, 4096, 4096).transpose_a == 1
     assert plan(2048, 2048, 2048).transpose_a == 1        # 256 tiles, at least one per SM
     assert plan(1024, 2304, 768).transpose_a == 0         # 144 tiles, under one per SM
@@ -131,17 +132,17 @@ def test_plan_transpose_choice(lib, monkeypatch):
     assert plan(1024, 1024, 1024).transpose_a == 0        # split-K plan, short K
     assert plan(4096, 512, 4096).transpose_a == 0         # N < 1024
     assert plan(4096, 4096, 4096, A=4100).transpose_a == 0   # not vector-aligned
-    monkeypatch.setenv("SGEMM_FORCE_TRANSPOSE_A", "0")
+    tune(transpose_a="0")
     q = plan(8192, 8192, 8192)
     assert q.transpose_a == 0 and q.workspace_bytes == 0 and q.bk == 16
-    monkeypatch.setenv("SGEMM_FORCE_TRANSPOSE_A", "1")
+    tune(transpose_a="1")
     r = plan(1023 * 2, 4096, 515, lda=516)
     assert r.transpose_a == 1 and r.a_t_ld == 2048 and r.edge == 1 and r.bk == 32
     assert r.workspace_bytes == sg.WORKSPACE_COUNTER_BYTES + (515 * 2048 * 4 + 255) // 256 * 256
 
 
-def test_plan_tail_split_is_opt_in(lib, monkeypatch):
-    monkeypatch.setenv("SGEMM_FORCE_TAIL", "2")
+def test_plan_tail_split_is_opt_in(lib, tune):
+    tune(tail_split="2")
     p = plan(8192, 8192, 8192)
     # 4096 tiles over 304 resident slots: 13 full waves + 144 tiles, which
     # are the ones split in two along K
@@ -154,7 +155,7 @@ def test_plan_tail_split_is_opt_in(lib, monkeypatch):
     assert q.tail_split == 1 and q.tail_start == q.tiles_m * q.tiles_n
     r = plan(1000, 1000, 100)                               # short K: nothing to split
     assert r.tail_split == 1 or r.tail_k_per_split >= 16
-    monkeypatch.setenv("SGEMM_FORCE_TAIL", "0")
+    tune(tail_split="0")
     t = plan(8192, 8192, 8192)
     assert t.tail_split == 1 and t.grid_ctas == 4096
 
@@ -167,7 +168,7 @@ def test_plan_ragged_shape_takes_the_checked_scalar_path(lib):
     assert p.tiles_m == 16 and p.tiles_n == 13
 
 
-def test_plan_tile_choice(lib, monkeypatch):
+def test_plan_tile_choice(lib, tune):
     assert plan(8192, 8192, 8192).bm == 128
     assert plan(1024, 2304, 768).bm == 128        # 144 tiles of 128
     assert plan(1024, 768, 3072).bm == 128        # 48 tiles of 128, but K is long
@@ -176,9 +177,9 @@ def test_plan_tile_choice(lib, monkeypatch):
     assert plan(1024, 64, 1024).bm == 64          # a 128-wide tile would be half padding
     assert plan(256, 256, 256).bm == 64
     assert plan(256, 256, 256, sms=4).bm == 128   # a small GPU is filled by 4 tiles
-    monkeypatch.setenv("SGEMM_FORCE_TILE", "128")
+    tune(tile="128")
     assert plan(256, 256, 256).bm == 128
-    monkeypatch.setenv("SGEMM_FORCE_TILE", "64")
+    tune(tile="64")
     q = plan(8192, 8192, 8192)
     assert q.bm == 64 and q.tiles_m == 128 and q.threads == 64 and q.edge == 0
 
@@ -189,9 +190,10 @@ def test_plan_misaligned_pointer_disables_vector_loads(lib):
     assert plan(256, 256, 256, C=4104).vec == 0
 
 
-def test_plan_split_k_fills_the_gpu_when_tiles_are_few(lib, monkeypatch):
-    monkeypatch.setenv("SGEMM_FORCE_TILE", "128")
-    monkeypatch.setenv("SGEMM_FORCE_TRANSPOSE_A", "0")   # split-K bookkeeping only
+def test_plan_split_k_fills_the_gpu_when_tiles_are_few(lib, tune):
+    tune(schedule=0)   # one CTA per (tile, K range); the stream-K plans have their own tests
+    tune(tile="128")
+    tune(transpose_a="0")   # split-K bookkeeping only
     p = plan(1024, 1024, 16384)          # 64 tiles, long K
     assert p.split_k > 1
     assert p.k_per_split % p.bk == 0
@@ -201,7 +203,7 @@ def test_plan_split_k_fills_the_gpu_when_tiles_are_few(lib, monkeypatch):
     assert p.workspace_bytes == sg.WORKSPACE_COUNTER_BYTES + 64 * p.split_k * 128 * 128 * 4
     # MLP-down: 48 tiles, K = 3072
     assert plan(1024, 768, 3072).split_k > 1
-    monkeypatch.setenv("SGEMM_FORCE_TILE", "64")
+    tune(tile="64")
     q = plan(1024, 1024, 16384)          # 64-wide tiles: 256 of them, still split along K
     tiles = q.tiles_m * q.tiles_n
     assert q.bm == 64 and tiles == 256 and q.split_k > 1
@@ -221,8 +223,9 @@ def test_plan_depends_on_sm_count(lib):
     assert big.split_k >= 1
 
 
-def test_sgemm_with_plan_rejects_mismatched_plan_and_small_workspace(lib, monkeypatch):
-    monkeypatch.setenv("SGEMM_FORCE_TILE", "128")
+def test_sgemm_with_plan_rejects_mismatched_plan_and_small_workspace(lib, tune):
+    tune(tile="128")
+    tune(schedule=0)
     p = plan(1024, 1024, 16384)
     assert p.split_k > 1
     # workspace too small -> SGEMM_ERR_WORKSPACE (checked before the device)
@@ -240,18 +243,90 @@ def test_sgemm_with_plan_rejects_mismatched_plan_and_small_workspace(lib, monkey
     assert rc == 1
 
 
-def test_forced_split_override(lib, monkeypatch):
-    monkeypatch.setenv("SGEMM_FORCE_TILE", "128")
-    monkeypatch.setenv("SGEMM_FORCE_SPLIT", "4")
+def test_forced_split_override(lib, tune):
+    tune(tile="128")
+    tune(split_k="4")
     p = plan(512, 512, 1024)
     assert p.split_k == 4 and p.k_per_split == 256
-    monkeypatch.setenv("SGEMM_FORCE_SPLIT", "1")
+    tune(split_k="1")
     assert plan(1024, 1024, 16384).split_k == 1
 
 
-def test_forced_kernel_override(lib, monkeypatch):
-    monkeypatch.setenv("SGEMM_FORCE_TILE", "128")
-    monkeypatch.setenv("SGEMM_FORCE_KERNEL", "0")
+def test_forced_kernel_override(lib, tune):
+    tune(tile="128")
+    tune(kernel="0")
     assert plan(256, 256, 256).kernel == 0
-    monkeypatch.setenv("SGEMM_FORCE_KERNEL", "1")
+    tune(kernel="1")
     assert plan(256, 256, 256).kernel == 1
+
+
+def test_tuning_knobs_round_trip_and_range_checks(lib, tune):
+    for knob in sg.TUNING_KNOBS:
+        assert sg.get_tuning(knob) is None or isinstance(sg.get_tuning(knob), int)
+    tune(tile=64, split_k=3, transpose_a=0)
+    assert sg.get_tuning("tile") == 64 and sg.get_tuning("split_k") == 3
+    assert plan(8192, 8192, 8192).bm == 64
+    tune(tile=None)
+    assert sg.get_tuning("tile") is None and plan(8192, 8192, 8192).bm == 128
+    # out-of-range values and unknown knobs are refused, the knob is unchanged
+    for knob, bad in (("tile", 96), ("split_k", 0), ("split_k", 33), ("kernel", 2),
+                      ("transpose_a", 5), ("workspace_limit_mib", -3)):
+        before = sg.get_tuning(knob)
+        assert lib.sgemm_set_tuning(sg.TUNING_KNOBS[knob], bad) == 1
+        assert sg.get_tuning(knob) == before
+    assert lib.sgemm_set_tuning(len(sg.TUNING_KNOBS), 1) == 1
+    assert lib.sgemm_set_tuning(-1, 1) == 1
+    assert lib.sgemm_get_tuning(len(sg.TUNING_KNOBS)) == -2
+
+
+def test_tuning_env_is_read_once_at_load(lib):
+    """The environment seeds the knobs when the library loads; changing it
+    afterwards changes no plan (the call path never reads it)."""
+    code = (
+        "import os, sys; sys.path.insert(0, %r)\n"
+        "import dense_fp32_matrix_06_gb300 as sg\n"
+        "sg.load_library()\n"
+        "a = sg.gemm_plan_for_sms(8192, 8192, 8192, 8192, 8192, 8192).bm\n"
+        "os.environ['SGEMM_FORCE_TILE'] = '128'\n"
+        "b = sg.gemm_plan_for_sms(8192, 8192, 8192, 8192, 8192, 8192).bm\n"
+        "print(a, b, sg.get_tuning('tile'), sg.get_tuning('split_k'))\n" % ROOT)
+    env = dict(os.environ, SGEMM_FORCE_TILE="64", SGEMM_FORCE_SPLIT="banana")
+    out = subprocess.run([sys.executable, "-c", code], env=env, check=True,
+                         capture_output=True, text=True).stdout.split()
+    assert out == ["64", "64", "64", "None"]
+
+
+def test_plan_schedule_choice(lib, tune):
+    """Persistent stream-K where it measured faster: tiny grids of 64-wide
+    tiles and few 128-wide tiles with long K; one CTA per (tile, K range)
+    elsewhere."""
+    p = plan(256, 256, 256)
+    assert p.schedule == 1 and p.bm == 64 and p.bk == 8 and p.stages == 4
+    q = plan(1024, 1024, 16384)      # 64 tiles, K = 16384: A transposed, then stream-K
+    assert q.schedule == 1 and q.transpose_a == 1 and q.bk == 32 and q.stages == 3
+    for shape in [(1024, 1024, 1024), (1023, 777, 513), (1024, 2304, 768), (2048, 2048, 2048),
+                  (8192, 8192, 8192), (8192, 8192, 64)]:
+        assert plan(*shape).schedule == 0, shape
+    tune(schedule=0)
+    assert plan(256, 256, 256).schedule == 0
+    tune(schedule=1)
+    assert plan(8192, 8192, 8192).schedule == 1
+
+
+def test_stream_k_plan_round_trips_through_sgemm_with_plan_checks(lib, tune):
+    """A stream-K plan is accepted by sgemm_with_plan's plan check (failing
+    only later, on the missing device) and a tampered one is refused."""
+    tune(schedule=1, tile=128, transpose_a=0)
+    p = plan(1024, 1024, 1024)
+    assert p.schedule == 1 and p.sk_iters > 0
+    # workspace too small -> SGEMM_ERR_WORKSPACE before the device is touched
+    rc = lib.sgemm_with_plan(ctypes.byref(p), 1024, 1024, 1024, 1.0, 4096, 1024, 4096, 1024,
+                             0.0, 4096, 1024, 4096, 16, None)
+    assert rc == 7
+    for field, value in (("grid_ctas", p.sk_iters + 1), ("dp_rounds", 1), ("stages", 3),
+                         ("sk_iters", p.sk_iters - 1), ("bk", 32)):
+        q = sg.GemmPlan.from_buffer_copy(p)
+        setattr(q, field, value)
+        rc = lib.sgemm_with_plan(ctypes.byref(q), 1024, 1024, 1024, 1.0, 4096, 1024, 4096,
+                                 1024, 0.0, 4096, 1024, 4096, 1 << 30, None)
+        assert rc == 1, field

@@ -89,3 +89,21 @@ def test_reference_arm_other_ranks_print_nothing():
                           "--workload", "square256", "--steps", "1", "--warmup", "1"],
                          capture_output=True, text=True, env=env, timeout=120, check=True).stdout
     assert out.strip() == ""
+
+
+def test_per_workload_roofline_arithmetic():
+    import workloads
+    p = workloads.workload("square1024ab")
+    # A, B read once; C read (beta != 0) and written
+    assert bench.algorithmic_bytes(p) == 4 * (1024 * 1024 * 4)
+    q = workloads.workload("skinny_k64")
+    assert bench.algorithmic_bytes(q) == 4 * (8192 * 64 * 2 + 8192 * 8192)
+    # 8192^2 x 64 at 80 TFLOP/s and 6.8 TB/s: 107 us of FMAs, 40 us of HBM
+    r = bench.roofline_entry(q.flops, bench.algorithmic_bytes(q), 214.7e-6, 80.0, 6800.0)
+    assert r["bound"] == "alu"
+    assert r["frac"] == pytest.approx(q.flops / 80e12 / 214.7e-6, rel=1e-3)
+    assert r["hbm_gbs"] == pytest.approx(bench.algorithmic_bytes(q) / 214.7e-6 / 1e9, rel=1e-3)
+    # at the tensor mode's effective peak the same shape is bound by HBM
+    t = bench.roofline_entry(q.flops, bench.algorithmic_bytes(q), 50e-6, 316.0, 6800.0)
+    assert t["bound"] == "hbm"
+    assert t["frac"] == pytest.approx(bench.algorithmic_bytes(q) / 6800e9 / 50e-6, rel=1e-3)

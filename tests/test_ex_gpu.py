@@ -131,8 +131,8 @@ def test_layouts_and_batches(sg, op_a, op_b, shape, batch):
 
 @pytest.mark.parametrize("op_a,op_b", LAYOUTS)
 @pytest.mark.parametrize("tile", ["64", "128"])
-def test_layouts_on_both_tiles(sg, monkeypatch, op_a, op_b, tile):
-    monkeypatch.setenv("SGEMM_FORCE_TILE", tile)
+def test_layouts_on_both_tiles(sg, tune, op_a, op_b, tile):
+    tune(tile=tile)
     p = ExProblem(op_a, op_b, 200, 136, 100, 2, seed=30, alpha=0.5, beta=-1.0, bias=True, act=1)
     p.check(p.run(sg), exact=False)
     q = ExProblem(op_a, op_b, 128, 192, 64, 3, seed=31, dist="int4", alpha=1.5, beta=0.5,

@@ -204,10 +204,10 @@ def test_empty_shapes_are_no_ops(sg):
 
 @pytest.mark.parametrize("kernel,tile", [("0", "128"), ("1", "128"), ("0", "64")])
 @pytest.mark.parametrize("split", ["1", "2", "3", "7"])
-def test_forced_kernel_and_split(sg, monkeypatch, kernel, tile, split):
-    monkeypatch.setenv("SGEMM_FORCE_KERNEL", kernel)
-    monkeypatch.setenv("SGEMM_FORCE_TILE", tile)
-    monkeypatch.setenv("SGEMM_FORCE_SPLIT", split)
+def test_forced_kernel_and_split(sg, tune, kernel, tile, split):
+    tune(kernel=kernel)
+    tune(tile=tile)
+    tune(split_k=split)
     p = workloads.make(300, 260, 1000, seed=31, beta=0.5, c0_dist="uniform")
     run_and_check(sg, p)
     q = workloads.make(256, 384, 1024, dist="int4", seed=32, alpha=1.5, beta=0.5,
@@ -222,23 +222,23 @@ def test_forced_kernel_and_split(sg, monkeypatch, kernel, tile, split):
     (2560, 2048, 1040, "uniform", None),
     (2500, 2000, 777, "uniform", (781, 2003, 2001)),   # ragged tail tiles, scalar path
 ])
-def test_tail_split_parity(sg, monkeypatch, M, N, K, dist, lds):
+def test_tail_split_parity(sg, tune, M, N, K, dist, lds):
     lda, ldb, ldc = lds if lds else (None, None, None)
     p = workloads.make(M, N, K, dist=dist, seed=51, lda=lda, ldb=ldb, ldc=ldc,
                        alpha=1.5 if dist == "int4" else 0.75, beta=0.5,
                        c0_dist="int4" if dist == "int4" else "uniform")
-    monkeypatch.setenv("SGEMM_FORCE_TAIL", "4")
+    tune(tail_split="4")
     plan = sg.gemm_plan_for_sms(p.M, p.N, p.K, p.lda, p.ldb, p.ldc, sm_count=152)
     assert plan.tail_split > 1
     run_and_check(sg, p, exact=dist == "int4")
-    monkeypatch.setenv("SGEMM_FORCE_TAIL", "0")
+    tune(tail_split="0")
     run_and_check(sg, p, exact=dist == "int4")
 
 
 @pytest.mark.parametrize("tile", ["64", "128"])
 @pytest.mark.parametrize("name", ["square1024ab", "ragged", "gpt2_qkv", "square256_int"])
-def test_forced_tile(sg, monkeypatch, tile, name):
-    monkeypatch.setenv("SGEMM_FORCE_TILE", tile)
+def test_forced_tile(sg, tune, tile, name):
+    tune(tile=tile)
     p = workloads.workload(name)
     run_and_check(sg, p, exact=p.meta["dist"] == "int4")
 
@@ -249,10 +249,10 @@ def test_forced_tile(sg, monkeypatch, tile, name):
     (2046, 1030, 515, (516, 1032, 1036), "uniform"),     # ragged: bounds-checked tiles
     (1024, 1536, 768, None, "int4"),
 ])
-def test_transposed_a_path(sg, monkeypatch, force, M, N, K, lds, dist):
-    monkeypatch.setenv("SGEMM_FORCE_TRANSPOSE_A", force)
-    monkeypatch.setenv("SGEMM_FORCE_SPLIT", "1")
-    monkeypatch.setenv("SGEMM_FORCE_TILE", "128")
+def test_transposed_a_path(sg, tune, force, M, N, K, lds, dist):
+    tune(transpose_a=force)
+    tune(split_k="1")
+    tune(tile="128")
     lda, ldb, ldc = lds if lds else (None, None, None)
     p = workloads.make(M, N, K, dist=dist, seed=61, lda=lda, ldb=ldb, ldc=ldc,
                        alpha=1.5 if dist == "int4" else 0.75, beta=0.5,
@@ -263,10 +263,10 @@ def test_transposed_a_path(sg, monkeypatch, force, M, N, K, lds, dist):
 
 
 @pytest.mark.parametrize("split", ["2", "3"])
-def test_transposed_a_with_split_k(sg, monkeypatch, split):
-    monkeypatch.setenv("SGEMM_FORCE_TRANSPOSE_A", "1")
-    monkeypatch.setenv("SGEMM_FORCE_SPLIT", split)
-    monkeypatch.setenv("SGEMM_FORCE_TILE", "128")
+def test_transposed_a_with_split_k(sg, tune, split):
+    tune(schedule=0, transpose_a="1")
+    tune(split_k=split)
+    tune(tile="128")
     p = workloads.make(512, 1024, 1000, seed=62, alpha=0.5, beta=-0.75, c0_dist="uniform")
     plan = sg.gemm_plan_for_sms(p.M, p.N, p.K, p.lda, p.ldb, p.ldc)
     assert plan.transpose_a == 1 and plan.split_k == int(split) and plan.bk == 32
@@ -275,7 +275,7 @@ def test_transposed_a_with_split_k(sg, monkeypatch, split):
     run_and_check(sg, q, exact=True)
 
 
-def test_transposed_a_with_caller_workspace(sg, monkeypatch):
+def test_transposed_a_with_caller_workspace(sg, tune):
     import torch
     p = workloads.workload("square4096")
     A = torch.from_numpy(p.A).cuda()
@@ -296,11 +296,11 @@ def test_transposed_a_with_caller_workspace(sg, monkeypatch):
     assert e.value.status == 7
 
 
-def test_both_kernels_bit_identical(sg, monkeypatch):
-    monkeypatch.setenv("SGEMM_FORCE_TILE", "128")
+def test_both_kernels_bit_identical(sg, tune):
+    tune(tile="128")
     outs = []
     for kernel in ("0", "1"):
-        monkeypatch.setenv("SGEMM_FORCE_KERNEL", kernel)
+        tune(kernel=kernel)
         for name in ("square1024ab", "ragged", "long_k"):
             p = workloads.workload(name)
             d = DeviceProblem(p)
@@ -332,7 +332,8 @@ def test_sgemm_with_plan_caller_workspace(sg):
     B = torch.from_numpy(p.B).cuda()
     C = torch.empty((p.M, p.N), device="cuda")
     plan = sg.plan_for(A, B, C)
-    assert plan.split_k > 1 and plan.workspace_bytes > 0
+    # tiles share K ranges (split-K or stream-K), so the plan needs counters
+    assert (plan.split_k > 1 or plan.sk_iters > 0) and plan.workspace_bytes > 0
     ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
     ref = oracle.problem(p)
     for _ in range(3):   # the counters are left zero, so the buffer can be reused
@@ -380,16 +381,32 @@ LARGE = ["square2048", "square4096", "square8192", "skinny_k64", "long_k"]
 @pytest.mark.parametrize("name", LARGE)
 @pytest.mark.parametrize("dist", ["uniform", "int4"])
 def test_large_workload_sampled(sg, name, dist):
+    """The benchmark-size launches, checked where the oracle can afford it:
+    3000 random entries, one random entry inside every output tile of the
+    launch's plan, three single rows, and one whole block of tile rows."""
     p = workloads.workload(name, dist=None if dist == "uniform" else dist)
     d = DeviceProblem(p)
+    plan = sg.gemm_plan(p.M, p.N, p.K, p.lda, p.ldb, p.ldc, d.a_ptr, d.b_ptr, d.c_ptr)
     d.run(sg)
     C, buf = d.result()
     d.check_untouched(buf)
     ii, jj = workloads.sample_indices(p.M, p.N, 3000, seed=7)
+    # one entry per output tile (tile rows x tile columns of the plan)
+    rng = np.random.default_rng(11)
+    tm, tn = np.meshgrid(np.arange(plan.tiles_m), np.arange(plan.tiles_n), indexing="ij")
+    ti = tm.ravel() * plan.bm + rng.integers(0, plan.bm, tm.size)
+    tj = tn.ravel() * plan.bn + rng.integers(0, plan.bn, tn.size)
+    keep = (ti < p.M) & (tj < p.N)
+    assert keep.sum() >= plan.tiles_m * plan.tiles_n - plan.tiles_m - plan.tiles_n
+    ii = np.concatenate([ii, ti[keep]])
+    jj = np.concatenate([jj, tj[keep]])
     ref = oracle.sgemm_entries(p.M, p.N, p.K, p.alpha, p.A, p.B, p.beta, p.C0, ii, jj,
                                lda=p.lda, ldb=p.ldb, ldc0=p.ldc)
     got = C[ii, jj]
-    rows = np.array([0, p.M // 2 + 1, p.M - 1], np.int64)
+    # three rows, plus every row of one seeded tile row
+    r0 = int(rng.integers(0, plan.tiles_m)) * plan.bm
+    block = np.arange(r0, min(r0 + plan.bm, p.M), dtype=np.int64)
+    rows = np.concatenate([np.array([0, p.M // 2 + 1, p.M - 1], np.int64), block])
     ref_rows = oracle.sgemm_rows(p.M, p.N, p.K, p.alpha, p.A, p.B, p.beta, p.C0, rows,
                                  lda=p.lda, ldb=p.ldb, ldc0=p.ldc)
     if dist == "int4":
@@ -401,3 +418,31 @@ def test_large_workload_sampled(sg, name, dist):
         assert float(np.abs(got.astype(np.float64) - ref).max()) / den <= TOL_FFMA
         assert float(np.abs(C[rows].astype(np.float64) - ref_rows).max()) / den <= TOL_FFMA
         assert np.all(np.isfinite(C))
+
+
+def test_transposed_plan_falls_back_when_the_workspace_is_capped(sg, tune):
+    """When the workspace for the transposed copy of A cannot be had (here a
+    1 MiB cap stands in for a failed allocation), sgemm runs the plan that
+    reads A as stored; the tensor mode, which has no such fallback, reports
+    SGEMM_ERR_ALLOC and leaves C alone."""
+    torch = _torch()
+    p = workloads.make(2048, 2048, 512, dist="int4", seed=71, alpha=1.5, beta=0.5,
+                       c0_dist="int4")
+    assert sg.gemm_plan_for_sms(p.M, p.N, p.K, p.lda, p.ldb, p.ldc).transpose_a == 1
+    tune(workspace_limit_mib=1)
+    stream = torch.cuda.Stream()     # a stream the library holds no workspace for yet
+    A = torch.from_numpy(p.A).cuda()
+    B = torch.from_numpy(p.B).cuda()
+    C = torch.from_numpy(p.C0).cuda()
+    with torch.cuda.stream(stream):
+        sg.sgemm_ptr(p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
+                     C.data_ptr(), p.ldc, stream.cuda_stream)
+    torch.cuda.synchronize()
+    assert np.array_equal(C.cpu().numpy()[:, :p.N], oracle.problem(p))
+    C2 = torch.from_numpy(p.C0).cuda()
+    with pytest.raises(sg.SgemmError) as e:
+        sg.sgemm_tf32x3_ptr(p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb,
+                            p.beta, C2.data_ptr(), p.ldc, stream.cuda_stream)
+    assert e.value.status == 6
+    torch.cuda.synchronize()
+    assert np.array_equal(C2.cpu().numpy(), p.C0)
