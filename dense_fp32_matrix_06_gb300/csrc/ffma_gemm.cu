@@ -28,8 +28,11 @@ __global__ void scale_kernel(float *C, int64_t M, int64_t N, int64_t ldc, float 
 // k) and the writes (along m) are coalesced.  Feeds the product that reads A
 // one k-row at a time (see the planner's transpose_a).
 __global__ void transpose_kernel(const float *__restrict__ A, int64_t M, int64_t K, int64_t lda,
-                                 float *__restrict__ At, int64_t ldt) {
+                                 float *__restrict__ At, int64_t ldt, int64_t stride_a,
+                                 int64_t stride_t) {
     __shared__ float tile[32][33];
+    A += int64_t(blockIdx.z) * stride_a;    // batch z
+    At += int64_t(blockIdx.z) * stride_t;
     const int64_t m0 = int64_t(blockIdx.y) * 32, k0 = int64_t(blockIdx.x) * 32;
     const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8
     for (int i = ty; i < 32; i += 8) {
@@ -50,8 +53,11 @@ __global__ void transpose_kernel(const float *__restrict__ A, int64_t M, int64_t
 // store phase then see at most two-way bank conflicts.
 __global__ void __launch_bounds__(256) transpose64_kernel(const float *__restrict__ A, int64_t M,
                                                           int64_t K, int64_t lda,
-                                                          float *__restrict__ At, int64_t ldt) {
+                                                          float *__restrict__ At, int64_t ldt,
+                                                          int64_t stride_a, int64_t stride_t) {
     __shared__ float tile[64][65];
+    A += int64_t(blockIdx.z) * stride_a;    // batch z
+    At += int64_t(blockIdx.z) * stride_t;
     const int64_t m0 = int64_t(blockIdx.y) * 64, k0 = int64_t(blockIdx.x) * 64;
     const int t = threadIdx.x;
     const int c4 = (t & 15) * 4;   // 4 consecutive columns of the tile
@@ -168,16 +174,19 @@ cudaError_t launch_ffma(const GemmArgs &a, int kernel, int tile, bool vec, bool 
 }
 
 cudaError_t launch_transpose(const float *A, int64_t M, int64_t K, int64_t lda, float *At,
-                             int64_t ldt, cudaStream_t stream) {
+                             int64_t ldt, cudaStream_t stream, int64_t batch, int64_t stride_a,
+                             int64_t stride_t) {
     const bool vec = (reinterpret_cast<uintptr_t>(A) & 15u) == 0 &&
                      (reinterpret_cast<uintptr_t>(At) & 15u) == 0 && lda % 4 == 0 &&
-                     ldt % 4 == 0 && ldt >= (M + 3) / 4 * 4;
+                     ldt % 4 == 0 && ldt >= (M + 3) / 4 * 4 && stride_a % 4 == 0 &&
+                     stride_t % 4 == 0;
     if (vec) {
-        const dim3 grid(unsigned((K + 63) / 64), unsigned((M + 63) / 64));
-        transpose64_kernel<<<grid, 256, 0, stream>>>(A, M, K, lda, At, ldt);
+        const dim3 grid(unsigned((K + 63) / 64), unsigned((M + 63) / 64), unsigned(batch));
+        transpose64_kernel<<<grid, 256, 0, stream>>>(A, M, K, lda, At, ldt, stride_a, stride_t);
     } else {
-        const dim3 grid(unsigned((K + 31) / 32), unsigned((M + 31) / 32));
-        transpose_kernel<<<grid, dim3(32, 8), 0, stream>>>(A, M, K, lda, At, ldt);
+        const dim3 grid(unsigned((K + 31) / 32), unsigned((M + 31) / 32), unsigned(batch));
+        transpose_kernel<<<grid, dim3(32, 8), 0, stream>>>(A, M, K, lda, At, ldt, stride_a,
+                                                          stride_t);
     }
     return cudaGetLastError();
 }

@@ -344,6 +344,44 @@ size_t transpose_workspace(const gemm_plan_t &p, int64_t M, int64_t K, int64_t *
     return *at_offset + transpose_bytes(M, K, ld);
 }
 
+// sgemm_ex's transposed copies: the same rule as choose_transpose_a, for each
+// operand to be copied (A's copy costs 8*M*K bytes against 2*M*N*K FLOPs, so
+// it needs N >= 1024; B's needs M >= 1024), on 128-wide one-CTA-per-tile
+// plans that fill the GPU (or split long K).
+bool ex_transpose_first(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int64_t batch,
+                        bool copy_a, bool copy_b, int sms) {
+    const bool able = p.schedule == 0 && p.bm == 128 && p.tail_split == 1 && p.vec &&
+                      batch <= 65535 && M <= int64_t(65535) * 32 && N <= int64_t(65535) * 32;
+    const int64_t tiles = p.tiles_m * p.tiles_n * batch;
+    bool want = able && K >= 256 && (!copy_a || N >= 1024) && (!copy_b || M >= 1024) &&
+                ((p.split_k == 1 && tiles >= sms) || (p.split_k > 1 && K >= 8192));
+    const int f = tuning(kKnobTransposeA);
+    if (f == 0) want = false;
+    if (f == 1) want = able;
+    return want;
+}
+
+// Re-plans a 128-wide one-CTA-per-(tile, K range) plan for the kernel that
+// copies both operands directly (op(A) = A^T, op(B) = B): K slices of 32
+// through a three-page ring, split-K chosen for that slice.
+void make_wide(gemm_plan_t &q, int64_t M, int64_t N, int64_t K, int64_t batch, int sms) {
+    q.bk = kWideBK;
+    q.stages = 3;
+    const int64_t tiles = q.tiles_m * q.tiles_n * batch;
+    int64_t kps = 0;
+    q.split_k = choose_split(tiles, K, sms, &kps, kWideBK, kCtasPerSm);
+    q.k_per_split = q.split_k > 1 ? kps : ceil_div(K, kWideBK) * kWideBK;
+    q.tail_split = 1;
+    q.tail_start = tiles;
+    q.tail_k_per_split = q.k_per_split;
+    q.grid_ctas = tiles * q.split_k;
+    q.edge = (q.vec && M % 128 == 0 && N % 128 == 0 && K % kWideBK == 0 &&
+              (q.split_k == 1 || K % q.k_per_split == 0))
+                 ? 0
+                 : 1;
+    q.workspace_bytes = split_workspace(tiles, q.split_k, q.tail_start, q.tail_split, 128);
+}
+
 sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                        int64_t ldc, const void *A, const void *B, const void *C,
                        int sms, gemm_plan_t *out, bool allow_transpose = true) {
@@ -360,19 +398,7 @@ sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb
             q.workspace_bytes = transpose_workspace(q, M, K, &q.a_t_ld, &at_offset);
             return SGEMM_OK;
         }
-        q.bk = kWideBK;
-        q.stages = 3;
-        const int64_t tiles = q.tiles_m * q.tiles_n;
-        int64_t kps = 0;
-        q.split_k = choose_split(tiles, K, sms, &kps, kWideBK, kCtasPerSm);
-        q.k_per_split = q.split_k > 1 ? kps : ceil_div(K, kWideBK) * kWideBK;
-        q.tail_start = tiles;
-        q.tail_k_per_split = q.k_per_split;
-        q.grid_ctas = tiles * q.split_k;
-        q.edge = (q.vec && M % 128 == 0 && N % 128 == 0 && K % kWideBK == 0 &&
-                  (q.split_k == 1 || K % q.k_per_split == 0))
-                     ? 0
-                     : 1;
+        make_wide(q, M, N, K, 1, sms);
         size_t at_offset = 0;
         q.workspace_bytes = transpose_workspace(q, M, K, &q.a_t_ld, &at_offset);
     }
@@ -518,7 +544,7 @@ sgemm_status run(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K, float
             e = launch_ffma_sk(sk_args(plan, a, workspace), plan.bm, plan.bk, plan.stages,
                                plan.vec != 0, true, false, false, stream);
         else
-            e = launch_ffma_tn_wide(a, plan.vec != 0, plan.edge != 0, stream);
+            e = launch_ffma_tn_wide(a, plan.vec != 0, plan.edge != 0, false, stream);
         return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
     }
     if (plan.schedule == 1) {
@@ -900,6 +926,32 @@ extern "C" sgemm_status sgemm_ex(int32_t op_a, int32_t op_b, int64_t M, int64_t 
     gemm_plan_t plan;
     plan_core(M, N, K, batch, vec, sms, &plan, ta && !tb);
     if (ta || tb) plan.kernel = kKernelFfma128;   // the packed form exists for op N, N only
+    // Large grids: the operands whose stored rows run along K (A as given,
+    // B^T) are first copied transposed into the workspace, so the product
+    // runs with both operands copied directly, in K slices of 32 -- what
+    // sgemm does for A.  Layout: [counters][split-K partials][A^T][B].
+    // (op T/N needs no copy, only the longer K slice.)
+    const bool copy_a = !ta, copy_b = tb;
+    const bool pre = ex_transpose_first(plan, M, N, K, batch, copy_a, copy_b, sms);
+    int64_t lda_t = 0, ldb_t = 0, sa_t = 0, sb_t = 0;
+    size_t a_off = 0, b_off = 0;
+    if (pre) {
+        make_wide(plan, M, N, K, batch, sms);
+        size_t off = std::max<size_t>(plan.workspace_bytes, kCounterBytes);
+        if (copy_a) {
+            lda_t = (M + 3) / 4 * 4;
+            sa_t = stride_a ? K * lda_t : 0;
+            a_off = off;
+            off += (size_t(stride_a ? batch : 1) * K * lda_t * sizeof(float) + 255) / 256 * 256;
+        }
+        if (copy_b) {
+            ldb_t = (N + 3) / 4 * 4;
+            sb_t = stride_b ? K * ldb_t : 0;
+            b_off = off;
+            off += (size_t(stride_b ? batch : 1) * K * ldb_t * sizeof(float) + 255) / 256 * 256;
+        }
+        plan.workspace_bytes = off;
+    }
     void *ws = nullptr;
     if (plan.workspace_bytes > 0) {
         s = library_workspace(dev, st, plan.workspace_bytes, &ws);
@@ -942,6 +994,30 @@ extern "C" sgemm_status sgemm_ex(int32_t op_a, int32_t op_b, int64_t M, int64_t 
         const bool ext = batch > 1 || bias != nullptr || act != SGEMM_ACT_NONE;
         e = launch_ffma_sk(sk_args(plan, a, ws), plan.bm, plan.bk, plan.stages, plan.vec != 0,
                            ta, tb, ext, st);
+        return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
+    }
+    if (pre) {
+        char *base = static_cast<char *>(ws);
+        if (copy_a) {
+            float *at = reinterpret_cast<float *>(base + a_off);
+            e = launch_transpose(A, M, K, lda, at, lda_t, st, stride_a ? batch : 1, stride_a,
+                                 sa_t);
+            if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
+            a.A = at;
+            a.lda = lda_t;
+            a.strideA = sa_t;
+        }
+        if (copy_b) {
+            float *bt = reinterpret_cast<float *>(base + b_off);
+            e = launch_transpose(B, N, K, ldb, bt, ldb_t, st, stride_b ? batch : 1, stride_b,
+                                 sb_t);
+            if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
+            a.B = bt;
+            a.ldb = ldb_t;
+            a.strideB = sb_t;
+        }
+        const bool ext = batch > 1 || bias != nullptr || act != SGEMM_ACT_NONE;
+        e = launch_ffma_tn_wide(a, plan.vec != 0, plan.edge != 0, ext, st);
         return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
     }
     e = launch_ffma(a, plan.kernel, plan.bm, plan.vec != 0, plan.edge != 0, ta, tb, st);

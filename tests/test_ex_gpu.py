@@ -32,7 +32,7 @@ def sg():
 
 class ExProblem:
     def __init__(self, op_a, op_b, M, N, K, batch, *, seed, dist="uniform", alpha=1.0, beta=0.0,
-                 bias=False, act=0, pad=3, shared_b=False):
+                 bias=False, act=0, pad=3, shared_b=False, aligned=False):
         rng = np.random.default_rng(seed)
         draw = (lambda s: rng.integers(-4, 5, s).astype(np.float32)) if dist == "int4" else \
             (lambda s: rng.uniform(-1, 1, s).astype(np.float32))
@@ -40,10 +40,17 @@ class ExProblem:
         self.alpha, self.beta, self.act = alpha, beta, act
         ra, ca = (K, M) if op_a else (M, K)
         rb, cb = (N, K) if op_b else (K, N)
-        self.lda, self.ldb, self.ldc = ca + pad, cb + pad, N + pad
-        self.sa = ra * self.lda + 5
-        self.sb = 0 if shared_b else rb * self.ldb + 7
-        self.sc = M * self.ldc + 2
+        if aligned:   # every row and batch starts on 16 bytes (the vector paths)
+            up = lambda x: (x + 3) // 4 * 4
+            self.lda, self.ldb, self.ldc = up(ca) + pad, up(cb) + pad, up(N) + pad
+            self.sa = ra * self.lda
+            self.sb = 0 if shared_b else rb * self.ldb
+            self.sc = M * self.ldc
+        else:
+            self.lda, self.ldb, self.ldc = ca + pad, cb + pad, N + pad
+            self.sa = ra * self.lda + 5
+            self.sb = 0 if shared_b else rb * self.ldb + 7
+            self.sc = M * self.ldc + 2
         self.A = np.full(self.sa * batch + 8, SENTINEL, np.float32)
         self.B = np.full(max(self.sb * batch, rb * self.ldb) + 8, SENTINEL, np.float32)
         self.C0 = np.full(self.sc * batch + 8, SENTINEL, np.float32)
@@ -210,3 +217,22 @@ def test_torch_matmul_api(sg):
                           40, 0, 0.0, None, 50, 64 * 50, 3, bias.cpu().numpy(), 1)
     assert C.shape == (3, 64, 50)
     assert float((C.cpu() - torch.from_numpy(ref)).abs().max()) <= 1e-6 * (40 * 0.25 + 0.5)
+
+
+@pytest.mark.parametrize("op_a,op_b", LAYOUTS)
+@pytest.mark.parametrize("batch,shared_b", [(1, False), (3, False), (2, True)])
+def test_transposed_copies_first(sg, tune, op_a, op_b, batch, shared_b):
+    """Operands whose rows run along K copied transposed into the workspace
+    (forced here), then the product with both operands copied directly --
+    batched, with a shared B, bias and GELU, ragged and exact."""
+    tune(transpose_a=1, tile=128, schedule=0)
+    p = ExProblem(op_a, op_b, 300, 260, 530, batch, seed=61 + batch, alpha=0.75, beta=0.5,
+                  bias=True, act=1, pad=4, shared_b=shared_b, aligned=True)
+    p.check(p.run(sg), exact=False)
+    q = ExProblem(op_a, op_b, 256, 384, 256, batch, seed=71 + batch, dist="int4", alpha=1.5,
+                  beta=0.5, bias=True, pad=0, shared_b=shared_b, aligned=True)
+    q.check(q.run(sg), exact=True)
+    r = ExProblem(op_a, op_b, 128, 129, 1001, batch, seed=81 + batch, pad=4, shared_b=shared_b,
+                  aligned=True)
+    tune(split_k=3)   # split-K on the copies too
+    r.check(r.run(sg), exact=False)
