@@ -41,4 +41,24 @@ cudaError_t launch_ffma_tn_wide(const GemmArgs &a, bool vec, bool edge, bool ext
                : launch_tn_wide<false>(a, vec, edge, stream);
 }
 
+// The same kernel scheduled as a persistent stream-K launch (kSched = 1).
+template <bool kExt>
+cudaError_t launch_tn_wide_sk(const GemmArgs &a, int64_t grid, bool vec, bool edge,
+                              cudaStream_t stream) {
+    if (!edge)
+        return ffma::launch_variant<128, false, true, false, false, true, false, kExt, kWideBK, 1>(
+            a, stream, grid);
+    if (vec)
+        return ffma::launch_variant<128, false, true, true, false, true, false, kExt, kWideBK, 1>(
+            a, stream, grid);
+    return ffma::launch_variant<128, false, false, true, false, true, false, kExt, kWideBK, 1>(
+        a, stream, grid);
+}
+
+cudaError_t launch_ffma_tn_wide_sk(const GemmArgs &a, int64_t grid, bool vec, bool edge, bool ext,
+                                   cudaStream_t stream) {
+    return ext ? launch_tn_wide_sk<true>(a, grid, vec, edge, stream)
+               : launch_tn_wide_sk<false>(a, grid, vec, edge, stream);
+}
+
 }  // namespace sgemm_impl

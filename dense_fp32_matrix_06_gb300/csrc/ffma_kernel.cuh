@@ -192,10 +192,40 @@ __device__ __forceinline__ WorkItem work_item(const GemmArgs &p, int64_t pid, in
     return w;
 }
 
+// Batch and first row/column of global tile `tile` (the grouped raster of
+// work_item), for the stream-K segments.
+__device__ __forceinline__ WorkItem tile_item(const GemmArgs &p, int64_t tile, int tsize) {
+    WorkItem w;
+    w.tile = tile;
+    const int64_t per_batch = int64_t(p.tiles_m) * p.tiles_n;
+    w.batch = tile / per_batch;
+    const int64_t t = tile - w.batch * per_batch;
+    const int64_t per_group = int64_t(kGroupM) * p.tiles_n;
+    const int64_t group = t / per_group;
+    const int64_t first_m = group * kGroupM;
+    const int64_t gm = min(int64_t(p.tiles_m) - first_m, int64_t(kGroupM));
+    const int64_t in_group = t - group * per_group;
+    w.row0 = (first_m + in_group % gm) * tsize;
+    w.col0 = (in_group / gm) * tsize;
+    w.kbeg = w.kend = 0;
+    w.split = 0;
+    w.nsplit = 1;
+    return w;
+}
+
 // kExt: batches, bias and activation are compiled in (sgemm_ex); the plain
 // product (sgemm) is built without them, which leaves it more registers.
+// kSched = 1: a persistent stream-K launch -- each CTA loops over the
+// segments (tile, K slices) of its share of the work, with the same main
+// loop; a tile whose slices several CTAs computed is summed, in ascending
+// CTA order, by the last of them to finish (see ffma_sk_kernel.cuh for the
+// decomposition).  Measured on GB300 the persistent form of this very loop
+// issues less well than the one-CTA-per-tile grid (ncu at 4096^3, A^T
+// plan: issue slots 75.9 % against 90.0 % busy, dispatch stalls 0.56
+// against 0.28 per issue, the same 128 registers and instruction count),
+// so the planner keeps it to few-tile, long-K shapes where balance wins.
 template <int kTile, bool kPacked, bool kVec, bool kEdge, bool kSplit, bool kTransA,
-          bool kTransB, bool kExt, int kBKT = kTile / 8>
+          bool kTransB, bool kExt, int kBKT = kTile / 8, int kSched = 0>
 __global__ void __launch_bounds__(TileCfg<kTile, kBKT>::kThreads,
                                   TileCfg<kTile, kBKT>::kMinBlocks)
 ffma_gemm_kernel(const GemmArgs p) {
@@ -225,17 +255,66 @@ ffma_gemm_kernel(const GemmArgs p) {
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
+    // stream-K segment state (kSched = 1), advanced by thread 0 between two
+    // barriers so it occupies no registers across the main loop
+    __shared__ long long s_sk_it, s_sk_tile;
+    __shared__ int s_sk_round, s_sk_k0, s_sk_k1, s_sk_first, s_sk_done;
+    if constexpr (kSched == 1) {
+        if (tid == 0) {
+            s_sk_round = 0;
+            s_sk_it = (long long)(int64_t(blockIdx.x) * p.sk_iters / gridDim.x);
+        }
+    }
+
+    for (;;) {   // one pass unless kSched == 1
     // ---- (batch, tile, K range) of this CTA; recomputed after the main loop
     // so none of it stays live in registers across it ----
     int64_t row0, col0, kbeg, kend;
     const float *Ab;
     const float *Bb;
-    {
+    if constexpr (kSched == 0) {
         const WorkItem w = work_item(p, blockIdx.x, T);
         row0 = w.row0;
         col0 = w.col0;
         kbeg = w.kbeg;
         kend = w.kend;
+        Ab = kExt ? p.A + w.batch * p.strideA : p.A;
+        Bb = kExt ? p.B + w.batch * p.strideB : p.B;
+    } else {
+        __syncthreads();   // everyone is done with the previous segment
+        if (tid == 0) {
+            const int G = gridDim.x, g = blockIdx.x;
+            const int64_t U = p.sk_iters;
+            const int64_t b_g = int64_t(g + 1) * U / G;   // end of this CTA's run
+            const int64_t it = s_sk_it;
+            s_sk_done = 0;
+            if (s_sk_round < p.dp_rounds) {
+                s_sk_tile = (long long)(int64_t(s_sk_round) * G + g);
+                s_sk_k0 = 0;
+                s_sk_k1 = p.sk_kt;
+                s_sk_first = 0;
+                ++s_sk_round;
+            } else if (it < b_g) {
+                const int64_t lt = it / p.sk_kt;
+                const int k0 = int(it - lt * p.sk_kt);
+                const int64_t left = b_g - it;
+                const int k1 = left < int64_t(p.sk_kt - k0) ? k0 + int(left) : p.sk_kt;
+                s_sk_tile = (long long)(int64_t(p.dp_rounds) * G + lt);
+                s_sk_k0 = k0;
+                s_sk_k1 = k1;
+                s_sk_first = it == int64_t(g) * U / G;
+                s_sk_it = (long long)(it + (k1 - k0));
+            } else {
+                s_sk_done = 1;
+            }
+        }
+        __syncthreads();
+        if (s_sk_done) break;
+        const WorkItem w = tile_item(p, s_sk_tile, T);
+        row0 = w.row0;
+        col0 = w.col0;
+        kbeg = int64_t(s_sk_k0) * BK;
+        kend = min(p.K, int64_t(s_sk_k1) * BK);
         Ab = kExt ? p.A + w.batch * p.strideA : p.A;
         Bb = kExt ? p.B + w.batch * p.strideB : p.B;
     }
@@ -474,8 +553,68 @@ ffma_gemm_kernel(const GemmArgs p) {
         }
     }
 
+    // ---- stream-K fix-up: a shared tile's partials summed in CTA order ----
+    if constexpr (kSched == 1) {
+        if (s_sk_k0 != 0 || s_sk_k1 != p.sk_kt) {
+            const int G = gridDim.x, g = blockIdx.x;
+            const int64_t U = p.sk_iters;
+            const int64_t lt = int64_t(s_sk_tile) - int64_t(p.dp_rounds) * G;
+            const int64_t x0 = lt * p.sk_kt;   // first slice of the tile
+            // contributors: the largest h with h*U/G <= x0, to the largest
+            // with h*U/G <= x0 + kt - 1
+            const int64_t g_first = ((x0 + 1) * G - 1) / U;
+            const int64_t g_last = ((x0 + p.sk_kt) * G - 1) / U;
+            float4 *part = reinterpret_cast<float4 *>(p.partials);
+            // slot 2h: CTA h's first segment; 2h+1: its last one
+            float4 *mine = part + size_t(2 * g + (s_sk_first ? 0 : 1)) * 16 * NT;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int i = j >> 1, h = j & 1;
+                __stcg(mine + j * NT + tid,
+                       make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
+                                   acc[i][2 * h + 1].y));
+            }
+            __threadfence();
+            __syncthreads();
+            unsigned *counter = p.counters + lt;
+            if (tid == 0) {
+                const unsigned prev = atomicAdd(counter, 1u);
+                s_last = prev == unsigned(g_last - g_first);
+            }
+            __syncthreads();
+            if (!s_last) continue;
+            __threadfence();
+            const size_t slot0 = size_t(2 * g_first) + ((g_first * U) / G == x0 ? 0 : 1);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                for (int j = 8 * half; j < 8 * half + 8; ++j) {
+                    const int i = j >> 1, h = j & 1;
+                    const float4 v = __ldcg(part + slot0 * 16 * NT + j * NT + tid);
+                    acc[i][2 * h] = make_float2(v.x, v.y);
+                    acc[i][2 * h + 1] = make_float2(v.z, v.w);
+                }
+                for (int64_t c = g_first + 1; c <= g_last; ++c) {
+                    float4 v[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        v[j] = __ldcg(part + size_t(2 * c) * 16 * NT + (8 * half + j) * NT + tid);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int i = (8 * half + j) >> 1, h = j & 1;
+                        acc[i][2 * h].x += v[j].x;
+                        acc[i][2 * h].y += v[j].y;
+                        acc[i][2 * h + 1].x += v[j].z;
+                        acc[i][2 * h + 1].y += v[j].w;
+                    }
+                }
+            }
+            if (tid == 0) *counter = 0u;   // rearmed for the next launch
+        }
+    }
+
     // ---- split-K: last CTA of the tile reduces the partials in order ----
-    if constexpr (kSplit) {
+    if constexpr (kSplit && kSched == 0) {
         const WorkItem w = work_item(p, blockIdx.x, T);
         if (w.nsplit > 1) {
             const int S = w.nsplit;
@@ -539,7 +678,12 @@ ffma_gemm_kernel(const GemmArgs p) {
     // ---- epilogue: C = act(alpha * acc (+ beta * C_old) (+ bias)) ----
     const float alpha = p.alpha, beta = p.beta;
     float *Cb = p.C;
-    if (kExt && p.batch > 1) Cb += work_item(p, blockIdx.x, T).batch * p.strideC;
+    if (kExt && p.batch > 1) {
+        if constexpr (kSched == 1)
+            Cb += tile_item(p, s_sk_tile, T).batch * p.strideC;
+        else
+            Cb += work_item(p, blockIdx.x, T).batch * p.strideC;
+    }
     const float *bias = kExt ? p.bias : nullptr;
     const int act = kExt ? p.act : kActNone;
 #pragma unroll
@@ -587,14 +731,16 @@ ffma_gemm_kernel(const GemmArgs p) {
             }
         }
     }
+    if constexpr (kSched == 0) break;
+    }   // segment loop
 }
 
 template <int kTile, bool kPacked, bool kVec, bool kEdge, bool kSplit, bool kTransA,
-          bool kTransB, bool kExt, int kBKT = kTile / 8>
-cudaError_t launch_variant(const GemmArgs &a, cudaStream_t stream) {
+          bool kTransB, bool kExt, int kBKT = kTile / 8, int kSched = 0>
+cudaError_t launch_variant(const GemmArgs &a, cudaStream_t stream, int64_t sk_grid = 0) {
     using TC = TileCfg<kTile, kBKT>;
     auto kernel = ffma_gemm_kernel<kTile, kPacked, kVec, kEdge, kSplit, kTransA, kTransB, kExt,
-                                   kBKT>;
+                                   kBKT, kSched>;
     int dyn = 0;
     if constexpr (TC::kDynSmem) {
         static bool configured[64];
@@ -604,7 +750,9 @@ cudaError_t launch_variant(const GemmArgs &a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
     }
     const int64_t tiles = int64_t(a.tiles_m) * a.tiles_n * a.batch;
-    const dim3 grid(unsigned(a.tail_start * a.split_k + (tiles - a.tail_start) * a.tail_split),
+    const dim3 grid(kSched == 1 ? unsigned(sk_grid)
+                                : unsigned(a.tail_start * a.split_k +
+                                           (tiles - a.tail_start) * a.tail_split),
                     1, 1);
     kernel<<<grid, TC::kThreads, dyn, stream>>>(a);
     return cudaGetLastError();

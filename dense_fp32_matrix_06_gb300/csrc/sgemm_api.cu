@@ -187,7 +187,7 @@ int choose_tile(int64_t M, int64_t N, int64_t K, int64_t batch, int sms) {
 // time, and its broadcast operand pairs push the kernel past 128 registers).
 int32_t default_kernel() {
     const int k = tuning(kKnobKernel);
-    if (k == kKernelFfma128 || k == kKernelFfma2x128) return k;
+    if (k == kKernelFfma128 || k == kKernelFfma2x128) return k;   // (2: direct-copy plans only)
     return kKernelFfma128;
 }
 
@@ -207,7 +207,8 @@ int64_t sk_slots(int tile, int sms) {
 // are split into G equal runs, G being the resident CTA count, or fewer so
 // that a run keeps at least kKnobSkMinSlices slices and a tile is shared by
 // at most kSkMaxContrib runs.
-void plan_stream_k(gemm_plan_t &p, int64_t tiles, int64_t K, int sms, bool direct) {
+void plan_stream_k(gemm_plan_t &p, int64_t M, int64_t N, int64_t tiles, int64_t K, int sms,
+                   bool direct) {
     const int tile = p.bm;
     const int bk = sk_config_bk(tile, direct);
     const int64_t kt = ceil_div(K, bk);
@@ -235,7 +236,11 @@ void plan_stream_k(gemm_plan_t &p, int64_t tiles, int64_t K, int sms, bool direc
     p.tail_start = tiles;
     p.k_per_split = kt * bk;
     p.tail_k_per_split = p.k_per_split;
-    p.edge = 1;   // every tile is bounds-checked (the checks cost a few instructions a slice)
+    // direct 128-wide plans of whole tiles run unchecked; the others check
+    // every tile (a few instructions a slice)
+    p.edge = (direct && tile == 128 && p.vec && M % tile == 0 && N % tile == 0 && K % bk == 0)
+                 ? 0
+                 : 1;
     p.workspace_bytes =
         p.sk_iters > 0 ? kCounterBytes + size_t(2 * G) * tile * tile * sizeof(float) : 0;
 }
@@ -296,7 +301,7 @@ void plan_core(int64_t M, int64_t N, int64_t K, int64_t batch, bool vec, int sms
     p.workspace_bytes = split_workspace(tiles, p.split_k, p.tail_start, p.tail_split, tile);
     if (M > 0 && N > 0 && K > 0 && batch > 0 && K <= kSkMaxK &&
         choose_stream_k(tile, tiles, K, sms))
-        plan_stream_k(p, tiles, K, sms, direct);
+        plan_stream_k(p, M, N, tiles, K, sms, direct);
     *out = p;
 }
 
@@ -361,6 +366,15 @@ bool ex_transpose_first(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, i
     return want;
 }
 
+// Kernel of a plan whose operands both arrive by direct copies: the 16 x 8
+// per-thread kernel when the tuning knob kKnobKernel asks for it (= 2) and
+// the plan does not split K; the 8 x 8 kernel otherwise.
+int32_t choose_wide_kernel(const gemm_plan_t &q) {
+    const int32_t k = tuning(kKnobKernel);
+    if (k == kKernelFfma16x8 && q.split_k == 1 && q.tail_split == 1) return kKernelFfma16x8;
+    return kKernelFfma128;
+}
+
 // Re-plans a 128-wide one-CTA-per-(tile, K range) plan for the kernel that
 // copies both operands directly (op(A) = A^T, op(B) = B): K slices of 32
 // through a three-page ring, split-K chosen for that slice.
@@ -380,6 +394,7 @@ void make_wide(gemm_plan_t &q, int64_t M, int64_t N, int64_t K, int64_t batch, i
                  ? 0
                  : 1;
     q.workspace_bytes = split_workspace(tiles, q.split_k, q.tail_start, q.tail_split, 128);
+    q.kernel = choose_wide_kernel(q);
 }
 
 sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
@@ -393,7 +408,7 @@ sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb
         gemm_plan_t &q = *out;
         q.transpose_a = 1;
         if (q.schedule == 1) {
-            plan_stream_k(q, q.tiles_m * q.tiles_n, K, sms, true);
+            plan_stream_k(q, M, N, q.tiles_m * q.tiles_n, K, sms, true);
             size_t at_offset = 0;
             q.workspace_bytes = transpose_workspace(q, M, K, &q.a_t_ld, &at_offset);
             return SGEMM_OK;
@@ -453,6 +468,25 @@ sgemm_status library_workspace(int dev, cudaStream_t stream, size_t bytes, void 
     }
     *out = p;
     return SGEMM_OK;
+}
+
+// `a` with the stream-K fields of `plan` filled in, for a persistent launch
+// of ffma_gemm_kernel (the workspace holds the tile counters and partials).
+GemmArgs sk_gemm_args(const gemm_plan_t &plan, GemmArgs a, void *workspace) {
+    a.sk_kt = int32_t(ceil_div(a.K, plan.bk));
+    a.dp_rounds = plan.dp_rounds;
+    a.sk_iters = plan.sk_iters;
+    a.split_k = 1;
+    a.tail_split = 1;
+    a.tail_start = int64_t(plan.tiles_m) * plan.tiles_n * a.batch;
+    a.k_per_split = a.tail_k_per_split = int64_t(a.sk_kt) * plan.bk;
+    a.counters = nullptr;
+    a.partials = nullptr;
+    if (plan.sk_iters > 0) {
+        a.counters = static_cast<unsigned *>(workspace);
+        a.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + kCounterBytes);
+    }
+    return a;
 }
 
 // Launch arguments of a stream-K plan, from the operand fields of `a`.
@@ -541,8 +575,10 @@ sgemm_status run(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K, float
         a.A = at;
         a.lda = plan.a_t_ld;
         if (plan.schedule == 1)
-            e = launch_ffma_sk(sk_args(plan, a, workspace), plan.bm, plan.bk, plan.stages,
-                               plan.vec != 0, true, false, false, stream);
+            e = launch_ffma_tn_wide_sk(sk_gemm_args(plan, a, workspace), plan.grid_ctas,
+                                       plan.vec != 0, plan.edge != 0, false, stream);
+        else if (plan.kernel == kKernelFfma16x8)
+            e = launch_ffma16x8(a, plan.edge != 0, false, stream);
         else
             e = launch_ffma_tn_wide(a, plan.vec != 0, plan.edge != 0, false, stream);
         return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
@@ -560,7 +596,12 @@ sgemm_status run(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K, float
 bool plan_matches(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int64_t lda,
                   int64_t ldb, int64_t ldc, const void *A, const void *B, const void *C) {
     if (p.mode != SGEMM_MODE_FFMA) return false;
-    if (p.kernel != kKernelFfma128 && p.kernel != kKernelFfma2x128) return false;
+    if (p.kernel != kKernelFfma128 && p.kernel != kKernelFfma2x128 &&
+        p.kernel != kKernelFfma16x8)
+        return false;
+    if (p.kernel == kKernelFfma16x8 &&
+        (!p.transpose_a || p.schedule != 0 || p.split_k != 1 || p.tail_split != 1))
+        return false;
     const int t = p.bm;
     if ((t != 128 && t != kSmallTile) || p.bn != t || p.threads != (t / 8) * (t / 8))
         return false;
@@ -572,8 +613,11 @@ bool plan_matches(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int64_t
         // stream-K: whole-K rounds, then every run non-empty, every tile
         // shared by few enough runs, counters and partials inside the workspace
         const bool direct = p.transpose_a != 0;
-        if (p.bk != sk_config_bk(t, direct) || p.stages != sk_config_pages(t, direct) ||
-            p.edge != 1)
+        if (p.bk != sk_config_bk(t, direct) || p.stages != sk_config_pages(t, direct))
+            return false;
+        // unchecked tiles only where every tile is whole
+        if (p.edge != 1 && !(p.edge == 0 && direct && t == 128 && p.vec && M % t == 0 &&
+                             N % t == 0 && K % p.bk == 0))
             return false;
         if (p.split_k != 1 || p.tail_split != 1 || p.tail_start != tiles) return false;
         if (K <= 0) return p.sk_iters == 0 && p.dp_rounds == 0;
@@ -992,8 +1036,12 @@ extern "C" sgemm_status sgemm_ex(int32_t op_a, int32_t op_b, int64_t M, int64_t 
     }
     if (plan.schedule == 1) {
         const bool ext = batch > 1 || bias != nullptr || act != SGEMM_ACT_NONE;
-        e = launch_ffma_sk(sk_args(plan, a, ws), plan.bm, plan.bk, plan.stages, plan.vec != 0,
-                           ta, tb, ext, st);
+        if (ta && !tb && plan.bm == 128)   // both operands direct: the split-K kernel's loop
+            e = launch_ffma_tn_wide_sk(sk_gemm_args(plan, a, ws), plan.grid_ctas, plan.vec != 0,
+                                       plan.edge != 0, ext, st);
+        else
+            e = launch_ffma_sk(sk_args(plan, a, ws), plan.bm, plan.bk, plan.stages,
+                               plan.vec != 0, ta, tb, ext, st);
         return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
     }
     if (pre) {
@@ -1017,7 +1065,9 @@ extern "C" sgemm_status sgemm_ex(int32_t op_a, int32_t op_b, int64_t M, int64_t 
             a.strideB = sb_t;
         }
         const bool ext = batch > 1 || bias != nullptr || act != SGEMM_ACT_NONE;
-        e = launch_ffma_tn_wide(a, plan.vec != 0, plan.edge != 0, ext, st);
+        e = plan.kernel == kKernelFfma16x8
+                ? launch_ffma16x8(a, plan.edge != 0, ext, st)
+                : launch_ffma_tn_wide(a, plan.vec != 0, plan.edge != 0, ext, st);
         return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
     }
     e = launch_ffma(a, plan.kernel, plan.bm, plan.vec != 0, plan.edge != 0, ta, tb, st);

@@ -107,6 +107,12 @@ struct GemmArgs {
     int64_t part_base;
     unsigned *counters;    // zero on entry and exit
     float *partials;
+    // Persistent stream-K launches of ffma_gemm_kernel (kSched = 1; G =
+    // gridDim.x): whole-K tiles [0, dp_rounds * G) round-robin, then the
+    // sk_iters K slices (of sk_kt per tile) of the rest in G equal runs.
+    int32_t sk_kt;
+    int32_t dp_rounds;
+    int64_t sk_iters;
 };
 
 // Kernel ids a plan can name.
@@ -116,6 +122,7 @@ struct GemmArgs {
 enum KernelId : int32_t {
     kKernelFfma128 = 0,    // scalar fma.rn.f32
     kKernelFfma2x128 = 1,  // packed fma.rn.f32x2 (two FMAs per instruction)
+    kKernelFfma16x8 = 2,   // 16 x 8 accumulators per thread (operands copied directly)
 };
 
 // ---- persistent stream-K kernel (ffma_sk_kernel.cuh) ----
@@ -185,6 +192,13 @@ cudaError_t launch_ffma_tt(const GemmArgs &a, int tile, bool vec, bool edge, cud
 constexpr int kWideBK = 32;
 cudaError_t launch_ffma_tn_wide(const GemmArgs &a, bool vec, bool edge, bool ext,
                                 cudaStream_t stream);
+// The same kernel as a persistent stream-K launch of `grid` CTAs (the
+// stream-K fields of `a` set).
+cudaError_t launch_ffma_tn_wide_sk(const GemmArgs &a, int64_t grid, bool vec, bool edge, bool ext,
+                                   cudaStream_t stream);
+// The 16 x 8 per-thread kernel (ffma_wide.cu): op(A) = A^T, op(B) = B, 128
+// tiles, K slices of 32, no split.
+cudaError_t launch_ffma16x8(const GemmArgs &a, bool edge, bool ext, cudaStream_t stream);
 // At_b = A_b^T (K x M, row stride ldt) for b < batch, with A_b = A +
 // b*stride_a and At_b = At + b*stride_t; M <= 65535 * 32, batch <= 65535.
 cudaError_t launch_transpose(const float *A, int64_t M, int64_t K, int64_t lda, float *At,

@@ -25,7 +25,7 @@ constexpr KnobInfo kKnobs[kKnobCount] = {
     {"SGEMM_FORCE_SPLIT", 1, kMaxSplit},
     {"SGEMM_FORCE_TAIL", 0, kMaxSplit},
     {"SGEMM_FORCE_TILE", 64, 128},
-    {"SGEMM_FORCE_KERNEL", 0, 1},
+    {"SGEMM_FORCE_KERNEL", 0, 2},
     {"SGEMM_FORCE_TRANSPOSE_A", 0, 1},
     {"SGEMM_FFMA_EXT", 0, 1},
     {"SGEMM_TF32X3_FORCE_SPLIT", 1, 64},

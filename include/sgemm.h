@@ -88,7 +88,9 @@ typedef enum {
 typedef struct {
     int32_t mode;          /* sgemm_mode */
     int32_t kernel;        /* 0: scalar fp32 FMA issue, 1: packed fp32x2 FMA issue
-                              (same arithmetic and summation order) */
+                              (same arithmetic and summation order), 2: a 16 x 8
+                              block of accumulators per thread (128 threads a CTA;
+                              transpose_a plans without split-K only) */
     int32_t bm, bn, bk;    /* CTA tile (rows of C, columns of C, K slice) */
     int32_t threads;       /* threads per CTA */
     int32_t split_k;       /* K partitions of tiles [0, tail_start) (1 = none) */
@@ -347,7 +349,9 @@ typedef enum {
     SGEMM_TUNE_TAIL_SPLIT = 1,    /* SGEMM_FORCE_TAIL: K ranges of the tiles of the
                                      last partial wave, 0..32 (< 2: none) */
     SGEMM_TUNE_TILE = 2,          /* SGEMM_FORCE_TILE: CTA tile 64 or 128 */
-    SGEMM_TUNE_KERNEL = 3,        /* SGEMM_FORCE_KERNEL: 0 scalar, 1 packed FMA issue */
+    SGEMM_TUNE_KERNEL = 3,        /* SGEMM_FORCE_KERNEL: 0 scalar, 1 packed FMA issue,
+                                     2 the 16 x 8 per-thread kernel on plans that copy
+                                     both operands directly and do not split K */
     SGEMM_TUNE_TRANSPOSE_A = 4,   /* SGEMM_FORCE_TRANSPOSE_A: 0 never, 1 whenever able */
     SGEMM_TUNE_FFMA_EXT = 5,      /* SGEMM_FFMA_EXT: 0/1, which compiled build of the
                                      FFMA kernel runs plain products */

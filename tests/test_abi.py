@@ -269,7 +269,7 @@ def test_tuning_knobs_round_trip_and_range_checks(lib, tune):
     tune(tile=None)
     assert sg.get_tuning("tile") is None and plan(8192, 8192, 8192).bm == 128
     # out-of-range values and unknown knobs are refused, the knob is unchanged
-    for knob, bad in (("tile", 96), ("split_k", 0), ("split_k", 33), ("kernel", 2),
+    for knob, bad in (("tile", 96), ("split_k", 0), ("split_k", 33), ("kernel", 3),
                       ("transpose_a", 5), ("workspace_limit_mib", -3)):
         before = sg.get_tuning(knob)
         assert lib.sgemm_set_tuning(sg.TUNING_KNOBS[knob], bad) == 1

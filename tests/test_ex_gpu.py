@@ -236,3 +236,16 @@ def test_transposed_copies_first(sg, tune, op_a, op_b, batch, shared_b):
                   aligned=True)
     tune(split_k=3)   # split-K on the copies too
     r.check(r.run(sg), exact=False)
+
+
+@pytest.mark.parametrize("op_a,op_b", LAYOUTS)
+def test_sixteen_by_eight_kernel_ex(sg, tune, op_a, op_b):
+    """sgemm_ex's direct-copy plans on the 16 x 8 per-thread kernel (forced),
+    batched with bias and GELU, and exact on integers."""
+    tune(kernel=2, transpose_a=1, split_k=1, tile=128, schedule=0)
+    p = ExProblem(op_a, op_b, 300, 260, 530, 2, seed=91, alpha=0.75, beta=0.5, bias=True,
+                  act=1, pad=4, aligned=True)
+    p.check(p.run(sg), exact=False)
+    q = ExProblem(op_a, op_b, 256, 384, 256, 3, seed=92, dist="int4", alpha=1.5, beta=0.5,
+                  bias=True, pad=0, aligned=True, shared_b=True)
+    q.check(q.run(sg), exact=True)

@@ -446,3 +446,21 @@ def test_transposed_plan_falls_back_when_the_workspace_is_capped(sg, tune):
     assert e.value.status == 6
     torch.cuda.synchronize()
     assert np.array_equal(C2.cpu().numpy(), p.C0)
+
+
+@pytest.mark.parametrize("M,N,K,lds,dist", [
+    (2048, 1024, 512, None, "uniform"),
+    (2046, 1030, 515, (516, 1032, 1036), "uniform"),     # bounds-checked tiles
+    (1024, 1536, 768, None, "int4"),
+    (1000, 1100, 37, (40, 1104, 1100), "int4"),
+])
+def test_sixteen_by_eight_kernel(sg, tune, M, N, K, lds, dist):
+    """The 16 x 8 per-thread kernel on transposed-A plans (forced)."""
+    tune(kernel=2, transpose_a=1, split_k=1, tile=128, schedule=0)
+    lda, ldb, ldc = lds if lds else (None, None, None)
+    p = workloads.make(M, N, K, dist=dist, seed=67, lda=lda, ldb=ldb, ldc=ldc,
+                       alpha=1.5 if dist == "int4" else 0.75, beta=0.5,
+                       c0_dist="int4" if dist == "int4" else "uniform")
+    plan = sg.gemm_plan_for_sms(p.M, p.N, p.K, p.lda, p.ldb, p.ldc)
+    assert plan.transpose_a == 1 and plan.kernel == 2 and plan.bk == 32
+    run_and_check(sg, p, exact=dist == "int4")
