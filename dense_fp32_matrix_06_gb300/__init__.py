@@ -71,6 +71,7 @@ TUNING_KNOBS = {
     "schedule": 10,
     "sk_min_slices": 11,
     "sk_grid": 12,
+    "tf32x3_bn": 13,
 }
 OP_N, OP_T = 0, 1
 ACT_NONE, ACT_GELU_TANH = 0, 1

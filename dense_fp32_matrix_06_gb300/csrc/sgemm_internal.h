@@ -69,7 +69,8 @@ enum Knob : int32_t {
     kKnobSchedule = 10,      // 0 one CTA per (tile, K range), 1 persistent stream-K
     kKnobSkMinSlices = 11,   // stream-K: fewest K slices per CTA run
     kKnobSkGrid = 12,        // stream-K: resident CTAs (grids of under two waves)
-    kKnobCount = 13
+    kKnobTf32x3Bn = 13,      // tensor mode: tile columns 128 or 256
+    kKnobCount = 14
 };
 int32_t tuning(Knob k);
 
@@ -220,6 +221,7 @@ constexpr int64_t kTf32x3MaxK = int64_t(65535) * 32;
 // `split` K ranges (small grids), or only the tiles from tail_start on (the
 // last, partly filled wave) cut into `tail_split` ranges.
 struct Tf32x3Plan {
+    int bn = 256;             // tile columns (tile rows are 128)
     int split = 1;
     int tail_split = 1;
     int64_t tiles = 0;

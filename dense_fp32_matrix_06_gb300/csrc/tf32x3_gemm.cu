@@ -996,6 +996,22 @@ constexpr int kTcStages = 2;
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 }  // namespace
 
+// Tile columns: 256 (the MMA's widest N), or 128 -- twice the tiles, but
+// each A tile is split (in the kernel) twice as often per FLOP, so a
+// 128-wide CTA does barely more than half a 256-wide one's work per unit of
+// time (2048^3: 104 against 194 TFLOP/s).  128 pays only where 256-wide
+// tiles fill at most half the SMs and K is short enough that split-K cannot
+// make up for it.  Measured on GB300 (microseconds, 256 / 128): 256^3 27.3 /
+// 25.2, 1024^3 58.0 / 47.8 (split 2), 1023x777x513 60.1 / 44.7, GPT-2 QKV
+// 48.8 / 46.8, MLP-down 95.9 / 68.3; but 1024x1024x16384 232 / 331 and
+// MLP-up (96 tiles) 49.8 / 72.4.  The tuning knob kKnobTf32x3Bn overrides.
+int choose_tc_bn(int64_t M, int64_t N, int64_t K, int sms) {
+    if (const int f = tuning(kKnobTf32x3Bn); f == 128 || f == 256) return f;
+    const int64_t tiles256 = ((M + kTcBM - 1) / kTcBM) * ((N + 255) / 256);
+    const int64_t nkb = (K + kTcBK - 1) / kTcBK;
+    return (2 * tiles256 <= sms && nkb <= 96) ? 128 : kTcBN;
+}
+
 // K ranges per tile.  One CTA runs per SM, so a grid of fewer tiles than SMs
 // leaves SMs idle; cutting K fills them but costs a partial-tile write and
 // read per range plus a second pass of prologue and epilogue.  Measured on
@@ -1005,7 +1021,8 @@ size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 // 3-4 -- and lost everywhere else (1024^3, GPT-2 QKV/MLP-up, 2048^3, 4096^3).
 Tf32x3Plan tf32x3_plan(int64_t M, int64_t N, int64_t K, int sms) {
     Tf32x3Plan plan;
-    const int64_t tiles = ((M + kTcBM - 1) / kTcBM) * ((N + kTcBN - 1) / kTcBN);
+    plan.bn = choose_tc_bn(M, N, K, sms);
+    const int64_t tiles = ((M + kTcBM - 1) / kTcBM) * ((N + plan.bn - 1) / plan.bn);
     const int64_t nkb = (K + kTcBK - 1) / kTcBK;
     plan.tiles = tiles;
     plan.tail_start = tiles;
@@ -1018,7 +1035,9 @@ Tf32x3Plan tf32x3_plan(int64_t M, int64_t N, int64_t K, int sms) {
         }
     }
     if (tiles <= kMaxSplitTiles && 2 * tiles <= sms) {
-        int64_t sp = std::min<int64_t>(sms / tiles, nkb / 24);
+        // at least 24 K blocks a range on 256-wide tiles, 16 on 128-wide
+        // ones (1024^3, 128-wide: 56.0 us unsplit, 47.8 in two ranges of 16)
+        int64_t sp = std::min<int64_t>(sms / tiles, nkb / (plan.bn == 128 ? 16 : 24));
         sp = std::min<int64_t>(sp, 16);
         plan.split = sp > 1 ? int(sp) : 1;
         return plan;
@@ -1064,7 +1083,7 @@ size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, const Tf32x3Plan 
     const int64_t kp = (K + 3) / 4 * 4;
     const size_t a = fused ? 0 : 2 * round256(size_t(M) * kp * 4);
     const size_t b = packed_b ? 0 : tf32x3_packed_b_bytes(K, N);
-    const size_t parts = size_t(plan.partial_slots()) * kTcBM * kTcBN * 4;
+    const size_t parts = size_t(plan.partial_slots()) * kTcBM * plan.bn * 4;
     return a + b + parts;
 }
 
@@ -1098,7 +1117,7 @@ TcArgs make_args(float *C, int64_t ldc, int64_t M, int64_t N, int64_t K, float a
     a.alpha = alpha;
     a.beta = beta;
     a.tiles_m = int32_t((M + kTcBM - 1) / kTcBM);
-    a.tiles_n = int32_t((N + kTcBN - 1) / kTcBN);
+    a.tiles_n = int32_t((N + plan.bn - 1) / plan.bn);
     a.limit_ns = limit_ns;
     a.inject_stall = inject_stall;
     const int64_t nkb = (K + kTcBK - 1) / kTcBK;
@@ -1133,11 +1152,13 @@ cudaError_t launch_tf32x3_packed(const float *A, int64_t lda, const void *packed
     if (fused) {
         CUtensorMap am, bh, bl;
         if (!encode_kmajor(&am, A, M, K, lda, kTcBM) ||
-            !encode_kmajor(&bh, b_hi, N, K, kp, kTcBN) || !encode_kmajor(&bl, b_lo, N, K, kp, kTcBN))
+            !encode_kmajor(&bh, b_hi, N, K, kp, plan.bn) ||
+            !encode_kmajor(&bl, b_lo, N, K, kp, plan.bn))
             return cudaErrorInvalidValue;
         const TcArgs a = make_args(C, ldc, M, N, K, alpha, beta, counters,
                                    reinterpret_cast<float *>(w), plan, limit_ns, inject_stall);
-        return launch_fused<kTcBN, kTcStages>(am, bh, bl, a, stream);
+        return plan.bn == 128 ? launch_fused<128, kTcStages>(am, bh, bl, a, stream)
+                              : launch_fused<kTcBN, kTcStages>(am, bh, bl, a, stream);
     }
     const size_t abytes = round256(size_t(M) * kp * 4);
     float *a_hi = reinterpret_cast<float *>(w);
@@ -1150,18 +1171,19 @@ cudaError_t launch_tf32x3_packed(const float *A, int64_t lda, const void *packed
     if (e != cudaSuccess) return e;
     CUtensorMap ah, al, bh, bl;
     if (!encode_kmajor(&ah, a_hi, M, K, kp, kTcBM) || !encode_kmajor(&al, a_lo, M, K, kp, kTcBM) ||
-        !encode_kmajor(&bh, b_hi, N, K, kp, kTcBN) || !encode_kmajor(&bl, b_lo, N, K, kp, kTcBN))
+        !encode_kmajor(&bh, b_hi, N, K, kp, plan.bn) || !encode_kmajor(&bl, b_lo, N, K, kp, plan.bn))
         return cudaErrorInvalidValue;
     const TcArgs a = make_args(C, ldc, M, N, K, alpha, beta, counters, parts, plan, limit_ns,
                                inject_stall);
-    return launch_mma<kTcBN, kTcStages>(ah, al, bh, bl, a, stream);
+    return plan.bn == 128 ? launch_mma<128, kTcStages>(ah, al, bh, bl, a, stream)
+                          : launch_mma<kTcBN, kTcStages>(ah, al, bh, bl, a, stream);
 }
 
 cudaError_t launch_tf32x3(const float *A, int64_t lda, const float *B, int64_t ldb, float *C,
                           int64_t ldc, int64_t M, int64_t N, int64_t K, float alpha, float beta,
                           void *workspace, unsigned *counters, const Tf32x3Plan &plan,
                           uint64_t limit_ns, int inject_stall, cudaStream_t stream) {
-    constexpr int BN = kTcBN, STAGES = kTcStages;
+    constexpr int STAGES = kTcStages;
     const int64_t kp = (K + 3) / 4 * 4;
     char *w = static_cast<char *>(workspace);
     if (tf32x3_use_fused_a(A, lda)) {
@@ -1191,11 +1213,12 @@ cudaError_t launch_tf32x3(const float *A, int64_t lda, const float *B, int64_t l
 
     CUtensorMap ah, al, bh, bl;
     if (!encode_kmajor(&ah, a_hi, M, K, kp, kTcBM) || !encode_kmajor(&al, a_lo, M, K, kp, kTcBM) ||
-        !encode_kmajor(&bh, b_hi, N, K, kp, BN) || !encode_kmajor(&bl, b_lo, N, K, kp, BN))
+        !encode_kmajor(&bh, b_hi, N, K, kp, plan.bn) || !encode_kmajor(&bl, b_lo, N, K, kp, plan.bn))
         return cudaErrorInvalidValue;
     const TcArgs a = make_args(C, ldc, M, N, K, alpha, beta, counters, parts, plan, limit_ns,
                                inject_stall);
-    return launch_mma<BN, STAGES>(ah, al, bh, bl, a, stream);
+    return plan.bn == 128 ? launch_mma<128, STAGES>(ah, al, bh, bl, a, stream)
+                          : launch_mma<kTcBN, STAGES>(ah, al, bh, bl, a, stream);
 }
 
 cudaError_t tf32x3_read_error(unsigned *out, cudaStream_t stream) {

@@ -35,12 +35,14 @@ constexpr KnobInfo kKnobs[kKnobCount] = {
     {"SGEMM_SCHEDULE", 0, 1},
     {"SGEMM_SK_MIN_SLICES", 1, 1 << 20},
     {"SGEMM_SK_GRID", 1, 1 << 20},
+    {"SGEMM_TF32X3_BN", 128, 256},
 };
 
 bool valid(int k, int32_t v) {
     if (v == -1) return true;
     if (v < kKnobs[k].lo || v > kKnobs[k].hi) return false;
     if (k == kKnobTile) return v == 64 || v == 128;
+    if (k == kKnobTf32x3Bn) return v == 128 || v == 256;
     return true;
 }
 

@@ -365,8 +365,9 @@ typedef enum {
                                      1 persistent stream-K (see gemm_plan_t.schedule) */
     SGEMM_TUNE_SK_MIN_SLICES = 11, /* SGEMM_SK_MIN_SLICES: stream-K, fewest K slices in
                                      one CTA's run (1..2^20) */
-    SGEMM_TUNE_SK_GRID = 12       /* SGEMM_SK_GRID: stream-K, CTAs of a grid of under two
+    SGEMM_TUNE_SK_GRID = 12,      /* SGEMM_SK_GRID: stream-K, CTAs of a grid of under two
                                      waves of tiles (1..2^20) */
+    SGEMM_TUNE_TF32X3_BN = 13     /* SGEMM_TF32X3_BN: tensor mode, tile columns 128 or 256 */
 } sgemm_tuning_knob;
 
 /* Sets a knob (value -1 restores the planner's choice).  Returns

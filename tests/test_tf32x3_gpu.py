@@ -326,3 +326,18 @@ def test_torch_api(sg):
     check(p, C.cpu().numpy(), exact=False)
     with pytest.raises(ValueError):
         sg.sgemm_tf32x3(A, B[:-1])
+
+
+@pytest.mark.parametrize("fuse", ["0", "1"])
+@pytest.mark.parametrize("split", [None, "3"])
+@pytest.mark.parametrize("M,N,K,dist", [
+    (1024, 2304, 768, "gpt2"), (1023, 777, 513, "uniform"), (300, 260, 1000, "int4"),
+    (129, 257, 31, "uniform"), (1024, 768, 3072, "int4"),
+])
+def test_narrow_tiles(sg, tune, M, N, K, dist, split, fuse):
+    """128-wide tensor tiles (forced): A split in the kernel and by a pre-pass,
+    with and without split-K."""
+    tune(tf32x3_bn=128, tf32x3_split=split, tf32x3_fuse_a=fuse)
+    p = workloads.make(M, N, K, dist=dist, seed=M + K, alpha=1.5 if dist == "int4" else 0.75,
+                       beta=0.5, c0_dist="int4" if dist == "int4" else "uniform")
+    check(p, run(sg, p, c_offset=1), exact=dist == "int4")
