@@ -256,7 +256,7 @@ void plan_stream_k(gemm_plan_t &p, int64_t M, int64_t N, int64_t tiles, int64_t 
 // eats what the even split gains.  The tuning knob kKnobSchedule overrides.
 bool choose_stream_k(int tile, int64_t tiles, int64_t K, int sms) {
     const int32_t force = tuning(kKnobSchedule);
-    if (force == 0 || force == 1) return force == 1;
+    if (force == 0 || force == 1 || force == 2) return force == 1;
     if (tile == kSmallTile) return 4 * tiles < sms;
     return 2 * tiles <= sms && K >= 8192;
 }
@@ -397,12 +397,56 @@ void make_wide(gemm_plan_t &q, int64_t M, int64_t N, int64_t K, int64_t batch, i
     q.kernel = choose_wide_kernel(q);
 }
 
+// The small-problem kernel: 32 x 32 tiles with the whole K range (<= 256)
+// staged in one go and split across the CTA's warps.  Chosen for products of
+// at most 2^25 multiply-adds whose 32 x 32 tiles fit in one wave (three CTAs
+// per SM), where the tiled kernels wait on loads and split-K round trips
+// rather than compute.  Measured on GB300 (microseconds, L2 flushed, small
+// kernel / tiled): 256^3 10.9 / 21.1, 512x512x128 10.9 / 17.1, 256x1024x128
+// 10.9 / 19.1, 128x128x256 10.9 / 19.1; but 1024x1024x32 (1024 tiles) 13.0 /
+// 10.9.  The tuning knob kKnobSchedule = 2 forces it (when K allows), 0 or 1
+// rule it out.
+bool choose_tiny(int64_t M, int64_t N, int64_t K, int sms) {
+    if (K < 1 || K > kTinyMaxK) return false;
+    const int32_t force = tuning(kKnobSchedule);
+    if (force >= 0) return force == 2;
+    return M * N * K <= (int64_t(1) << 25) && ceil_div(M, 32) * ceil_div(N, 32) <= 3 * sms;
+}
+
+void plan_tiny(gemm_plan_t &p, int64_t M, int64_t N, int64_t K) {
+    const int64_t tiles_m = ceil_div(M, 32), tiles_n = ceil_div(N, 32);
+    const int64_t kp = 8 * (ceil_div(K, 32) * 4);
+    p.schedule = 2;
+    p.kernel = kKernelFfma128;
+    p.bm = p.bn = 32;
+    p.bk = int32_t(kp);
+    p.threads = 256;
+    p.stages = 1;
+    p.split_k = 1;
+    p.tail_split = 1;
+    p.tiles_m = tiles_m;
+    p.tiles_n = tiles_n;
+    p.tail_start = tiles_m * tiles_n;
+    p.k_per_split = p.tail_k_per_split = kp;
+    p.grid_ctas = tiles_m * tiles_n;
+    p.edge = 1;
+    p.dp_rounds = 0;
+    p.sk_iters = 0;
+    p.transpose_a = 0;
+    p.a_t_ld = 0;
+    p.workspace_bytes = 0;
+}
+
 sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                        int64_t ldc, const void *A, const void *B, const void *C,
                        int sms, gemm_plan_t *out, bool allow_transpose = true) {
     const bool vec = lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0 && aligned16(A) &&
                      aligned16(B) && aligned16(C);
     plan_core(M, N, K, 1, vec, sms, out);
+    if (M > 0 && N > 0 && choose_tiny(M, N, K, sms)) {
+        plan_tiny(*out, M, N, K);
+        return SGEMM_OK;
+    }
     if (allow_transpose && M > 0 && N > 0 && K > 0 && choose_transpose_a(*out, M, N, K, sms)) {
         // the product then runs with both operands copied by rows, in K slices of 32
         gemm_plan_t &q = *out;
@@ -565,6 +609,10 @@ sgemm_status run(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K, float
         a.counters = static_cast<unsigned *>(workspace);
         a.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + kCounterBytes);
     }
+    if (plan.schedule == 2) {
+        e = launch_ffma_tiny(a, plan.vec != 0, stream);
+        return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
+    }
     if (plan.transpose_a) {
         int64_t ld = 0;
         size_t at_offset = 0;
@@ -596,6 +644,18 @@ sgemm_status run(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K, float
 bool plan_matches(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int64_t lda,
                   int64_t ldb, int64_t ldc, const void *A, const void *B, const void *C) {
     if (p.mode != SGEMM_MODE_FFMA) return false;
+    if (p.schedule == 2) {
+        gemm_plan_t q;
+        std::memset(&q, 0, sizeof(q));
+        q.mode = p.mode;
+        q.vec = p.vec;
+        if (K < 1 || K > kTinyMaxK || M <= 0 || N <= 0) return false;
+        plan_tiny(q, M, N, K);
+        const bool vec_ok = lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0 && aligned16(A) &&
+                            aligned16(B) && aligned16(C);
+        if (p.vec && !vec_ok) return false;
+        return std::memcmp(&p, &q, sizeof(q)) == 0;
+    }
     if (p.kernel != kKernelFfma128 && p.kernel != kKernelFfma2x128 &&
         p.kernel != kKernelFfma16x8)
         return false;

@@ -66,7 +66,7 @@ enum Knob : int32_t {
     kKnobTf32x3Tail = 7,     // tensor mode: K ranges of the last partial wave
     kKnobTf32x3FuseA = 8,    // tensor mode: 0 forces the pre-pass split of A
     kKnobWorkspaceLimitMiB = 9,  // cap on each library-owned workspace
-    kKnobSchedule = 10,      // 0 one CTA per (tile, K range), 1 persistent stream-K
+    kKnobSchedule = 10,      // 0 one CTA per (tile, K range), 1 persistent stream-K, 2 small-problem kernel
     kKnobSkMinSlices = 11,   // stream-K: fewest K slices per CTA run
     kKnobSkGrid = 12,        // stream-K: resident CTAs (grids of under two waves)
     kKnobTf32x3Bn = 13,      // tensor mode: tile columns 128 or 256
@@ -197,6 +197,11 @@ cudaError_t launch_ffma_tn_wide(const GemmArgs &a, bool vec, bool edge, bool ext
 // stream-K fields of `a` set).
 cudaError_t launch_ffma_tn_wide_sk(const GemmArgs &a, int64_t grid, bool vec, bool edge, bool ext,
                                    cudaStream_t stream);
+// The small-problem kernel (ffma_tiny.cu): 32 x 32 tiles, the whole K range
+// (at most kTinyMaxK) staged at once, K split across the CTA's 8 warps.
+constexpr int64_t kTinyMaxK = 256;
+cudaError_t launch_ffma_tiny(const GemmArgs &a, bool vec, cudaStream_t stream);
+size_t tiny_smem_bytes(int64_t K);
 // The 16 x 8 per-thread kernel (ffma_wide.cu): op(A) = A^T, op(B) = B, 128
 // tiles, K slices of 32, no split.
 cudaError_t launch_ffma16x8(const GemmArgs &a, bool edge, bool ext, cudaStream_t stream);

@@ -32,7 +32,7 @@ constexpr KnobInfo kKnobs[kKnobCount] = {
     {"SGEMM_TF32X3_FORCE_TAIL", 0, 64},
     {"SGEMM_TF32X3_FUSE_A", 0, 1},
     {"SGEMM_WORKSPACE_LIMIT_MIB", 0, INT32_MAX},
-    {"SGEMM_SCHEDULE", 0, 1},
+    {"SGEMM_SCHEDULE", 0, 2},
     {"SGEMM_SK_MIN_SLICES", 1, 1 << 20},
     {"SGEMM_SK_GRID", 1, 1 << 20},
     {"SGEMM_TF32X3_BN", 128, 256},

@@ -119,7 +119,10 @@ typedef struct {
                               stream-K: grid_ctas CTAs stay resident, take whole-K
                               tiles round-robin for dp_rounds rounds, then split the
                               K slices of the remaining tiles into grid_ctas equal
-                              runs (split_k = tail_split = 1 then) */
+                              runs (split_k = tail_split = 1 then); 2: small
+                              problems (K <= 256): 32 x 32 tiles, 256 threads, the
+                              whole K range (bk, padded) staged at once and split
+                              across the CTA's 8 warps, no workspace */
     int32_t dp_rounds;     /* stream-K: rounds of whole-K tiles */
     int64_t sk_iters;      /* stream-K: K slices (of bk) of the tiles after the
                               dp_rounds * grid_ctas whole-K ones */
@@ -362,7 +365,8 @@ typedef enum {
                                      library-owned workspace; a larger request fails
                                      as a failed allocation would (SGEMM_ERR_ALLOC) */
     SGEMM_TUNE_SCHEDULE = 10,     /* SGEMM_SCHEDULE: 0 one CTA per (tile, K range),
-                                     1 persistent stream-K (see gemm_plan_t.schedule) */
+                                     1 persistent stream-K, 2 the small-problem kernel
+                                     where K <= 256 (see gemm_plan_t.schedule) */
     SGEMM_TUNE_SK_MIN_SLICES = 11, /* SGEMM_SK_MIN_SLICES: stream-K, fewest K slices in
                                      one CTA's run (1..2^20) */
     SGEMM_TUNE_SK_GRID = 12,      /* SGEMM_SK_GRID: stream-K, CTAs of a grid of under two

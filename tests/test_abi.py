@@ -169,6 +169,7 @@ def test_plan_ragged_shape_takes_the_checked_scalar_path(lib):
 
 
 def test_plan_tile_choice(lib, tune):
+    tune(schedule=0)   # the tiled kernels (small problems have their own kernel)
     assert plan(8192, 8192, 8192).bm == 128
     assert plan(1024, 2304, 768).bm == 128        # 144 tiles of 128
     assert plan(1024, 768, 3072).bm == 128        # 48 tiles of 128, but K is long
@@ -253,6 +254,7 @@ def test_forced_split_override(lib, tune):
 
 
 def test_forced_kernel_override(lib, tune):
+    tune(schedule=0)
     tune(tile="128")
     tune(kernel="0")
     assert plan(256, 256, 256).kernel == 0
@@ -300,7 +302,10 @@ def test_plan_schedule_choice(lib, tune):
     """Persistent stream-K where it measured faster: tiny grids of 64-wide
     tiles and few 128-wide tiles with long K; one CTA per (tile, K range)
     elsewhere."""
-    p = plan(256, 256, 256)
+    p = plan(256, 256, 256)          # 2^24 multiply-adds: the small-problem kernel
+    assert p.schedule == 2 and p.bm == 32 and p.bk == 256 and p.threads == 256
+    assert p.grid_ctas == 64 and p.workspace_bytes == 0
+    p = plan(64, 64, 1000)           # K too long for it: 64-wide stream-K
     assert p.schedule == 1 and p.bm == 64 and p.bk == 8 and p.stages == 4
     q = plan(1024, 1024, 16384)      # 64 tiles, K = 16384: A transposed, then stream-K
     assert q.schedule == 1 and q.transpose_a == 1 and q.bk == 32 and q.stages == 3
@@ -311,6 +316,24 @@ def test_plan_schedule_choice(lib, tune):
     assert plan(256, 256, 256).schedule == 0
     tune(schedule=1)
     assert plan(8192, 8192, 8192).schedule == 1
+    tune(schedule=2)
+    assert plan(2000, 3000, 256).schedule == 2       # forced where K allows
+    assert plan(2000, 3000, 257).schedule == 0
+
+
+def test_small_problem_plan_checks(lib, tune):
+    p = plan(100, 70, 33, lda=35, ldb=70, ldc=71)
+    assert p.schedule == 2 and p.vec == 0 and p.bk == 64 and p.tiles_m == 4 and p.tiles_n == 3
+    q = plan(256, 256, 256)
+    # a tampered plan is refused before the device is touched
+    for field, value in (("bk", 128), ("grid_ctas", 65), ("threads", 128), ("workspace_bytes", 64)):
+        r = sg.GemmPlan.from_buffer_copy(q)
+        setattr(r, field, value)
+        assert lib.sgemm_with_plan(ctypes.byref(r), 256, 256, 256, 1.0, 4096, 256, 4096, 256, 0.0,
+                                   4096, 256, None, 0, None) == 1, field
+    # a plan for another K
+    assert lib.sgemm_with_plan(ctypes.byref(q), 256, 256, 200, 1.0, 4096, 256, 4096, 256, 0.0,
+                               4096, 256, None, 0, None) == 1
 
 
 def test_stream_k_plan_round_trips_through_sgemm_with_plan_checks(lib, tune):

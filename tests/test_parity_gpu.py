@@ -135,8 +135,10 @@ def test_ragged_leading_dimensions_and_alpha_beta(sg):
     run_and_check(sg, p)
 
 
+@pytest.mark.parametrize("sched", [None, 0])   # as planned; the tiled kernels only
 @pytest.mark.parametrize("seed", range(24))
-def test_shape_fuzz(sg, seed):
+def test_shape_fuzz(sg, tune, seed, sched):
+    tune(schedule=sched)
     rng = np.random.default_rng(1000 + seed)
     M, N, K = (int(x) for x in rng.integers(1, 301, size=3))
     lda = K + int(rng.integers(0, 9))
@@ -154,9 +156,11 @@ def test_shape_fuzz(sg, seed):
     run_and_check(sg, p, exact=(dist == "int4"), **offs)
 
 
+@pytest.mark.parametrize("sched", [None, 0])
 @pytest.mark.parametrize("M,N,K", [(1, 1, 1), (1, 513, 17), (129, 1, 300), (128, 128, 16),
                                    (127, 129, 15), (256, 384, 1), (3, 5, 4096)])
-def test_edge_shapes(sg, M, N, K):
+def test_edge_shapes(sg, tune, M, N, K, sched):
+    tune(schedule=sched)
     p = workloads.make(M, N, K, seed=M + N + K)
     run_and_check(sg, p)
     q = workloads.make(M, N, K, dist="int4", seed=M + N + K)
@@ -238,7 +242,7 @@ def test_tail_split_parity(sg, tune, M, N, K, dist, lds):
 @pytest.mark.parametrize("tile", ["64", "128"])
 @pytest.mark.parametrize("name", ["square1024ab", "ragged", "gpt2_qkv", "square256_int"])
 def test_forced_tile(sg, tune, tile, name):
-    tune(tile=tile)
+    tune(tile=tile, schedule=0)
     p = workloads.workload(name)
     run_and_check(sg, p, exact=p.meta["dist"] == "int4")
 
@@ -464,3 +468,24 @@ def test_sixteen_by_eight_kernel(sg, tune, M, N, K, lds, dist):
     plan = sg.gemm_plan_for_sms(p.M, p.N, p.K, p.lda, p.ldb, p.ldc)
     assert plan.transpose_a == 1 and plan.kernel == 2 and plan.bk == 32
     run_and_check(sg, p, exact=dist == "int4")
+
+
+@pytest.mark.parametrize("M,N,K,lds,beta,dist", [
+    (256, 256, 256, None, 0.0, "uniform"),
+    (256, 256, 256, None, 0.5, "int4"),
+    (100, 70, 33, (35, 70, 71), 1.25, "uniform"),      # unaligned: 4-byte copies
+    (31, 33, 1, None, 0.0, "int4"),
+    (1000, 900, 256, (257, 903, 901), -0.5, "uniform"),
+    (64, 2000, 96, None, 0.0, "int4"),
+    (513, 7, 255, None, 2.0, "int4"),
+])
+def test_small_problem_kernel(sg, tune, M, N, K, lds, beta, dist):
+    """The small-problem kernel (forced where the planner would not pick it):
+    edges, unaligned operands, beta, exact integers, C's padding untouched."""
+    tune(schedule=2)
+    lda, ldb, ldc = lds if lds else (None, None, None)
+    p = workloads.make(M, N, K, dist=dist, seed=M + N + K, alpha=1.5 if dist == "int4" else 0.75,
+                       beta=beta, lda=lda, ldb=ldb, ldc=ldc,
+                       c0_dist=("int4" if dist == "int4" else "uniform") if beta else None)
+    assert sg.gemm_plan_for_sms(p.M, p.N, p.K, p.lda, p.ldb, p.ldc).schedule == 2
+    run_and_check(sg, p, exact=dist == "int4", c_offset=1 if lds else 0)
