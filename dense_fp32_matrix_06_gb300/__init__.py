@@ -513,8 +513,8 @@ def plan_for(A, B, C) -> GemmPlan:
 def sgemm_with_plan(plan: GemmPlan, A, B, C, alpha: float = 1.0, beta: float = 0.0,
                     workspace=None, stream=None):
     """sgemm_with_plan() on torch tensors; `workspace` is a CUDA uint8 tensor
-    (or None when plan.workspace_bytes == 0) whose first
-    WORKSPACE_COUNTER_BYTES bytes are zero before its first use."""
+    of at least plan.workspace_bytes bytes (or None when that is 0); its
+    contents need no initialisation."""
     import torch
     M, K = A.shape
     N = B.shape[1]

@@ -54,10 +54,9 @@
 //  * Split-K: when the tile grid cannot fill the GPU, K is cut into split_k
 //    ranges (and, opt-in, only the tiles of a partly filled last wave into
 //    tail_split ranges).  Every CTA of a split tile writes its partial tile
-//    to the workspace; the last CTA of the tile to arrive (atomic ticket, no
-//    waiting) sums all partials in ascending split order and runs the
-//    epilogue, then rearms the counter.  The sum order is fixed, so results
-//    are deterministic run to run.
+//    to the workspace; a second launch (partial_reduce_kernel) sums each
+//    tile's partials in ascending range order and runs the epilogue.  The
+//    sum order is fixed, so results are deterministic run to run.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -217,13 +216,15 @@ __device__ __forceinline__ WorkItem tile_item(const GemmArgs &p, int64_t tile, i
 // product (sgemm) is built without them, which leaves it more registers.
 // kSched = 1: a persistent stream-K launch -- each CTA loops over the
 // segments (tile, K slices) of its share of the work, with the same main
-// loop; a tile whose slices several CTAs computed is summed, in ascending
-// CTA order, by the last of them to finish (see ffma_sk_kernel.cuh for the
-// decomposition).  Measured on GB300 the persistent form of this very loop
-// issues less well than the one-CTA-per-tile grid (ncu at 4096^3, A^T
-// plan: issue slots 75.9 % against 90.0 % busy, dispatch stalls 0.56
-// against 0.28 per issue, the same 128 registers and instruction count),
-// so the planner keeps it to few-tile, long-K shapes where balance wins.
+// loop; a segment that is not a whole tile leaves its partial tile in the
+// workspace, and partial_reduce_kernel sums them in ascending CTA order after the
+// launch (see ffma_sk_kernel.cuh for the decomposition).  Measured on GB300
+// with the A^T plan, the persistent loop issues a little worse than the
+// one-tile-per-CTA grid (2048^3 with one whole tile per CTA: 351 against
+// 338 us); summing the partials inside the persistent kernel cost far more
+// (391 us, ncu at 4096^3: issue slots 75.9 % against 90.0 % busy, dispatch
+// stalls 0.56 against 0.28 per issue), which is why the sum is a second
+// launch.
 template <int kTile, bool kPacked, bool kVec, bool kEdge, bool kSplit, bool kTransA,
           bool kTransB, bool kExt, int kBKT = kTile / 8, int kSched = 0>
 __global__ void __launch_bounds__(TileCfg<kTile, kBKT>::kThreads,
@@ -242,7 +243,6 @@ ffma_gemm_kernel(const GemmArgs p) {
     constexpr int kStaticBK = TC::kDynSmem ? 1 : BK;
     __shared__ __align__(16) float sa[2][kStaticBK][T];
     __shared__ __align__(16) float sb[2][kStaticBK][T];
-    __shared__ int s_last;
     extern __shared__ __align__(16) float dyn_smem[];
     constexpr int NP = TC::kPages;
     static_assert(NP == 2 || TC::kDynSmem, "three pages only for the dynamic layout");
@@ -309,7 +309,11 @@ ffma_gemm_kernel(const GemmArgs p) {
             }
         }
         __syncthreads();
-        if (s_sk_done) break;
+        if (s_sk_done) {
+            // the reduction launch may be scheduled once every CTA is here
+            asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+            break;
+        }
         const WorkItem w = tile_item(p, s_sk_tile, T);
         row0 = w.row0;
         col0 = w.col0;
@@ -553,20 +557,13 @@ ffma_gemm_kernel(const GemmArgs p) {
         }
     }
 
-    // ---- stream-K fix-up: a shared tile's partials summed in CTA order ----
+    // ---- stream-K: a segment that is not a whole tile leaves its partial
+    // tile in this CTA's slot (2g for its run's first segment, 2g + 1 for
+    // its last) and moves on; partial_reduce_kernel sums the slots afterwards ----
     if constexpr (kSched == 1) {
         if (s_sk_k0 != 0 || s_sk_k1 != p.sk_kt) {
-            const int G = gridDim.x, g = blockIdx.x;
-            const int64_t U = p.sk_iters;
-            const int64_t lt = int64_t(s_sk_tile) - int64_t(p.dp_rounds) * G;
-            const int64_t x0 = lt * p.sk_kt;   // first slice of the tile
-            // contributors: the largest h with h*U/G <= x0, to the largest
-            // with h*U/G <= x0 + kt - 1
-            const int64_t g_first = ((x0 + 1) * G - 1) / U;
-            const int64_t g_last = ((x0 + p.sk_kt) * G - 1) / U;
-            float4 *part = reinterpret_cast<float4 *>(p.partials);
-            // slot 2h: CTA h's first segment; 2h+1: its last one
-            float4 *mine = part + size_t(2 * g + (s_sk_first ? 0 : 1)) * 16 * NT;
+            float4 *mine = reinterpret_cast<float4 *>(p.partials) +
+                           size_t(2 * blockIdx.x + (s_sk_first ? 0 : 1)) * 16 * NT;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int i = j >> 1, h = j & 1;
@@ -574,57 +571,20 @@ ffma_gemm_kernel(const GemmArgs p) {
                        make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
                                    acc[i][2 * h + 1].y));
             }
-            __threadfence();
-            __syncthreads();
-            unsigned *counter = p.counters + lt;
-            if (tid == 0) {
-                const unsigned prev = atomicAdd(counter, 1u);
-                s_last = prev == unsigned(g_last - g_first);
-            }
-            __syncthreads();
-            if (!s_last) continue;
-            __threadfence();
-            const size_t slot0 = size_t(2 * g_first) + ((g_first * U) / G == x0 ? 0 : 1);
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-#pragma unroll
-                for (int j = 8 * half; j < 8 * half + 8; ++j) {
-                    const int i = j >> 1, h = j & 1;
-                    const float4 v = __ldcg(part + slot0 * 16 * NT + j * NT + tid);
-                    acc[i][2 * h] = make_float2(v.x, v.y);
-                    acc[i][2 * h + 1] = make_float2(v.z, v.w);
-                }
-                for (int64_t c = g_first + 1; c <= g_last; ++c) {
-                    float4 v[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        v[j] = __ldcg(part + size_t(2 * c) * 16 * NT + (8 * half + j) * NT + tid);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int i = (8 * half + j) >> 1, h = j & 1;
-                        acc[i][2 * h].x += v[j].x;
-                        acc[i][2 * h].y += v[j].y;
-                        acc[i][2 * h + 1].x += v[j].z;
-                        acc[i][2 * h + 1].y += v[j].w;
-                    }
-                }
-            }
-            if (tid == 0) *counter = 0u;   // rearmed for the next launch
+            continue;
         }
     }
 
-    // ---- split-K: last CTA of the tile reduces the partials in order ----
+    // ---- split-K: a CTA of a split tile leaves its partial tile in its
+    // slot (the tile's ranges own consecutive slots) and is done;
+    // partial_reduce_kernel sums each tile's slots in range order ----
     if constexpr (kSplit && kSched == 0) {
+        // the reduction launch may be scheduled once every CTA is here
+        asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
         const WorkItem w = work_item(p, blockIdx.x, T);
         if (w.nsplit > 1) {
-            const int S = w.nsplit;
-            const int split = w.split;
-            const int64_t pid = blockIdx.x;
-            float4 *part = reinterpret_cast<float4 *>(p.partials);
-            // slots of this tile's ranges are consecutive, starting at pid - split
-            const size_t tile_base = size_t(pid - split - p.part_base) * 16 * NT;
-            float4 *mine = part + tile_base + size_t(split) * 16 * NT;
-            unsigned *counter = p.counters + (w.tile - p.split_base);
+            float4 *mine = reinterpret_cast<float4 *>(p.partials) +
+                           size_t(int64_t(blockIdx.x) - p.part_base) * 16 * NT;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int i = j >> 1, h = j & 1;
@@ -632,46 +592,7 @@ ffma_gemm_kernel(const GemmArgs p) {
                        make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
                                    acc[i][2 * h + 1].y));
             }
-            __threadfence();
-            __syncthreads();
-            if (tid == 0) {
-                const unsigned prev = atomicAdd(counter, 1u);
-                s_last = (prev == unsigned(S - 1));
-            }
-            __syncthreads();
-            if (!s_last) return;
-            __threadfence();
-            // every partial, this CTA's own included, is read back from the
-            // workspace (each thread reads only what it wrote itself or what
-            // the fence and ticket made visible), so the sum order is the
-            // same whichever CTA arrives last.  Half a tile at a time with a
-            // partial's eight loads in flight together: 2S L2 round trips
-            // rather than 16S.
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-#pragma unroll
-                for (int j = 8 * half; j < 8 * half + 8; ++j) {
-                    const int i = j >> 1, h = j & 1;
-                    acc[i][2 * h] = make_float2(0.0f, 0.0f);
-                    acc[i][2 * h + 1] = make_float2(0.0f, 0.0f);
-                }
-                for (int s = 0; s < S; ++s) {
-                    float4 v[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        v[j] = __ldcg(part + tile_base + size_t(s) * 16 * NT +
-                                      (8 * half + j) * NT + tid);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int i = (8 * half + j) >> 1, h = j & 1;
-                        acc[i][2 * h].x += v[j].x;
-                        acc[i][2 * h].y += v[j].y;
-                        acc[i][2 * h + 1].x += v[j].z;
-                        acc[i][2 * h + 1].y += v[j].w;
-                    }
-                }
-            }
-            if (tid == 0) *counter = 0u;
+            return;
         }
     }
 
@@ -735,6 +656,207 @@ ffma_gemm_kernel(const GemmArgs p) {
     }   // segment loop
 }
 
+// What the reduction of partial tiles needs of a launch (filled from
+// GemmArgs or SkArgs by the product kernels' launchers).
+struct ReduceArgs {
+    const float *partials;   // partial tiles of (T/8)^2 * 16 float4 each
+    float *C;
+    const float *bias;
+    int64_t M, N, ldc, strideC;
+    float alpha, beta;
+    int32_t act;
+    int32_t tiles_m, tiles_n;
+    int64_t first_tile;      // global id of the first tile reduced
+    int64_t tiles;           // tiles reduced: first_tile .. first_tile + tiles - 1
+    // split-K (split > 1): tile first_tile + i sums slots i*split .. i*split + split - 1
+    int32_t split;
+    // stream-K (split == 0): the sk_iters K slices of the tiles, kt per tile,
+    // were cut into `grid` equal runs; run g left its first segment in slot
+    // 2g and its last in slot 2g + 1
+    int32_t kt;
+    int32_t grid;
+    int64_t sk_iters;
+};
+
+// The second half of a split-K or stream-K launch: for every tile whose K
+// range several CTAs shared, the sum of their partial tiles in K order and
+// the same epilogue as the product kernels.  Split-K: the tile's ranges in
+// ascending order.  Stream-K: the first contributor's slot (2g, or 2g + 1
+// when the tile does not start its run), then slot 2h of each later CTA h,
+// which holds that run's first segment.  Four CTAs per tile, each a quarter
+// of the accumulator rows with the product kernels' thread mapping, so a
+// thread reads back exactly the values one product thread stored; all of a
+// thread's loads of one contributor are in flight together.  A stream-K
+// tile that one CTA computed whole was stored by the product kernel; its
+// CTAs return at once.
+//
+// Summing in a second launch rather than in the product kernel's last CTA
+// to arrive keeps the product kernels' main loops as fast as the plain
+// grid's (measured on GB300, persistent stream-K with the A^T plan at
+// 2048^3: 324 us against 342 with the sum in the persistent kernel; ncu at
+// 4096^3 put the in-kernel version's issue slots at 75.9 % busy against
+// 90.0 %, with twice the dispatch stalls), and the reduction runs on every
+// SM at once instead of on one CTA per tile after all the others.
+template <int kTile, bool kVec, bool kEdge, bool kExt>
+__global__ void __launch_bounds__(TileCfg<kTile>::kThreads) partial_reduce_kernel(const ReduceArgs p) {
+    using TC = TileCfg<kTile>;
+    constexpr int T = TC::kT, NT = TC::kThreads;
+    const int64_t i_tile = blockIdx.x >> 2;  // tile among those reduced
+    const int q = blockIdx.x & 3;            // accumulator rows 2q, 2q + 1
+    int64_t slot0, c_lo, c_hi, stride, base;  // slots: slot0, then base + stride * c
+    if (p.split > 1) {
+        slot0 = i_tile * p.split;
+        base = slot0;
+        stride = 1;
+        c_lo = 1;
+        c_hi = p.split - 1;
+    } else {
+        const int64_t G = p.grid, U = p.sk_iters;
+        const int64_t x0 = i_tile * p.kt;    // the tile's first slice
+        // contributors: CTA h's run starts at slice h*U/G, so the first is
+        // the largest h with h*U/G <= x0, the last the largest with
+        // h*U/G <= x0 + kt - 1
+        const int64_t g_first = ((x0 + 1) * G - 1) / U;
+        const int64_t g_last = ((x0 + p.kt) * G - 1) / U;
+        if (g_first == g_last) return;
+        slot0 = 2 * g_first + ((g_first * U) / G == x0 ? 0 : 1);
+        base = 0;
+        stride = 2;
+        c_lo = g_first + 1;
+        c_hi = g_last;
+    }
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tm = (warp / TC::kWarpsN) * 4 + (lane >> 3);
+    const int tn = (warp % TC::kWarpsN) * 8 + (lane & 7);
+
+    // the tile's batch and origin: batch-major, grouped raster within a batch
+    const int64_t tile = p.first_tile + i_tile;
+    const int64_t per_batch = int64_t(p.tiles_m) * p.tiles_n;
+    const int64_t bidx = tile / per_batch;
+    const int64_t t_in = tile - bidx * per_batch;
+    const int64_t per_group = int64_t(kGroupM) * p.tiles_n;
+    const int64_t first_m = (t_in / per_group) * kGroupM;
+    const int64_t gm = min(int64_t(p.tiles_m) - first_m, int64_t(kGroupM));
+    const int64_t in_group = t_in - (t_in / per_group) * per_group;
+    const int64_t row0 = (first_m + in_group % gm) * T;
+    const int64_t col0 = (in_group / gm) * T;
+
+    float *Cb = kExt ? p.C + bidx * p.strideC : p.C;
+    const float *bias = kExt ? p.bias : nullptr;
+    const int act = kExt ? p.act : kActNone;
+    const float alpha = p.alpha, beta = p.beta;
+
+    // Everything above ran while the product kernel may still be running
+    // (programmatic dependent launch); from here on its partial tiles are
+    // complete and visible.  The old C values the product kernel never
+    // touches are fetched first, beside the partials.
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    float4 old[4];
+    bool whole[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int i = (4 * q + j) >> 1, h = j & 1;
+        const int64_t row = row0 + (i < 4 ? tm * 4 + i : T / 2 + tm * 4 + (i - 4));
+        const int64_t col = col0 + h * (T / 2) + tn * 4;
+        whole[j] = !kEdge || (row < p.M && kVec && col + 3 < p.N);
+        old[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (beta != 0.0f && whole[j])
+            old[j] = *reinterpret_cast<const float4 *>(Cb + row * p.ldc + col);
+    }
+    // partial sums in contributor order, four contributors' loads in flight
+    const float4 *part = reinterpret_cast<const float4 *>(p.partials) + (4 * q) * NT + tid;
+    float4 s[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) s[j] = __ldcg(part + size_t(slot0) * 16 * NT + j * NT);
+    for (int64_t c0 = c_lo; c0 <= c_hi; c0 += 4) {
+        float4 v[4][4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (c0 + u <= c_hi) {
+                const float4 *src = part + size_t(base + stride * (c0 + u)) * 16 * NT;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) v[u][j] = __ldcg(src + j * NT);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (c0 + u <= c_hi) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    s[j].x += v[u][j].x;
+                    s[j].y += v[u][j].y;
+                    s[j].z += v[u][j].z;
+                    s[j].w += v[u][j].w;
+                }
+            }
+        }
+    }
+
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int i = (4 * q + j) >> 1, h = j & 1;
+        const int64_t row = row0 + (i < 4 ? tm * 4 + i : T / 2 + tm * 4 + (i - 4));
+        if (kEdge && row >= p.M) continue;
+        const int64_t col = col0 + h * (T / 2) + tn * 4;
+        float *cp = Cb + row * p.ldc + col;
+        float v[4] = {alpha * s[j].x, alpha * s[j].y, alpha * s[j].z, alpha * s[j].w};
+        if (whole[j]) {
+            if (beta != 0.0f) {
+                v[0] = fmaf(beta, old[j].x, v[0]);
+                v[1] = fmaf(beta, old[j].y, v[1]);
+                v[2] = fmaf(beta, old[j].z, v[2]);
+                v[3] = fmaf(beta, old[j].w, v[3]);
+            }
+            if (bias) {
+                const float4 bv = *reinterpret_cast<const float4 *>(bias + col);
+                v[0] += bv.x;
+                v[1] += bv.y;
+                v[2] += bv.z;
+                v[3] += bv.w;
+            }
+            if (act == kActGeluTanh) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) v[c] = gelu_tanh(v[c]);
+            }
+            *reinterpret_cast<float4 *>(cp) = make_float4(v[0], v[1], v[2], v[3]);
+        } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (col + c < p.N) {
+                    float x = v[c];
+                    if (beta != 0.0f) x = fmaf(beta, cp[c], x);
+                    if (bias) x += bias[col + c];
+                    if (act == kActGeluTanh) x = gelu_tanh(x);
+                    cp[c] = x;
+                }
+            }
+        }
+    }
+}
+
+// Launches partial_reduce_kernel over r.tiles tiles (nothing when there
+// are none).
+// It is launched as a programmatic dependent of the product kernel: its
+// CTAs may be scheduled once every product CTA has passed its main loop, and
+// they wait (griddepcontrol.wait, released by the hardware when the product
+// grid has completed and its writes are visible) before reading a partial.
+template <int kTile, bool kVec, bool kEdge, bool kExt>
+cudaError_t launch_partial_reduce(const ReduceArgs &r, cudaStream_t stream) {
+    if (r.tiles <= 0 || (r.split <= 1 && r.sk_iters <= 0)) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(4 * r.tiles), 1, 1);
+    cfg.blockDim = dim3(TileCfg<kTile>::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, partial_reduce_kernel<kTile, kVec, kEdge, kExt>, r);
+}
+
 template <int kTile, bool kPacked, bool kVec, bool kEdge, bool kSplit, bool kTransA,
           bool kTransB, bool kExt, int kBKT = kTile / 8, int kSched = 0>
 cudaError_t launch_variant(const GemmArgs &a, cudaStream_t stream, int64_t sk_grid = 0) {
@@ -755,7 +877,33 @@ cudaError_t launch_variant(const GemmArgs &a, cudaStream_t stream, int64_t sk_gr
                                            (tiles - a.tail_start) * a.tail_split),
                     1, 1);
     kernel<<<grid, TC::kThreads, dyn, stream>>>(a);
-    return cudaGetLastError();
+    {
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    // split or stream-K tiles, if any, are summed by a second launch
+    ReduceArgs r{a.partials, a.C, a.bias, a.M, a.N, a.ldc, a.strideC, a.alpha, a.beta, a.act,
+                 a.tiles_m, a.tiles_n, 0, 0, 0, 0, 0, 0};
+    if constexpr (kSched == 1) {
+        r.first_tile = int64_t(a.dp_rounds) * sk_grid;
+        r.tiles = tiles - r.first_tile;
+        r.kt = a.sk_kt;
+        r.grid = int32_t(sk_grid);
+        r.sk_iters = a.sk_iters;
+        return launch_partial_reduce<kTile, kVec, kEdge, kExt>(r, stream);
+    } else if constexpr (kSplit) {
+        if (a.split_k > 1) {
+            r.first_tile = 0;
+            r.tiles = tiles;
+            r.split = a.split_k;
+        } else {
+            r.first_tile = a.tail_start;
+            r.tiles = tiles - a.tail_start;
+            r.split = a.tail_split;
+        }
+        return launch_partial_reduce<kTile, kVec, kEdge, kExt>(r, stream);
+    }
+    return cudaSuccess;
 }
 
 // All (vec, edge, split) variants of one tile, layout and issue form.

@@ -16,12 +16,12 @@
 //    Dense Matrix-Matrix Multiplication on the GPU" (PPoPP 2023).  Grids of
 //    fewer tiles than resident CTAs, and partial last waves, then keep every
 //    SM busy to the end, where split-K into equal ranges could not.
-//  * Fixed-order fix-up.  A CTA that computed only part of a tile's K range
-//    stores its partial tile in its own slot and takes a ticket on the tile;
-//    the CTA that takes the last ticket sums every contributor's partial in
-//    ascending CTA order (its own included, read back from memory) and runs
-//    the epilogue.  Nobody waits on anybody, and the sum order depends only
-//    on the shape and the grid, so results are bit-identical run to run.
+//  * Fixed-order fix-up in a second launch.  A CTA that computed only part
+//    of a tile's K range stores its partial tile in its own slot and moves
+//    on; once the persistent launch is done, partial_reduce_kernel (ffma_kernel.cuh)
+//    sums every contributor's partial in ascending CTA order and runs the
+//    epilogue.  Nobody waits on anybody, and the sum order depends only on
+//    the shape and the grid, so results are bit-identical run to run.
 //  * Every operand goes through an NP-page ring of 16-byte (or, for
 //    unaligned operands, 4-byte) cp.async copies, so NP - 2 slices are in
 //    flight while one is computed.  An operand whose stored rows run along M
@@ -121,7 +121,6 @@ ffma_sk_kernel(const SkArgs p) {
     float *const ringB = smem + NP * PG;              // NP pages
     float *const compA = smem + 2 * NP * PG;          // 2 pages when A is staged
     float *const compB = compA + (kStA ? 2 * PG : 0); // 2 pages when B is staged
-    __shared__ int s_last;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -170,7 +169,11 @@ ffma_sk_kernel(const SkArgs p) {
             }
         }
         __syncthreads();
-        if (s_done) break;
+        if (s_done) {
+            // the reduction launch may be scheduled once every CTA is here
+            asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+            break;
+        }
 
         const int nsl = s_k1 - s_k0;
         // operand pointers and bounds for this segment (recomputed after the
@@ -352,20 +355,12 @@ ffma_sk_kernel(const SkArgs p) {
         }
         cp_async_wait<0>();   // no copy of this segment outlives it
 
-        // ---- stream-K fix-up: partial tiles summed in CTA order ----
+        // ---- a segment that is not a whole tile: its partial tile goes to
+        // this CTA's slot (2g for its run's first segment, 2g + 1 for its
+        // last) and partial_reduce_kernel sums the slots afterwards ----
         if (s_k0 != 0 || s_k1 != p.kt) {
-            const int G = gridDim.x, g = blockIdx.x;
-            const int64_t U = p.sk_iters;
-            const int64_t lt = int64_t(s_tile) - int64_t(p.dp_rounds) * G;
-            const int64_t x0 = lt * p.kt;                  // first slice of the tile
-            // contributors: the CTAs whose runs meet [x0, x0 + kt); CTA h's
-            // run starts at h*U/G, so the first is the largest h with
-            // h*U/G <= x0 and the last the largest with h*U/G <= x0+kt-1
-            const int64_t g_first = ((x0 + 1) * G - 1) / U;
-            const int64_t g_last = ((x0 + p.kt) * G - 1) / U;
-            float4 *part = reinterpret_cast<float4 *>(p.partials);
-            // slot 2h: the run's first segment; 2h+1: its last one
-            float4 *mine = part + size_t(2 * g + (s_first ? 0 : 1)) * 16 * NT;
+            float4 *mine = reinterpret_cast<float4 *>(p.partials) +
+                           size_t(2 * blockIdx.x + (s_first ? 0 : 1)) * 16 * NT;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int i = j >> 1, hh = j & 1;
@@ -373,48 +368,7 @@ ffma_sk_kernel(const SkArgs p) {
                        make_float4(acc[i][2 * hh].x, acc[i][2 * hh].y, acc[i][2 * hh + 1].x,
                                    acc[i][2 * hh + 1].y));
             }
-            __threadfence();
-            __syncthreads();
-            unsigned *counter = p.counters + lt;
-            if (tid == 0) {
-                const unsigned prev = atomicAdd(counter, 1u);
-                s_last = prev == unsigned(g_last - g_first);
-            }
-            __syncthreads();
-            if (!s_last) continue;
-            __threadfence();
-            // the first contributor's share of this tile is its run's first
-            // segment only if its run starts exactly at the tile
-            const size_t slot0 = size_t(2 * g_first) + ((g_first * U) / G == x0 ? 0 : 1);
-            // Half a tile at a time, all eight loads of a contributor in
-            // flight together: the L2 round trips are twice the contributor
-            // count, not sixteen times it.  Each element is still summed in
-            // ascending contributor order.
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-#pragma unroll
-                for (int j = 8 * half; j < 8 * half + 8; ++j) {
-                    const int i = j >> 1, hh = j & 1;
-                    const float4 v = __ldcg(part + slot0 * 16 * NT + j * NT + tid);
-                    acc[i][2 * hh] = make_float2(v.x, v.y);
-                    acc[i][2 * hh + 1] = make_float2(v.z, v.w);
-                }
-                for (int64_t h = g_first + 1; h <= g_last; ++h) {
-                    float4 v[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        v[j] = __ldcg(part + size_t(2 * h) * 16 * NT + (8 * half + j) * NT + tid);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int i = (8 * half + j) >> 1, hh = j & 1;
-                        acc[i][2 * hh].x += v[j].x;
-                        acc[i][2 * hh].y += v[j].y;
-                        acc[i][2 * hh + 1].x += v[j].z;
-                        acc[i][2 * hh + 1].y += v[j].w;
-                    }
-                }
-            }
-            if (tid == 0) *counter = 0u;   // rearmed for the next launch
+            continue;
         }
 
         // ---- epilogue: C = act(alpha * acc (+ beta * C_old) (+ bias)) ----
@@ -481,7 +435,17 @@ cudaError_t launch_sk_variant(const SkArgs &a, cudaStream_t stream) {
         set_smem_once(reinterpret_cast<const void *>(kernel), bytes, configured, true);
     if (e != cudaSuccess) return e;
     kernel<<<unsigned(a.grid), Cfg<T, BK, NP>::kThreads, bytes, stream>>>(a);
-    return cudaGetLastError();
+    const cudaError_t e2 = cudaGetLastError();
+    if (e2 != cudaSuccess) return e2;
+    // the stream-K tiles, if any, summed by a second launch on the stream
+    ffma::ReduceArgs r{a.partials, a.C, a.bias, a.M, a.N, a.ldc, a.strideC, a.alpha, a.beta,
+                       a.act,      a.tiles_m, a.tiles_n, 0, 0, 0, 0, 0, 0};
+    r.first_tile = int64_t(a.dp_rounds) * a.grid;
+    r.tiles = a.tiles - r.first_tile;
+    r.kt = a.kt;
+    r.grid = a.grid;
+    r.sk_iters = a.sk_iters;
+    return ffma::launch_partial_reduce<T, kVec, true, kExt>(r, stream);
 }
 
 // The slice and ring each layout is built with (sk_config gives the same

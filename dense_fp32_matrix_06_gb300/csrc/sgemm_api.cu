@@ -515,7 +515,7 @@ sgemm_status library_workspace(int dev, cudaStream_t stream, size_t bytes, void 
 }
 
 // `a` with the stream-K fields of `plan` filled in, for a persistent launch
-// of ffma_gemm_kernel (the workspace holds the tile counters and partials).
+// of ffma_gemm_kernel (the workspace holds the partial tiles after the counter block).
 GemmArgs sk_gemm_args(const gemm_plan_t &plan, GemmArgs a, void *workspace) {
     a.sk_kt = int32_t(ceil_div(a.K, plan.bk));
     a.dp_rounds = plan.dp_rounds;
@@ -524,12 +524,10 @@ GemmArgs sk_gemm_args(const gemm_plan_t &plan, GemmArgs a, void *workspace) {
     a.tail_split = 1;
     a.tail_start = int64_t(plan.tiles_m) * plan.tiles_n * a.batch;
     a.k_per_split = a.tail_k_per_split = int64_t(a.sk_kt) * plan.bk;
-    a.counters = nullptr;
+    // the partial tiles follow the workspace's reserved counter block
     a.partials = nullptr;
-    if (plan.sk_iters > 0) {
-        a.counters = static_cast<unsigned *>(workspace);
+    if (plan.sk_iters > 0)
         a.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + kCounterBytes);
-    }
     return a;
 }
 
@@ -560,12 +558,9 @@ SkArgs sk_args(const gemm_plan_t &plan, const GemmArgs &a, void *workspace) {
     k.grid = int32_t(plan.grid_ctas);
     k.tiles = plan.tiles_m * plan.tiles_n * a.batch;
     k.sk_iters = plan.sk_iters;
-    k.counters = nullptr;
     k.partials = nullptr;
-    if (plan.sk_iters > 0) {
-        k.counters = static_cast<unsigned *>(workspace);
+    if (plan.sk_iters > 0)
         k.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + kCounterBytes);
-    }
     return k;
 }
 
@@ -601,14 +596,10 @@ sgemm_status run(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K, float
     a.tail_split = plan.tail_split;
     a.tiles_m = int32_t(plan.tiles_m);
     a.tiles_n = int32_t(plan.tiles_n);
-    a.split_base = plan.split_k > 1 ? 0 : plan.tail_start;
     a.part_base = plan.split_k > 1 ? 0 : plan.tail_start;
-    a.counters = nullptr;
     a.partials = nullptr;
-    if (plan.split_k > 1 || plan.tail_split > 1) {
-        a.counters = static_cast<unsigned *>(workspace);
+    if (plan.split_k > 1 || plan.tail_split > 1)
         a.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + kCounterBytes);
-    }
     if (plan.schedule == 2) {
         e = launch_ffma_tiny(a, plan.vec != 0, stream);
         return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
@@ -671,7 +662,7 @@ bool plan_matches(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int64_t
     if (p.schedule != 0 && p.schedule != 1) return false;
     if (p.schedule == 1) {
         // stream-K: whole-K rounds, then every run non-empty, every tile
-        // shared by few enough runs, counters and partials inside the workspace
+        // shared by few enough runs, partials inside the workspace
         const bool direct = p.transpose_a != 0;
         if (p.bk != sk_config_bk(t, direct) || p.stages != sk_config_pages(t, direct))
             return false;
@@ -857,8 +848,8 @@ sgemm_status sgemm_ffma_probe(int64_t ctas, int64_t iters, int32_t packed, float
 // lives inside the library, so the call never allocates device memory.
 // ---------------------------------------------------------------------------
 
-// The scratch buffer: tile counters followed by partial tiles, exactly the
-// layout of a split-K workspace.  Every GPU that loads the library holds it
+// The scratch buffer, laid out as a plan's workspace: the reserved counter
+// block, then the partial tiles.  Every GPU that loads the library holds it
 // until the process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SGEMM_NOALLOC_SCRATCH_BYTES];
 
@@ -906,16 +897,8 @@ extern "C" sgemm_status sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alp
         if (plan.workspace_bytes > size_t(SGEMM_NOALLOC_SCRATCH_BYTES)) return SGEMM_ERR_WORKSPACE;
         s = noalloc_scratch(dev, &ws);
         if (s != SGEMM_OK) return s;
-        // The buffer keeps whatever the previous call left; the tile counters
-        // must start at zero, so clear the ones this launch uses.
-        const int64_t tiles = plan.tiles_m * plan.tiles_n;
-        const int64_t split_tiles =
-            plan.schedule == 1 ? tiles - int64_t(plan.dp_rounds) * plan.grid_ctas
-            : plan.split_k > 1 ? tiles
-                               : tiles - plan.tail_start;
-        const size_t counter_bytes = size_t(split_tiles) * sizeof(unsigned);
-        const cudaError_t e = cudaMemsetAsync(ws, 0, counter_bytes, st);
-        if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
+        // The buffer keeps whatever the previous call left, which is fine:
+        // every partial tile is written before it is read back.
     }
     return run(plan, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, ws, st);
 }
@@ -1086,14 +1069,10 @@ extern "C" sgemm_status sgemm_ex(int32_t op_a, int32_t op_b, int64_t M, int64_t 
     a.tail_split = plan.tail_split;
     a.tiles_m = int32_t(plan.tiles_m);
     a.tiles_n = int32_t(plan.tiles_n);
-    a.split_base = plan.split_k > 1 ? 0 : plan.tail_start;
     a.part_base = plan.split_k > 1 ? 0 : plan.tail_start;
-    a.counters = nullptr;
     a.partials = nullptr;
-    if (plan.workspace_bytes > 0) {
-        a.counters = static_cast<unsigned *>(ws);
+    if (plan.workspace_bytes > 0)
         a.partials = reinterpret_cast<float *>(static_cast<char *>(ws) + kCounterBytes);
-    }
     if (plan.schedule == 1) {
         const bool ext = batch > 1 || bias != nullptr || act != SGEMM_ACT_NONE;
         if (ta && !tb && plan.bm == 128)   // both operands direct: the split-K kernel's loop

@@ -26,9 +26,11 @@ constexpr int kSmallCtasPerSm = 8;
 // GB with 16, the same 65.9 TFLOP/s.
 constexpr int kGroupM = 16;
 
-// Split-K workspace layout: [tile counters: kCounterBytes][partials].  The
-// counter block has a fixed size so a buffer reused across plans never sees
-// stale partial data where a counter is expected.
+// Workspace layout: [counter block: kCounterBytes][partial tiles][...].  The
+// 3xTF32 mode keeps its split-K tile counters in the block (fixed size, so a
+// buffer reused across plans never sees stale partial data where a counter
+// is expected); the FFMA kernels take no tickets and leave it untouched.
+// Split plans stay within kMaxSplitTiles split tiles either way.
 constexpr size_t kCounterBytes = 16384;
 constexpr int64_t kMaxSplitTiles = kCounterBytes / sizeof(unsigned);
 constexpr int kMaxSplit = 32;
@@ -102,11 +104,9 @@ struct GemmArgs {
     int32_t tail_split;
     int32_t tiles_m, tiles_n;
     // Tiles are numbered over all batches (batch-major).
-    // Split tiles only: counter of tile t is counters[t - split_base], partial
-    // of CTA pid is slot pid - part_base (16 x kThreads float4 per slot).
-    int64_t split_base;
+    // Split tiles only: the partial tile of CTA pid is slot pid - part_base
+    // (16 x kThreads float4 per slot), summed by partial_reduce_kernel.
     int64_t part_base;
-    unsigned *counters;    // zero on entry and exit
     float *partials;
     // Persistent stream-K launches of ffma_gemm_kernel (kSched = 1; G =
     // gridDim.x): whole-K tiles [0, dp_rounds * G) round-robin, then the
@@ -149,8 +149,7 @@ struct SkArgs {
     int32_t grid;         // G, the CTAs launched (every stream-K run non-empty: G <= sk_iters)
     int64_t tiles;        // over all batches (batch-major)
     int64_t sk_iters;     // slices of tiles [dp_rounds * G, tiles), spread over the G CTAs
-    unsigned *counters;   // one per stream-K tile; zero on entry and on exit
-    float *partials;      // 2 * G partial tiles
+    float *partials;      // 2 * G partial tiles, summed by partial_reduce_kernel
 };
 constexpr int kSkMaxContrib = 16;   // most CTAs that may share one tile's K slices
 // K slice and ring depth of the stream-K kernel for a tile: both operands

@@ -78,7 +78,8 @@ typedef enum {
     SGEMM_ACT_GELU_TANH = 1  /* 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) */
 } sgemm_act;
 
-/* Size of the tile-counter block at the start of a split-K workspace. */
+/* Size of the block at the start of every workspace that the 3xTF32 mode
+ * keeps its tile counters in; the FFMA kernels leave it untouched. */
 #define SGEMM_WORKSPACE_COUNTER_BYTES 16384
 
 /* A per-shape launch configuration chosen by gemm_plan.  Plain data: the
@@ -100,10 +101,11 @@ typedef struct {
     int64_t k_per_split;   /* K extent of one partition (a multiple of bk) */
     int64_t tiles_m, tiles_n;
     int64_t grid_ctas;     /* CTAs launched */
-    size_t workspace_bytes;/* device scratch the plan needs: the split-K tile
-                              counters and partial tiles, and the transposed
-                              copy of A when transpose_a is set; 0 when it has
-                              neither */
+    size_t workspace_bytes;/* device scratch the plan needs: a
+                              SGEMM_WORKSPACE_COUNTER_BYTES block, then the
+                              split-K or stream-K partial tiles, then the
+                              transposed copy of A when transpose_a is set; 0
+                              when it has neither partials nor copy */
     int64_t tail_start;    /* first tile (in launch order) of the tail region; tiles
                               when there is none.  Only the last, partly filled wave
                               of tiles is split, so it ends sooner */
@@ -174,10 +176,10 @@ sgemm_status sgemm(int64_t M, int64_t N, int64_t K, float alpha,
  * sgemm_with_plan -- like sgemm, with a plan from gemm_plan and caller-owned
  * workspace.  `workspace` is a device buffer of at least
  * plan->workspace_bytes bytes, 256-byte aligned, used only by work queued on
- * `stream`.  Its first SGEMM_WORKSPACE_COUNTER_BYTES bytes (the tile
- * counters) must be zero before the first use; every call that completes
- * leaves them zero again, so one zeroed buffer serves any number of calls and
- * plans.  Calls that share a workspace must not overlap on the GPU.
+ * `stream`.  Its contents need no initialisation: a call writes every
+ * partial tile and every transposed element before it reads them, so one
+ * buffer serves any number of calls and plans.  Calls that share a
+ * workspace must not overlap on the GPU.
  * workspace may be NULL when plan->workspace_bytes == 0.
  * Returns SGEMM_ERR_WORKSPACE when workspace_bytes < plan->workspace_bytes,
  * SGEMM_ERR_INVALID_ARG when the plan does not match the arguments.
@@ -215,8 +217,9 @@ sgemm_status sgemm_with_plan(const gemm_plan_t *plan, int64_t M, int64_t N, int6
  * It calls no cudaMalloc, cudaFree or other allocating routine.  The first
  * call on each device looks up the buffer's device address (with that device
  * current) and caches it; make that first call before any stream capture.
- * Each call clears the tile counters it uses with cudaMemsetAsync on
- * `stream`, then launches the GEMM.
+ * Nothing in the buffer has to start at zero (a call writes each partial
+ * tile before it reads it back), so a call only launches the GEMM's kernels
+ * on `stream`.
  *
  * All calls on a device share the one buffer: calls that overlap on the GPU
  * (different streams without ordering between them) race and give wrong

@@ -3,7 +3,7 @@
 Every case forces the stream-K kernel (tuning knob schedule = 1) and varies
 what decides its work split: the tile (64 or 128), the fewest K slices a CTA
 run may hold (1 and 3 make many CTAs share each tile, so the fixed-order
-fix-up runs with up to 16 contributors), alignment (16-byte and 4-byte
+reduction sums up to 16 contributors), alignment (16-byte and 4-byte
 copies), the operand layouts, batches and the fused epilogue.  Tolerances as
 everywhere: bit-exact on integer-valued inputs, normalised error <= 1e-6
 otherwise; every result is also checked for writes outside C's logical block.
@@ -85,10 +85,10 @@ def test_whole_k_rounds_then_stream_k(sg, tune):
     run_and_check(sg, p, exact=True)
 
 
-def test_runs_are_bit_identical_and_counters_rearm(sg, tune):
-    """The fix-up order is fixed, so repeated runs agree bit for bit; and the
-    tile counters return to zero, so plans of other shapes that reuse the
-    same workspace right after are right too."""
+def test_runs_are_bit_identical_and_workspace_reusable(sg, tune):
+    """The fix-up order is fixed, so repeated runs agree bit for bit; and
+    plans of other shapes that reuse the same workspace right after, over
+    whatever partials the previous call left there, are right too."""
     tune(schedule=1, tile=128, sk_min_slices=2)
     p = workloads.workload("square1024ab")
     outs = []
@@ -123,8 +123,8 @@ def test_attention_shapes(sg, tune):
 
 
 def test_noalloc_runs_stream_k_plans(sg, tune):
-    """sgemm_noalloc clears the stream-K tile counters it uses in its own
-    scratch, twice in a row."""
+    """sgemm_noalloc runs stream-K plans in its own scratch, twice in a row,
+    over the partials the previous call left there."""
     import torch
     tune(schedule=1, sk_min_slices=2)
     p = workloads.workload("square1024ab", dist="int4")
@@ -160,8 +160,8 @@ def test_transposed_a_then_stream_k(sg, tune, M, N, K, lds, dist):
 
 @pytest.mark.parametrize("transpose_a", [0, 1])
 def test_stream_k_plan_with_caller_workspace(sg, tune, transpose_a):
-    """gemm_plan + sgemm_with_plan on a stream-K plan, with a caller-owned,
-    zeroed workspace used for three calls in a row."""
+    """gemm_plan + sgemm_with_plan on a stream-K plan, with a caller-owned
+    workspace that starts as garbage, used for three calls in a row."""
     import torch
     tune(schedule=1, tile=128, transpose_a=transpose_a, sk_min_slices=2)
     p = workloads.make(1024, 1280, 1536, dist="int4", seed=98, alpha=1.5, beta=0.5,
@@ -171,7 +171,7 @@ def test_stream_k_plan_with_caller_workspace(sg, tune, transpose_a):
     plan = sg.gemm_plan(p.M, p.N, p.K, p.lda, p.ldb, p.ldc, A.data_ptr(), B.data_ptr(),
                         A.data_ptr())
     assert plan.schedule == 1 and plan.transpose_a == transpose_a and plan.sk_iters > 0
-    ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    ws = torch.full((plan.workspace_bytes,), 0xFF, dtype=torch.uint8, device="cuda")
     ref = oracle.problem(p)
     for _ in range(3):
         C = torch.from_numpy(p.C0).cuda()
@@ -180,5 +180,5 @@ def test_stream_k_plan_with_caller_workspace(sg, tune, transpose_a):
                                plan.workspace_bytes, torch.cuda.current_stream().cuda_stream)
         torch.cuda.synchronize()
         assert np.array_equal(C.cpu().numpy()[:, :p.N], ref)
-    # the tile counters are back at zero after every call
-    assert int(ws[:sg.WORKSPACE_COUNTER_BYTES].sum()) == 0
+    # stream-K takes no tickets: the counter block is never written
+    assert bool((ws[:sg.WORKSPACE_COUNTER_BYTES] == 0xFF).all())

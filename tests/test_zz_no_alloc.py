@@ -106,8 +106,8 @@ def test_noalloc_bit_exact_on_integer_inputs(sg, tune, name):
 
 
 def test_noalloc_tail_split(sg, tune):
-    """Only the tiles of the last partial wave cut along K: the counters the
-    launch uses sit at the start of the buffer, past those of no other tile."""
+    """Only the tiles of the last partial wave cut along K: their partial
+    tiles sit at the start of the buffer's partial area."""
     tune(tail_split=4)
     p = workloads.make(2560, 2048, 1024, dist="int4", seed=51, alpha=1.5, beta=0.5,
                        c0_dist="int4", name="tail_int4")
