@@ -305,30 +305,63 @@ void plan_core(int64_t M, int64_t N, int64_t K, int64_t batch, bool vec, int sms
     *out = p;
 }
 
-// Transposing A first.  The kernel stages an operand whose stored rows run
-// along K (A as given) through registers and transposing shared stores, and
-// copies one whose rows run along M (A^T) straight in with cp.async, which
-// leaves it 8 registers and ~10 instructions per K slice lighter, and lets
-// the product run in K slices of 32 through a three-page ring.  A transpose
-// pass costs 8*M*K bytes of HBM traffic, about 35/N of the product's time.
-// Measured on GB300 (TFLOP/s, without / with the pass): 8192^3 60.7 / 65.8,
-// 4096^3 58.4 / 62.4, 2048^3 48.7 / 50.9, 1024x1024x16384 (split-K) 47.0 /
-// 49.2; it loses for K = 64 (47.5 / 46.7), for GPT-2 QKV (144 tiles, under
-// one per SM: 43.9 / 43.4) and for split-K plans with short K (1024^3 31.5 /
-// 29.3, MLP-up 39.8 / 38.2).  Hence: N >= 1024, K >= 256, and either no
-// split with at least one tile per SM, or split-K with K >= 8192.  The copy
-// lives in the workspace after the counters and any split-K partials.
-// The tuning knob kKnobTransposeA (0/1) overrides the choice for sweeps.
-bool choose_transpose_a(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int sms) {
+// Transposing A first, and how the product then runs.  The kernel stages an
+// operand whose stored rows run along K (A as given) through registers and
+// transposing shared stores, and copies one whose rows run along M (A^T)
+// straight in with cp.async, which leaves it 8 registers and ~10
+// instructions per K slice lighter, and lets the product run in K slices of
+// 32 through a three-page ring.  A transpose pass costs 8*M*K bytes of HBM
+// traffic, about 35/N of the product's time.  Measured on GB300 (TFLOP/s,
+// without / with the pass): 8192^3 60.7 / 65.8, 4096^3 58.4 / 62.4, 2048^3
+// 48.7 / 50.9; it loses for K = 64 (47.5 / 46.7) and for short K on few
+// tiles (GPT-2 QKV, 144 tiles: 43.9 / 43.4).
+//
+// Below one wave of 128-wide tiles (S = 2 resident CTAs per SM) the choice is
+// three-way: split-K without the pass (kTransposeNone), the pass and one CTA
+// per tile or K range (kTransposeGrid), or the pass and a persistent
+// stream-K launch (kTransposeStreamK).  Measured on GB300 (N = 1024 and
+// 2048, 32..256 tiles, K = 768..4096; microseconds, L2 flushed): the pass
+// wins from K = 1024 on for 96 tiles and more (2560x1024x1024: 150 without,
+// 139 with); stream-K after the pass wins for K >= 4096 on any grid up to
+// 0.7 S, for K >= 2048 from 0.3 S to 0.7 S and for K >= 1024 from 0.5 S to
+// 0.7 S (1280x2048x2048, 160 tiles: 279 split-K, 233 grid, 212 stream-K;
+// 512x2048x4096: 194 / 181 / 171); between 0.7 S and S the plain grid after
+// the pass is the fastest (1792x2048x2048, 224 tiles: 271 grid, 287
+// stream-K; 2048^3 is the exception, 338 / 322); with K = 768, or K = 1024
+// on under 0.3 S tiles, split-K without the pass (1024^3: 57 / 59 / 63).
+// Tuning knobs: kKnobTransposeA (0/1) forces the pass off or on,
+// kKnobSchedule (0/1) the grid or stream-K after it.
+enum TransposeFamily { kTransposeNone = 0, kTransposeGrid = 1, kTransposeStreamK = 2 };
+
+int choose_transpose_a(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int sms) {
     const bool able = p.bm == 128 && p.tail_split == 1 && p.vec && K >= 1 &&
                       M <= int64_t(65535) * 32;
+    if (!able) return kTransposeNone;
     const int64_t tiles = p.tiles_m * p.tiles_n;
+    const int64_t S = int64_t(sms) * kCtasPerSm;
     const bool k_split = p.split_k > 1 || p.schedule == 1;
-    bool want = able && N >= 1024 && K >= 256 &&
-                ((!k_split && tiles >= sms) || (k_split && K >= 8192));
-    const int f = tuning(kKnobTransposeA);
-    if (f == 0) want = false;
-    if (f == 1) want = able;
+    const bool one_per_sm = !k_split && tiles >= sms;
+    int want = kTransposeNone;
+    if (N >= 1024 && K >= 256) {
+        if (10 * tiles > 7 * S)
+            want = (K >= 1024 || one_per_sm) ? kTransposeGrid : kTransposeNone;
+        else if (K >= 4096)
+            want = kTransposeStreamK;
+        else if (K >= 2048)
+            want = 10 * tiles >= 3 * S ? kTransposeStreamK : kTransposeGrid;
+        else if (K >= 1024)
+            want = 2 * tiles > S ? kTransposeStreamK
+                                 : (10 * tiles >= 3 * S ? kTransposeGrid : kTransposeNone);
+        else
+            want = one_per_sm ? kTransposeGrid : kTransposeNone;
+    }
+    const int32_t f = tuning(kKnobTransposeA);
+    if (f == 0) return kTransposeNone;
+    if (f == 1 && want == kTransposeNone)
+        want = p.schedule == 1 ? kTransposeStreamK : kTransposeGrid;
+    const int32_t sched = tuning(kKnobSchedule);
+    if (want != kTransposeNone && (sched == 0 || sched == 1))
+        want = sched == 1 ? kTransposeStreamK : kTransposeGrid;
     return want;
 }
 
@@ -447,16 +480,22 @@ sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb
         plan_tiny(*out, M, N, K);
         return SGEMM_OK;
     }
-    if (allow_transpose && M > 0 && N > 0 && K > 0 && choose_transpose_a(*out, M, N, K, sms)) {
+    const int fam = (allow_transpose && M > 0 && N > 0 && K > 0)
+                        ? choose_transpose_a(*out, M, N, K, sms)
+                        : int(kTransposeNone);
+    if (fam != kTransposeNone) {
         // the product then runs with both operands copied by rows, in K slices of 32
         gemm_plan_t &q = *out;
         q.transpose_a = 1;
-        if (q.schedule == 1) {
+        if (fam == kTransposeStreamK) {
             plan_stream_k(q, M, N, q.tiles_m * q.tiles_n, K, sms, true);
             size_t at_offset = 0;
             q.workspace_bytes = transpose_workspace(q, M, K, &q.a_t_ld, &at_offset);
             return SGEMM_OK;
         }
+        q.schedule = 0;
+        q.dp_rounds = 0;
+        q.sk_iters = 0;
         make_wide(q, M, N, K, 1, sms);
         size_t at_offset = 0;
         q.workspace_bytes = transpose_workspace(q, M, K, &q.a_t_ld, &at_offset);

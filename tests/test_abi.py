@@ -141,6 +141,32 @@ def test_plan_transpose_choice(lib, tune):
     assert r.workspace_bytes == sg.WORKSPACE_COUNTER_BYTES + (515 * 2048 * 4 + 255) // 256 * 256
 
 
+@pytest.mark.parametrize("M,N,K,family", [
+    # one wave of 128-wide tiles is S = 304 resident CTAs on 152 SMs
+    (1024, 1024, 1024, "none"),        # 64 tiles, K = 1024: split-K, no pass
+    (1536, 1024, 1024, "grid"),        # 96 tiles (>= 0.3 S), K = 1024
+    (2560, 1024, 1024, "stream_k"),    # 160 tiles (> 0.5 S), K = 1024
+    (512, 2048, 2048, "grid"),         # 64 tiles (< 0.3 S), K = 2048
+    (1280, 2048, 2048, "stream_k"),    # 160 tiles, K = 2048
+    (512, 2048, 4096, "stream_k"),     # 64 tiles, K = 4096
+    (1792, 2048, 2048, "grid"),        # 224 tiles (> 0.7 S): the grid
+    (2048, 2048, 2048, "grid"),        # 256 tiles
+    (1024, 2304, 768, "none"),         # 144 tiles, K = 768
+    (1024, 3072, 768, "none"),         # 192 tiles, K = 768, split-K
+    (1024, 1024, 16384, "stream_k"),   # 64 tiles, long K
+    (4096, 4096, 4096, "grid"),        # several waves
+    (2048, 768, 4096, "none"),         # N < 1024: the pass costs too much
+])
+def test_plan_transpose_family_bands(lib, M, N, K, family):
+    """Below one wave, the pass over A and the schedule after it follow the
+    bands measured on GB300 (tile count as a fraction of a wave, and K)."""
+    p = plan(M, N, K)
+    got = "none" if not p.transpose_a else ("stream_k" if p.schedule == 1 else "grid")
+    assert got == family
+    if p.transpose_a:
+        assert p.bk == 32 and p.stages == 3
+
+
 def test_plan_tail_split_is_opt_in(lib, tune):
     tune(tail_split="2")
     p = plan(8192, 8192, 8192)
