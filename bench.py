@@ -280,8 +280,10 @@ def run_ours(args):
     sh = stream.cuda_stream
     plan = sg.gemm_plan(p.M, p.N, p.K, p.lda, p.ldb, p.ldc, A.data_ptr(), B.data_ptr(),
                         C.data_ptr())
-    # one kernel per GEMM, plus the transpose pass when the plan copies A first
-    launches_per_gemm = 1 + int(plan.transpose_a)
+    # one product kernel per GEMM, plus the transpose pass when the plan copies
+    # A first, plus the reduction of partial tiles when tiles share K ranges
+    shares_k = plan.split_k > 1 or plan.tail_split > 1 or (plan.schedule == 1 and plan.sk_iters > 0)
+    launches_per_gemm = 1 + int(plan.transpose_a) + int(shares_k)
 
     def step():
         sg.sgemm_ptr(p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,

@@ -991,7 +991,19 @@ cudaError_t launch_fused(const CUtensorMap &a, const CUtensorMap &bh, const CUte
 
 namespace {
 constexpr int kTcBN = 256;
-constexpr int kTcStages = 2;
+// Ring depths.  256-wide tiles fit two stages of B (with the three-slot A
+// ring of the fused kernel: 224 KiB); 128-wide tiles leave room for more.
+// Measured on GB300 (microseconds, two stages / deeper): the split-operand
+// kernel with three stages on 1023x777x513 44.7 / 42.7; the fused kernel's
+// B ring with four stages 1024^3 47.7 / 51.9, MLP-down 68.2 / 72.4, so it
+// keeps two.
+constexpr int kTcStages = 2;           // 256-wide tiles, both kernels
+constexpr int kTcMmaStages128 = 3;     // split-operand kernel, 128-wide: 192 KiB
+constexpr int kTcFusedStages128 = 2;   // fused kernel's B ring, 128-wide
+static_assert(FusedSmem<128, kTcFusedStages128>::kDynBytes <= 227 * 1024, "fused ring too deep");
+static_assert(TcSmem<128, kTcMmaStages128>::kDynBytes <= 227 * 1024, "split-operand ring too deep");
+static_assert(FusedSmem<256, kTcStages>::kDynBytes <= 227 * 1024, "fused ring too deep");
+static_assert(TcSmem<256, kTcStages>::kDynBytes <= 227 * 1024, "split-operand ring too deep");
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 }  // namespace
@@ -1157,7 +1169,7 @@ cudaError_t launch_tf32x3_packed(const float *A, int64_t lda, const void *packed
             return cudaErrorInvalidValue;
         const TcArgs a = make_args(C, ldc, M, N, K, alpha, beta, counters,
                                    reinterpret_cast<float *>(w), plan, limit_ns, inject_stall);
-        return plan.bn == 128 ? launch_fused<128, kTcStages>(am, bh, bl, a, stream)
+        return plan.bn == 128 ? launch_fused<128, kTcFusedStages128>(am, bh, bl, a, stream)
                               : launch_fused<kTcBN, kTcStages>(am, bh, bl, a, stream);
     }
     const size_t abytes = round256(size_t(M) * kp * 4);
@@ -1175,7 +1187,7 @@ cudaError_t launch_tf32x3_packed(const float *A, int64_t lda, const void *packed
         return cudaErrorInvalidValue;
     const TcArgs a = make_args(C, ldc, M, N, K, alpha, beta, counters, parts, plan, limit_ns,
                                inject_stall);
-    return plan.bn == 128 ? launch_mma<128, kTcStages>(ah, al, bh, bl, a, stream)
+    return plan.bn == 128 ? launch_mma<128, kTcMmaStages128>(ah, al, bh, bl, a, stream)
                           : launch_mma<kTcBN, kTcStages>(ah, al, bh, bl, a, stream);
 }
 
@@ -1217,7 +1229,7 @@ cudaError_t launch_tf32x3(const float *A, int64_t lda, const float *B, int64_t l
         return cudaErrorInvalidValue;
     const TcArgs a = make_args(C, ldc, M, N, K, alpha, beta, counters, parts, plan, limit_ns,
                                inject_stall);
-    return plan.bn == 128 ? launch_mma<128, STAGES>(ah, al, bh, bl, a, stream)
+    return plan.bn == 128 ? launch_mma<128, kTcMmaStages128>(ah, al, bh, bl, a, stream)
                           : launch_mma<kTcBN, STAGES>(ah, al, bh, bl, a, stream);
 }
 
