@@ -327,8 +327,11 @@ void plan_core(int64_t M, int64_t N, int64_t K, int64_t batch, bool vec, int sms
 // 0.7 S (1280x2048x2048, 160 tiles: 279 split-K, 233 grid, 212 stream-K;
 // 512x2048x4096: 194 / 181 / 171); between 0.7 S and S the plain grid after
 // the pass is the fastest (1792x2048x2048, 224 tiles: 271 grid, 287
-// stream-K; 2048^3 is the exception, 338 / 322); with K = 768, or K = 1024
-// on under 0.3 S tiles, split-K without the pass (1024^3: 57 / 59 / 63).
+// stream-K; 4480x1024x2048, 280 tiles: 345 / 359) except from 0.75 S to
+// 0.875 S with K >= 2048, where stream-K gains 1-6 % (2048^3, 256 tiles:
+// 338 / 324; 3968x1024x2048, 248 tiles: 343 / 324; 4224x1024x4096, 264
+// tiles: 675 / 654); with K = 768, or K = 1024 on under 0.3 S tiles,
+// split-K without the pass (1024^3: 57 / 59 / 63).
 // Tuning knobs: kKnobTransposeA (0/1) forces the pass off or on,
 // kKnobSchedule (0/1) the grid or stream-K after it.
 enum TransposeFamily { kTransposeNone = 0, kTransposeGrid = 1, kTransposeStreamK = 2 };
@@ -344,7 +347,9 @@ int choose_transpose_a(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, in
     int want = kTransposeNone;
     if (N >= 1024 && K >= 256) {
         if (10 * tiles > 7 * S)
-            want = (K >= 1024 || one_per_sm) ? kTransposeGrid : kTransposeNone;
+            want = (K >= 2048 && 4 * tiles > 3 * S && 8 * tiles <= 7 * S)
+                       ? kTransposeStreamK
+                       : ((K >= 1024 || one_per_sm) ? kTransposeGrid : kTransposeNone);
         else if (K >= 4096)
             want = kTransposeStreamK;
         else if (K >= 2048)
@@ -499,7 +504,17 @@ sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb
         make_wide(q, M, N, K, 1, sms);
         size_t at_offset = 0;
         q.workspace_bytes = transpose_workspace(q, M, K, &q.a_t_ld, &at_offset);
+        return SGEMM_OK;
     }
+    // Split-K plans of 128-wide tiles without the pass issue their FMAs
+    // packed (fma.rn.f32x2; the same roundings in the same order, so the
+    // same C bit for bit).  Measured on GB300 (microseconds, scalar /
+    // packed): 1024^3 58.0 / 56.0, MLP-up 108.1 / 103.0, MLP-down 104.0 /
+    // 100.0, 1023x777x513 on 64-wide tiles unchanged; unsplit grids lose
+    // (GPT-2 QKV 82.6 / 105.1, 8192x8192x64 181 / 201), so they stay scalar.
+    gemm_plan_t &q = *out;
+    if (q.schedule == 0 && q.bm == 128 && q.split_k > 1 && tuning(kKnobKernel) < 0)
+        q.kernel = kKernelFfma2x128;
     return SGEMM_OK;
 }
 

@@ -125,7 +125,7 @@ def test_plan_full_tiles_take_the_unchecked_vector_path(lib):
 
 def test_plan_transpose_choice(lib, tune):
     assert plan(4096, 4096, 4096).transpose_a == 1
-    assert plan(2048, 2048, 2048).transpose_a == 1        # 256 tiles, at least one per SM
+    assert plan(2048, 2048, 2048).transpose_a == 1        # 256 tiles, more than one per SM
     assert plan(1024, 2304, 768).transpose_a == 0         # 144 tiles, under one per SM
     assert plan(1024, 1024, 16384).transpose_a == 1       # split-K with long K
     assert plan(8192, 8192, 64).transpose_a == 0         # K too short to pay for the pass
@@ -150,7 +150,9 @@ def test_plan_transpose_choice(lib, tune):
     (1280, 2048, 2048, "stream_k"),    # 160 tiles, K = 2048
     (512, 2048, 4096, "stream_k"),     # 64 tiles, K = 4096
     (1792, 2048, 2048, "grid"),        # 224 tiles (> 0.7 S): the grid
-    (2048, 2048, 2048, "grid"),        # 256 tiles
+    (2048, 2048, 2048, "stream_k"),    # 256 tiles (0.75 S .. 0.875 S, K >= 2048)
+    (2048, 2048, 1024, "grid"),        # the same grid with K = 1024
+    (4480, 1024, 2048, "grid"),        # 280 tiles (> 0.875 S)
     (1024, 2304, 768, "none"),         # 144 tiles, K = 768
     (1024, 3072, 768, "none"),         # 192 tiles, K = 768, split-K
     (1024, 1024, 16384, "stream_k"),   # 64 tiles, long K
@@ -326,8 +328,8 @@ def test_tuning_env_is_read_once_at_load(lib):
 
 def test_plan_schedule_choice(lib, tune):
     """Persistent stream-K where it measured faster: tiny grids of 64-wide
-    tiles and few 128-wide tiles with long K; one CTA per (tile, K range)
-    elsewhere."""
+    tiles, and (after the A^T pass) partial waves of 128-wide tiles with long
+    enough K; one CTA per (tile, K range) elsewhere."""
     p = plan(256, 256, 256)          # 2^24 multiply-adds: the small-problem kernel
     assert p.schedule == 2 and p.bm == 32 and p.bk == 256 and p.threads == 256
     assert p.grid_ctas == 64 and p.workspace_bytes == 0
@@ -335,7 +337,9 @@ def test_plan_schedule_choice(lib, tune):
     assert p.schedule == 1 and p.bm == 64 and p.bk == 8 and p.stages == 4
     q = plan(1024, 1024, 16384)      # 64 tiles, K = 16384: A transposed, then stream-K
     assert q.schedule == 1 and q.transpose_a == 1 and q.bk == 32 and q.stages == 3
-    for shape in [(1024, 1024, 1024), (1023, 777, 513), (1024, 2304, 768), (2048, 2048, 2048),
+    r = plan(2048, 2048, 2048)       # 256 tiles, 0.84 of a wave: A transposed, then stream-K
+    assert r.schedule == 1 and r.transpose_a == 1
+    for shape in [(1024, 1024, 1024), (1023, 777, 513), (1024, 2304, 768), (4096, 4096, 4096),
                   (8192, 8192, 8192), (8192, 8192, 64)]:
         assert plan(*shape).schedule == 0, shape
     tune(schedule=0)
