@@ -330,7 +330,8 @@ def run_ours(args):
     traffic = committed_traffic(plan.kernel, p.name, flops)
     roofline = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 3),
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                "kernel": ("ffma_gemm_kernel<128, op(A)=A^T copy, K slice 32> after "
+                "kernel": (f"ffma_gemm_kernel<128, op(A)=A^T copy, K slice 32, "
+                           f"{'packed' if plan.kernel == 1 else 'scalar'} FMA issue> after "
                            "transpose_kernel" if plan.transpose_a else
                            f"ffma_gemm_kernel (plan kernel {plan.kernel})"),
                 "timed": "each sgemm call (all of its launches) with CUDA events",

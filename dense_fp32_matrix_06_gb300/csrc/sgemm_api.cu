@@ -404,13 +404,21 @@ bool ex_transpose_first(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, i
     return want;
 }
 
-// Kernel of a plan whose operands both arrive by direct copies: the 16 x 8
-// per-thread kernel when the tuning knob kKnobKernel asks for it (= 2) and
-// the plan does not split K; the 8 x 8 kernel otherwise.
+// Kernel of a plan whose operands both arrive by direct copies (op(A) = A^T
+// copied first, op(B) = B): the 8 x 8 kernel with packed FMA issue
+// (fma.rn.f32x2; the same roundings in the same order as scalar issue, so
+// the same C bit for bit).  Without register staging of A the packed build
+// stays within 128 registers, and half as many FMA instructions leave the
+// issue slots room: measured on GB300 (scalar / packed), 8192^3 16.70 /
+// 15.85 ms, 4096^3 2205 / 2090 us, split-K plans 1536x1024x1024 79.6 /
+// 75.4 and 1792x2048x2048 270.0 / 258.7 us, stream-K 2048^3 323.3 / 320.1
+// us.  The tuning knob kKnobKernel picks scalar issue (0) or the 16 x 8
+// per-thread kernel (2, plans that do not split K).
 int32_t choose_wide_kernel(const gemm_plan_t &q) {
     const int32_t k = tuning(kKnobKernel);
     if (k == kKernelFfma16x8 && q.split_k == 1 && q.tail_split == 1) return kKernelFfma16x8;
-    return kKernelFfma128;
+    if (k == kKernelFfma128) return kKernelFfma128;
+    return kKernelFfma2x128;
 }
 
 // Re-plans a 128-wide one-CTA-per-(tile, K range) plan for the kernel that
@@ -494,6 +502,7 @@ sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb
         q.transpose_a = 1;
         if (fam == kTransposeStreamK) {
             plan_stream_k(q, M, N, q.tiles_m * q.tiles_n, K, sms, true);
+            q.kernel = tuning(kKnobKernel) == kKernelFfma128 ? kKernelFfma128 : kKernelFfma2x128;
             size_t at_offset = 0;
             q.workspace_bytes = transpose_workspace(q, M, K, &q.a_t_ld, &at_offset);
             return SGEMM_OK;
@@ -667,11 +676,17 @@ sgemm_status run(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K, float
         if (e != cudaSuccess) return cuda_fail(e, SGEMM_ERR_LAUNCH);
         a.A = at;
         a.lda = plan.a_t_ld;
+        const bool packed = plan.kernel == kKernelFfma2x128;
         if (plan.schedule == 1)
-            e = launch_ffma_tn_wide_sk(sk_gemm_args(plan, a, workspace), plan.grid_ctas,
-                                       plan.vec != 0, plan.edge != 0, false, stream);
+            e = packed ? launch_ffma_tn_wide_sk_packed(sk_gemm_args(plan, a, workspace),
+                                                       plan.grid_ctas, plan.vec != 0,
+                                                       plan.edge != 0, stream)
+                       : launch_ffma_tn_wide_sk(sk_gemm_args(plan, a, workspace), plan.grid_ctas,
+                                                plan.vec != 0, plan.edge != 0, false, stream);
         else if (plan.kernel == kKernelFfma16x8)
             e = launch_ffma16x8(a, plan.edge != 0, false, stream);
+        else if (packed)
+            e = launch_ffma_tn_wide_packed(a, plan.vec != 0, plan.edge != 0, stream);
         else
             e = launch_ffma_tn_wide(a, plan.vec != 0, plan.edge != 0, false, stream);
         return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
@@ -1158,8 +1173,11 @@ extern "C" sgemm_status sgemm_ex(int32_t op_a, int32_t op_b, int64_t M, int64_t 
             a.strideB = sb_t;
         }
         const bool ext = batch > 1 || bias != nullptr || act != SGEMM_ACT_NONE;
-        e = plan.kernel == kKernelFfma16x8
-                ? launch_ffma16x8(a, plan.edge != 0, ext, st)
+        // (packed issue is built for plain products; batches, bias and GELU
+        // run the scalar build)
+        e = plan.kernel == kKernelFfma16x8 ? launch_ffma16x8(a, plan.edge != 0, ext, st)
+            : (plan.kernel == kKernelFfma2x128 && !ext)
+                ? launch_ffma_tn_wide_packed(a, plan.vec != 0, plan.edge != 0, st)
                 : launch_ffma_tn_wide(a, plan.vec != 0, plan.edge != 0, ext, st);
         return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
     }

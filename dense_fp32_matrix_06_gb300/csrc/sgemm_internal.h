@@ -204,6 +204,11 @@ size_t tiny_smem_bytes(int64_t K);
 // The 16 x 8 per-thread kernel (ffma_wide.cu): op(A) = A^T, op(B) = B, 128
 // tiles, K slices of 32, no split.
 cudaError_t launch_ffma16x8(const GemmArgs &a, bool edge, bool ext, cudaStream_t stream);
+// The same two schedules with packed FMA issue (plain products only).
+cudaError_t launch_ffma_tn_wide_packed(const GemmArgs &a, bool vec, bool edge,
+                                       cudaStream_t stream);
+cudaError_t launch_ffma_tn_wide_sk_packed(const GemmArgs &a, int64_t grid, bool vec, bool edge,
+                                          cudaStream_t stream);
 // At_b = A_b^T (K x M, row stride ldt) for b < batch, with A_b = A +
 // b*stride_a and At_b = At + b*stride_t; M <= 65535 * 32, batch <= 65535.
 cudaError_t launch_transpose(const float *A, int64_t M, int64_t K, int64_t lda, float *At,

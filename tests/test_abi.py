@@ -169,6 +169,21 @@ def test_plan_transpose_family_bands(lib, M, N, K, family):
         assert p.bk == 32 and p.stages == 3
 
 
+def test_plan_issue_form(lib, tune):
+    """Packed FMA issue on A^T plans and on split-K plans without the pass;
+    scalar issue on other plans; the knob overrides."""
+    assert plan(8192, 8192, 8192).kernel == 1            # A^T grid
+    assert plan(2048, 2048, 2048).kernel == 1            # A^T + stream-K
+    assert plan(1024, 1024, 1024).kernel == 1            # split-K, no pass
+    assert plan(1024, 2304, 768).kernel == 0             # one tile per SM, no split
+    assert plan(8192, 8192, 64).kernel == 0              # unsplit grid, no pass
+    tune(kernel=0)
+    assert plan(8192, 8192, 8192).kernel == 0
+    assert plan(1024, 1024, 1024).kernel == 0
+    tune(kernel=2)
+    assert plan(8192, 8192, 8192).kernel == 2
+
+
 def test_plan_tail_split_is_opt_in(lib, tune):
     tune(tail_split="2")
     p = plan(8192, 8192, 8192)

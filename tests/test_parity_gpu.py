@@ -315,6 +315,30 @@ def test_both_kernels_bit_identical(sg, tune):
         assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
 
 
+@pytest.mark.parametrize("M,N,K,lds,dist,knobs", [
+    (2048, 1024, 512, None, "uniform", dict(transpose_a=1, schedule=0, split_k=1)),  # A^T grid
+    (2046, 1030, 515, (516, 1032, 1036), "uniform", dict(transpose_a=1, schedule=0)),  # checked
+    (1536, 1024, 1024, None, "int4", {}),                  # as planned: A^T + split-K
+    (1024, 1024, 1024, None, "uniform", dict(transpose_a=1, schedule=1)),  # A^T + stream-K
+    (1280, 2048, 2048, None, "int4", {}),                  # as planned: A^T + stream-K
+])
+def test_packed_issue_on_transposed_a_plans(sg, tune, M, N, K, lds, dist, knobs):
+    """A^T plans issue their FMAs packed by default; scalar issue (tuning
+    knob kernel = 0) gives the same C bit for bit, and both match the oracle."""
+    tune(**knobs)
+    lda, ldb, ldc = lds if lds else (None, None, None)
+    p = workloads.make(M, N, K, dist=dist, seed=71, lda=lda, ldb=ldb, ldc=ldc,
+                       alpha=1.5 if dist == "int4" else 0.75, beta=0.5,
+                       c0_dist="int4" if dist == "int4" else "uniform")
+    plan = sg.gemm_plan_for_sms(p.M, p.N, p.K, p.lda, p.ldb, p.ldc)
+    assert plan.transpose_a == 1 and plan.kernel == 1
+    outs = []
+    for kernel in (None, 0):
+        tune(kernel=kernel)
+        outs.append(run_and_check(sg, p, exact=dist == "int4"))
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+
+
 def test_deterministic_run_to_run(sg):
     for name in ("long_k", "ragged", "gpt2_mlp_down"):
         p = workloads.workload(name)
