@@ -309,29 +309,28 @@ void plan_core(int64_t M, int64_t N, int64_t K, int64_t batch, bool vec, int sms
 // operand whose stored rows run along K (A as given) through registers and
 // transposing shared stores, and copies one whose rows run along M (A^T)
 // straight in with cp.async, which leaves it 8 registers and ~10
-// instructions per K slice lighter, and lets the product run in K slices of
-// 32 through a three-page ring.  A transpose pass costs 8*M*K bytes of HBM
-// traffic, about 35/N of the product's time.  Measured on GB300 (TFLOP/s,
-// without / with the pass): 8192^3 60.7 / 65.8, 4096^3 58.4 / 62.4, 2048^3
-// 48.7 / 50.9; it loses for K = 64 (47.5 / 46.7) and for short K on few
-// tiles (GPT-2 QKV, 144 tiles: 43.9 / 43.4).
+// instructions per K slice lighter, lets the product run in K slices of 32
+// through a three-page ring, and lets it issue its FMAs packed within 128
+// registers (choose_wide_kernel).  A transpose pass costs 8*M*K bytes of HBM
+// traffic, about 35/N of the product's time.
 //
-// Below one wave of 128-wide tiles (S = 2 resident CTAs per SM) the choice is
-// three-way: split-K without the pass (kTransposeNone), the pass and one CTA
-// per tile or K range (kTransposeGrid), or the pass and a persistent
-// stream-K launch (kTransposeStreamK).  Measured on GB300 (N = 1024 and
-// 2048, 32..256 tiles, K = 768..4096; microseconds, L2 flushed): the pass
-// wins from K = 1024 on for 96 tiles and more (2560x1024x1024: 150 without,
-// 139 with); stream-K after the pass wins for K >= 4096 on any grid up to
-// 0.7 S, for K >= 2048 from 0.3 S to 0.7 S and for K >= 1024 from 0.5 S to
-// 0.7 S (1280x2048x2048, 160 tiles: 279 split-K, 233 grid, 212 stream-K;
-// 512x2048x4096: 194 / 181 / 171); between 0.7 S and S the plain grid after
-// the pass is the fastest (1792x2048x2048, 224 tiles: 271 grid, 287
-// stream-K; 4480x1024x2048, 280 tiles: 345 / 359) except from 0.75 S to
-// 0.875 S with K >= 2048, where stream-K gains 1-6 % (2048^3, 256 tiles:
-// 338 / 324; 3968x1024x2048, 248 tiles: 343 / 324; 4224x1024x4096, 264
-// tiles: 675 / 654); with K = 768, or K = 1024 on under 0.3 S tiles,
-// split-K without the pass (1024^3: 57 / 59 / 63).
+// Three plans compete: split-K without the pass (kTransposeNone), the pass
+// and one CTA per tile or K range (kTransposeGrid), the pass and a
+// persistent stream-K launch (kTransposeStreamK).  Measured on GB300 with
+// packed issue (N = 768, 1024 and 2048, 32..1216 tiles of 128, K = 64..4096;
+// microseconds, L2 flushed; none / grid / stream-K):
+//  * the pass pays for K >= 256 from 0.45 of a wave (S = 2 CTAs per SM) on:
+//    1152x2048x768, 144 tiles: 82.6 / 70.3 / 88.7; 9728x2048x512, 1216
+//    tiles: 356 / 318 / 371; for K < 256 only on grids of 8 waves and more
+//    (8192x8192x64: 181 / 173);
+//  * for K >= 1024 it pays except on small grids: under 0.3 S at K = 1024
+//    (1024^3: 57 / 57 / 63) and under 0.15 S at larger K (256x2048x2048:
+//    55.9 / 56.0 / 62.0);
+//  * stream-K after the pass beats the grid where the grid would put a
+//    second CTA on only a few SMs, from sms to 1.25 sms tiles (2560x1024x2048,
+//    160 tiles: 252 / 225 / 215); elsewhere the grid wins (2048^3: 353 /
+//    316 / 320; 1792x2048x2048, 224 tiles: 277 / 260 / 286; 1024x1024x16384,
+//    64 tiles split along K: 612 against 620 stream-K).
 // Tuning knobs: kKnobTransposeA (0/1) forces the pass off or on,
 // kKnobSchedule (0/1) the grid or stream-K after it.
 enum TransposeFamily { kTransposeNone = 0, kTransposeGrid = 1, kTransposeStreamK = 2 };
@@ -342,23 +341,18 @@ int choose_transpose_a(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, in
     if (!able) return kTransposeNone;
     const int64_t tiles = p.tiles_m * p.tiles_n;
     const int64_t S = int64_t(sms) * kCtasPerSm;
-    const bool k_split = p.split_k > 1 || p.schedule == 1;
-    const bool one_per_sm = !k_split && tiles >= sms;
     int want = kTransposeNone;
-    if (N >= 1024 && K >= 256) {
-        if (10 * tiles > 7 * S)
-            want = (K >= 2048 && 4 * tiles > 3 * S && 8 * tiles <= 7 * S)
-                       ? kTransposeStreamK
-                       : ((K >= 1024 || one_per_sm) ? kTransposeGrid : kTransposeNone);
-        else if (K >= 4096)
+    if (N >= 768) {
+        if (K < 256)
+            want = tiles >= 8 * S ? kTransposeGrid : kTransposeNone;
+        else if (K < 1024)
+            want = 20 * tiles >= 9 * S ? kTransposeGrid : kTransposeNone;
+        else if (tiles > sms && 4 * tiles <= 5 * int64_t(sms))
             want = kTransposeStreamK;
-        else if (K >= 2048)
-            want = 10 * tiles >= 3 * S ? kTransposeStreamK : kTransposeGrid;
-        else if (K >= 1024)
-            want = 2 * tiles > S ? kTransposeStreamK
-                                 : (10 * tiles >= 3 * S ? kTransposeGrid : kTransposeNone);
+        else if (K < 2048)
+            want = 10 * tiles >= 3 * S ? kTransposeGrid : kTransposeNone;
         else
-            want = one_per_sm ? kTransposeGrid : kTransposeNone;
+            want = 20 * tiles >= 3 * S ? kTransposeGrid : kTransposeNone;
     }
     const int32_t f = tuning(kKnobTransposeA);
     if (f == 0) return kTransposeNone;

@@ -126,11 +126,12 @@ def test_plan_full_tiles_take_the_unchecked_vector_path(lib):
 def test_plan_transpose_choice(lib, tune):
     assert plan(4096, 4096, 4096).transpose_a == 1
     assert plan(2048, 2048, 2048).transpose_a == 1        # 256 tiles, more than one per SM
-    assert plan(1024, 2304, 768).transpose_a == 0         # 144 tiles, under one per SM
-    assert plan(1024, 1024, 16384).transpose_a == 1       # split-K with long K
-    assert plan(8192, 8192, 64).transpose_a == 0         # K too short to pay for the pass
-    assert plan(1024, 1024, 1024).transpose_a == 0        # split-K plan, short K
-    assert plan(4096, 512, 4096).transpose_a == 0         # N < 1024
+    assert plan(1024, 2304, 768).transpose_a == 1         # 144 tiles (>= 0.45 of a wave)
+    assert plan(1024, 1024, 16384).transpose_a == 1       # long K
+    assert plan(8192, 8192, 64).transpose_a == 1          # K = 64 on 13 waves
+    assert plan(2048, 2048, 64).transpose_a == 0          # K = 64 on under 8 waves
+    assert plan(1024, 1024, 1024).transpose_a == 0        # 64 tiles, K = 1024
+    assert plan(4096, 512, 4096).transpose_a == 0         # N < 768
     assert plan(4096, 4096, 4096, A=4100).transpose_a == 0   # not vector-aligned
     tune(transpose_a="0")
     q = plan(8192, 8192, 8192)
@@ -143,21 +144,25 @@ def test_plan_transpose_choice(lib, tune):
 
 @pytest.mark.parametrize("M,N,K,family", [
     # one wave of 128-wide tiles is S = 304 resident CTAs on 152 SMs
-    (1024, 1024, 1024, "none"),        # 64 tiles, K = 1024: split-K, no pass
+    (1024, 1024, 1024, "none"),        # 64 tiles (< 0.3 S), K = 1024: split-K, no pass
     (1536, 1024, 1024, "grid"),        # 96 tiles (>= 0.3 S), K = 1024
-    (2560, 1024, 1024, "stream_k"),    # 160 tiles (> 0.5 S), K = 1024
-    (512, 2048, 2048, "grid"),         # 64 tiles (< 0.3 S), K = 2048
-    (1280, 2048, 2048, "stream_k"),    # 160 tiles, K = 2048
-    (512, 2048, 4096, "stream_k"),     # 64 tiles, K = 4096
-    (1792, 2048, 2048, "grid"),        # 224 tiles (> 0.7 S): the grid
-    (2048, 2048, 2048, "stream_k"),    # 256 tiles (0.75 S .. 0.875 S, K >= 2048)
-    (2048, 2048, 1024, "grid"),        # the same grid with K = 1024
-    (4480, 1024, 2048, "grid"),        # 280 tiles (> 0.875 S)
-    (1024, 2304, 768, "none"),         # 144 tiles, K = 768
-    (1024, 3072, 768, "none"),         # 192 tiles, K = 768, split-K
-    (1024, 1024, 16384, "stream_k"),   # 64 tiles, long K
+    (2560, 1024, 1024, "stream_k"),    # 160 tiles: just over one CTA per SM
+    (2560, 1024, 4096, "stream_k"),
+    (256, 2048, 2048, "none"),         # 32 tiles (< 0.15 S), K = 2048
+    (512, 2048, 2048, "grid"),         # 64 tiles, K = 2048
+    (1280, 2048, 768, "grid"),         # 160 tiles, K = 768: the grid (stream-K needs K >= 1024)
+    (1536, 2048, 2048, "grid"),        # 192 tiles (> 1.25 sms)
+    (1792, 2048, 2048, "grid"),        # 224 tiles
+    (2048, 2048, 2048, "grid"),        # 256 tiles
+    (4480, 1024, 2048, "grid"),        # 280 tiles
+    (1024, 2304, 768, "grid"),         # 144 tiles, K = 768
+    (1024, 3072, 768, "grid"),         # 192 tiles, K = 768
+    (1024, 768, 3072, "grid"),         # 48 tiles, N = 768, K = 3072
+    (768, 1024, 768, "none"),          # 48 tiles, K = 768 (< 0.45 S)
+    (1024, 1024, 16384, "grid"),       # 64 tiles, long K: split along K after the pass
     (4096, 4096, 4096, "grid"),        # several waves
-    (2048, 768, 4096, "none"),         # N < 1024: the pass costs too much
+    (8192, 8192, 64, "grid"),          # 13 waves of K = 64
+    (2048, 512, 4096, "none"),         # N < 768: the pass costs too much
 ])
 def test_plan_transpose_family_bands(lib, M, N, K, family):
     """Below one wave, the pass over A and the schedule after it follow the
@@ -173,10 +178,9 @@ def test_plan_issue_form(lib, tune):
     """Packed FMA issue on A^T plans and on split-K plans without the pass;
     scalar issue on other plans; the knob overrides."""
     assert plan(8192, 8192, 8192).kernel == 1            # A^T grid
-    assert plan(2048, 2048, 2048).kernel == 1            # A^T + stream-K
+    assert plan(2560, 1024, 2048).kernel == 1            # A^T + stream-K
     assert plan(1024, 1024, 1024).kernel == 1            # split-K, no pass
-    assert plan(1024, 2304, 768).kernel == 0             # one tile per SM, no split
-    assert plan(8192, 8192, 64).kernel == 0              # unsplit grid, no pass
+    assert plan(2048, 2048, 64).kernel == 0              # unsplit grid, no pass
     tune(kernel=0)
     assert plan(8192, 8192, 8192).kernel == 0
     assert plan(1024, 1024, 1024).kernel == 0
@@ -350,12 +354,12 @@ def test_plan_schedule_choice(lib, tune):
     assert p.grid_ctas == 64 and p.workspace_bytes == 0
     p = plan(64, 64, 1000)           # K too long for it: 64-wide stream-K
     assert p.schedule == 1 and p.bm == 64 and p.bk == 8 and p.stages == 4
-    q = plan(1024, 1024, 16384)      # 64 tiles, K = 16384: A transposed, then stream-K
-    assert q.schedule == 1 and q.transpose_a == 1 and q.bk == 32 and q.stages == 3
-    r = plan(2048, 2048, 2048)       # 256 tiles, 0.84 of a wave: A transposed, then stream-K
+    q = plan(1024, 1024, 16384)      # 64 tiles, K = 16384: A transposed, then split-K
+    assert q.schedule == 0 and q.transpose_a == 1 and q.bk == 32 and q.split_k > 1
+    r = plan(2560, 1024, 2048)       # 160 tiles, just over one per SM: A^T, then stream-K
     assert r.schedule == 1 and r.transpose_a == 1
-    for shape in [(1024, 1024, 1024), (1023, 777, 513), (1024, 2304, 768), (4096, 4096, 4096),
-                  (8192, 8192, 8192), (8192, 8192, 64)]:
+    for shape in [(1024, 1024, 1024), (1023, 777, 513), (1024, 2304, 768), (2048, 2048, 2048),
+                  (4096, 4096, 4096), (8192, 8192, 8192), (8192, 8192, 64)]:
         assert plan(*shape).schedule == 0, shape
     tune(schedule=0)
     assert plan(256, 256, 256).schedule == 0
