@@ -46,8 +46,10 @@ METRIC = "SGEMM TFLOP/s (2MNK/t) at M=N=K=8192 fp32; % of GB300 FP32 FFMA peak"
 UNIT = "TFLOP/s"
 FMA_PER_SM_PER_CLK = 128      # fp32 FMA lanes per SM (4 sub-partitions x 32)
 L2_BYTES = 129 * 1000 * 1000
+# the headline product (kernel template, the translation unit that builds
+# its packed A^T instantiation, the argument structs) and the transpose pass
 KERNEL_SOURCES = [os.path.join(ROOT, "dense_fp32_matrix_06_gb300", "csrc", f)
-                  for f in ("ffma_kernel.cuh", "ffma_gemm.cu", "ffma_gemm_tn.cu",
+                  for f in ("ffma_kernel.cuh", "ffma_gemm_tn_packed.cu", "ffma_gemm.cu",
                             "sgemm_internal.h")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 

@@ -335,25 +335,22 @@ void plan_core(int64_t M, int64_t N, int64_t K, int64_t batch, bool vec, int sms
 // kKnobSchedule (0/1) the grid or stream-K after it.
 enum TransposeFamily { kTransposeNone = 0, kTransposeGrid = 1, kTransposeStreamK = 2 };
 
+// The bands above, for `tiles` 128-wide tiles (over all batches) and K.
+int transpose_band(int64_t tiles, int64_t K, int sms) {
+    const int64_t S = int64_t(sms) * kCtasPerSm;
+    if (K < 256) return tiles >= 8 * S ? kTransposeGrid : kTransposeNone;
+    if (K < 1024) return 20 * tiles >= 9 * S ? kTransposeGrid : kTransposeNone;
+    if (tiles > sms && 4 * tiles <= 5 * int64_t(sms)) return kTransposeStreamK;
+    if (K < 2048) return 10 * tiles >= 3 * S ? kTransposeGrid : kTransposeNone;
+    return 20 * tiles >= 3 * S ? kTransposeGrid : kTransposeNone;
+}
+
 int choose_transpose_a(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int sms) {
     const bool able = p.bm == 128 && p.tail_split == 1 && p.vec && K >= 1 &&
                       M <= int64_t(65535) * 32;
     if (!able) return kTransposeNone;
     const int64_t tiles = p.tiles_m * p.tiles_n;
-    const int64_t S = int64_t(sms) * kCtasPerSm;
-    int want = kTransposeNone;
-    if (N >= 768) {
-        if (K < 256)
-            want = tiles >= 8 * S ? kTransposeGrid : kTransposeNone;
-        else if (K < 1024)
-            want = 20 * tiles >= 9 * S ? kTransposeGrid : kTransposeNone;
-        else if (tiles > sms && 4 * tiles <= 5 * int64_t(sms))
-            want = kTransposeStreamK;
-        else if (K < 2048)
-            want = 10 * tiles >= 3 * S ? kTransposeGrid : kTransposeNone;
-        else
-            want = 20 * tiles >= 3 * S ? kTransposeGrid : kTransposeNone;
-    }
+    int want = N >= 768 ? transpose_band(tiles, K, sms) : int(kTransposeNone);
     const int32_t f = tuning(kKnobTransposeA);
     if (f == 0) return kTransposeNone;
     if (f == 1 && want == kTransposeNone)
@@ -381,17 +378,20 @@ size_t transpose_workspace(const gemm_plan_t &p, int64_t M, int64_t K, int64_t *
     return *at_offset + transpose_bytes(M, K, ld);
 }
 
-// sgemm_ex's transposed copies: the same rule as choose_transpose_a, for each
-// operand to be copied (A's copy costs 8*M*K bytes against 2*M*N*K FLOPs, so
-// it needs N >= 1024; B's needs M >= 1024), on 128-wide one-CTA-per-tile
-// plans that fill the GPU (or split long K).
+// sgemm_ex's transposed copies: the bands of choose_transpose_a over all
+// the batches' tiles, for each operand to be copied (A's copy costs 8*M*K
+// bytes against 2*M*N*K FLOPs, so it needs N >= 768; B's needs M >= 768), on
+// 128-wide one-CTA-per-(tile, K range) plans; where the bands ask for
+// stream-K after the pass, sgemm_ex runs the grid after it.  With op(A) =
+// A^T and op(B) = B nothing is copied: the pass is only the switch to the
+// direct-copy kernel (K slices of 32).
 bool ex_transpose_first(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int64_t batch,
                         bool copy_a, bool copy_b, int sms) {
     const bool able = p.schedule == 0 && p.bm == 128 && p.tail_split == 1 && p.vec &&
                       batch <= 65535 && M <= int64_t(65535) * 32 && N <= int64_t(65535) * 32;
     const int64_t tiles = p.tiles_m * p.tiles_n * batch;
-    bool want = able && K >= 256 && (!copy_a || N >= 1024) && (!copy_b || M >= 1024) &&
-                ((p.split_k == 1 && tiles >= sms) || (p.split_k > 1 && K >= 8192));
+    bool want = able && (!copy_a || N >= 768) && (!copy_b || M >= 768) &&
+                transpose_band(tiles, K, sms) != kTransposeNone;
     const int f = tuning(kKnobTransposeA);
     if (f == 0) want = false;
     if (f == 1) want = able;
@@ -680,7 +680,7 @@ sgemm_status run(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K, float
         else if (plan.kernel == kKernelFfma16x8)
             e = launch_ffma16x8(a, plan.edge != 0, false, stream);
         else if (packed)
-            e = launch_ffma_tn_wide_packed(a, plan.vec != 0, plan.edge != 0, stream);
+            e = launch_ffma_tn_wide_packed(a, plan.vec != 0, plan.edge != 0, false, stream);
         else
             e = launch_ffma_tn_wide(a, plan.vec != 0, plan.edge != 0, false, stream);
         return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
@@ -1075,7 +1075,13 @@ extern "C" sgemm_status sgemm_ex(int32_t op_a, int32_t op_b, int64_t M, int64_t 
                      aligned16(C) && aligned16(bias);
     gemm_plan_t plan;
     plan_core(M, N, K, batch, vec, sms, &plan, ta && !tb);
-    if (ta || tb) plan.kernel = kKernelFfma128;   // the packed form exists for op N, N only
+    const bool ext = batch > 1 || bias != nullptr || act != SGEMM_ACT_NONE;
+    // packed issue without the pass: split-K plans of plain op N, N products
+    // (as sgemm); the other layouts and the fused epilogue stage A or B^T
+    // through registers with scalar issue
+    if (ta || tb || ext) plan.kernel = kKernelFfma128;
+    else if (plan.schedule == 0 && plan.bm == 128 && plan.split_k > 1 && tuning(kKnobKernel) < 0)
+        plan.kernel = kKernelFfma2x128;
     // Large grids: the operands whose stored rows run along K (A as given,
     // B^T) are first copied transposed into the workspace, so the product
     // runs with both operands copied directly, in K slices of 32 -- what
@@ -1137,7 +1143,6 @@ extern "C" sgemm_status sgemm_ex(int32_t op_a, int32_t op_b, int64_t M, int64_t 
     if (plan.workspace_bytes > 0)
         a.partials = reinterpret_cast<float *>(static_cast<char *>(ws) + kCounterBytes);
     if (plan.schedule == 1) {
-        const bool ext = batch > 1 || bias != nullptr || act != SGEMM_ACT_NONE;
         if (ta && !tb && plan.bm == 128)   // both operands direct: the split-K kernel's loop
             e = launch_ffma_tn_wide_sk(sk_gemm_args(plan, a, ws), plan.grid_ctas, plan.vec != 0,
                                        plan.edge != 0, ext, st);
@@ -1166,12 +1171,9 @@ extern "C" sgemm_status sgemm_ex(int32_t op_a, int32_t op_b, int64_t M, int64_t 
             a.ldb = ldb_t;
             a.strideB = sb_t;
         }
-        const bool ext = batch > 1 || bias != nullptr || act != SGEMM_ACT_NONE;
-        // (packed issue is built for plain products; batches, bias and GELU
-        // run the scalar build)
         e = plan.kernel == kKernelFfma16x8 ? launch_ffma16x8(a, plan.edge != 0, ext, st)
-            : (plan.kernel == kKernelFfma2x128 && !ext)
-                ? launch_ffma_tn_wide_packed(a, plan.vec != 0, plan.edge != 0, st)
+            : plan.kernel == kKernelFfma2x128
+                ? launch_ffma_tn_wide_packed(a, plan.vec != 0, plan.edge != 0, ext, st)
                 : launch_ffma_tn_wide(a, plan.vec != 0, plan.edge != 0, ext, st);
         return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
     }

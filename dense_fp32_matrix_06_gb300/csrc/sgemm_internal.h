@@ -204,8 +204,8 @@ size_t tiny_smem_bytes(int64_t K);
 // The 16 x 8 per-thread kernel (ffma_wide.cu): op(A) = A^T, op(B) = B, 128
 // tiles, K slices of 32, no split.
 cudaError_t launch_ffma16x8(const GemmArgs &a, bool edge, bool ext, cudaStream_t stream);
-// The same two schedules with packed FMA issue (plain products only).
-cudaError_t launch_ffma_tn_wide_packed(const GemmArgs &a, bool vec, bool edge,
+// The same two schedules with packed FMA issue (stream-K: plain products only).
+cudaError_t launch_ffma_tn_wide_packed(const GemmArgs &a, bool vec, bool edge, bool ext,
                                        cudaStream_t stream);
 cudaError_t launch_ffma_tn_wide_sk_packed(const GemmArgs &a, int64_t grid, bool vec, bool edge,
                                           cudaStream_t stream);

@@ -239,6 +239,24 @@ def test_transposed_copies_first(sg, tune, op_a, op_b, batch, shared_b):
 
 
 @pytest.mark.parametrize("op_a,op_b", LAYOUTS)
+@pytest.mark.parametrize("batch,bias,act", [(1, False, 0), (2, True, 1)])
+def test_transposed_copies_packed_issue_bit_identical(sg, tune, op_a, op_b, batch, bias, act):
+    """The direct-copy product issues its FMAs packed by default (plain and
+    with batches, bias and GELU); scalar issue (tuning knob kernel = 0) gives
+    the same C bit for bit, and both match the oracle."""
+    tune(transpose_a=1, tile=128, schedule=0)
+    p = ExProblem(op_a, op_b, 300, 260, 530, batch, seed=95, alpha=0.75, beta=0.5, bias=bias,
+                  act=act, pad=4, aligned=True)
+    outs = []
+    for kernel in (None, 0):
+        tune(kernel=kernel)
+        out = p.run(sg)
+        p.check(out, exact=False)
+        outs.append(out)
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+
+
+@pytest.mark.parametrize("op_a,op_b", LAYOUTS)
 def test_sixteen_by_eight_kernel_ex(sg, tune, op_a, op_b):
     """sgemm_ex's direct-copy plans on the 16 x 8 per-thread kernel (forced),
     batched with bias and GELU, and exact on integers."""
