@@ -150,10 +150,14 @@ cudaError_t launch_ffma(const GemmArgs &a, int kernel, int tile, bool vec, bool 
                                 : launch_ffma_tn(a, tile, vec, edge, stream);
     if (trans_b) return launch_ffma_nt(a, tile, vec, edge, stream);
     const bool ext = a.batch > 1 || a.bias != nullptr || a.act != kActNone;
-    if (tile == kSmallTile)
-        return ext ? ffma::launch_layout<kSmallTile, false, false, false, true>(a, vec, edge, stream)
+    if (tile == kSmallTile) {
+        if (ext)
+            return ffma::launch_layout<kSmallTile, false, false, false, true>(a, vec, edge, stream);
+        return kernel == kKernelFfma2x128
+                   ? ffma::launch_layout<kSmallTile, true, false, false, false>(a, vec, edge, stream)
                    : ffma::launch_layout<kSmallTile, false, false, false, false>(a, vec, edge,
                                                                                  stream);
+    }
     // Plain products can run either instantiation (the extended one with
     // batch 1, no bias, no activation computes the same thing).  ptxas
     // allocates the two differently, and measured on GB300 neither wins

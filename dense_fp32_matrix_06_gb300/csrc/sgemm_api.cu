@@ -271,7 +271,7 @@ void plan_core(int64_t M, int64_t N, int64_t K, int64_t batch, bool vec, int sms
     const int bk = tile / 8;
     const int cps = tile == kSmallTile ? kSmallCtasPerSm : kCtasPerSm;
     p.mode = SGEMM_MODE_FFMA;
-    p.kernel = tile == kSmallTile ? kKernelFfma128 : default_kernel();
+    p.kernel = default_kernel();
     p.bm = tile;
     p.bn = tile;
     p.bk = bk;
@@ -509,14 +509,16 @@ sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb
         q.workspace_bytes = transpose_workspace(q, M, K, &q.a_t_ld, &at_offset);
         return SGEMM_OK;
     }
-    // Split-K plans of 128-wide tiles without the pass issue their FMAs
-    // packed (fma.rn.f32x2; the same roundings in the same order, so the
-    // same C bit for bit).  Measured on GB300 (microseconds, scalar /
-    // packed): 1024^3 58.0 / 56.0, MLP-up 108.1 / 103.0, MLP-down 104.0 /
-    // 100.0, 1023x777x513 on 64-wide tiles unchanged; unsplit grids lose
-    // (GPT-2 QKV 82.6 / 105.1, 8192x8192x64 181 / 201), so they stay scalar.
+    // Without the pass, split-K plans of 128-wide tiles and every 64-wide
+    // plan issue their FMAs packed (fma.rn.f32x2; the same roundings in the
+    // same order, so the same C bit for bit).  Measured on GB300
+    // (microseconds, scalar / packed): 1024^3 58.0 / 56.0, MLP-up 108.1 /
+    // 103.0, MLP-down 104.0 / 100.0; 64-wide tiles: 1023x777x513 37.5 / 34.5,
+    // 768^3 74.4 / 70.3, 1000x1000x300 29.3 / 28.3.  Unsplit 128-wide grids
+    // lose (GPT-2 QKV 82.6 / 105.1, 8192x8192x64 181 / 201): they stay
+    // scalar.
     gemm_plan_t &q = *out;
-    if (q.schedule == 0 && q.bm == 128 && q.split_k > 1 && tuning(kKnobKernel) < 0)
+    if (q.schedule == 0 && (q.bm == kSmallTile || q.split_k > 1) && tuning(kKnobKernel) < 0)
         q.kernel = kKernelFfma2x128;
     return SGEMM_OK;
 }
@@ -719,7 +721,7 @@ bool plan_matches(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int64_t
     const int t = p.bm;
     if ((t != 128 && t != kSmallTile) || p.bn != t || p.threads != (t / 8) * (t / 8))
         return false;
-    if (t == kSmallTile && p.kernel != kKernelFfma128) return false;
+    if (t == kSmallTile && p.kernel == kKernelFfma16x8) return false;
     if (p.tiles_m != ceil_div(M, t) || p.tiles_n != ceil_div(N, t)) return false;
     const int64_t tiles = p.tiles_m * p.tiles_n;
     if (p.schedule != 0 && p.schedule != 1) return false;
@@ -1076,11 +1078,12 @@ extern "C" sgemm_status sgemm_ex(int32_t op_a, int32_t op_b, int64_t M, int64_t 
     gemm_plan_t plan;
     plan_core(M, N, K, batch, vec, sms, &plan, ta && !tb);
     const bool ext = batch > 1 || bias != nullptr || act != SGEMM_ACT_NONE;
-    // packed issue without the pass: split-K plans of plain op N, N products
-    // (as sgemm); the other layouts and the fused epilogue stage A or B^T
-    // through registers with scalar issue
+    // packed issue without the pass: 64-wide and split-K plans of plain op
+    // N, N products (as sgemm); the other layouts and the fused epilogue
+    // stage A or B^T through registers with scalar issue
     if (ta || tb || ext) plan.kernel = kKernelFfma128;
-    else if (plan.schedule == 0 && plan.bm == 128 && plan.split_k > 1 && tuning(kKnobKernel) < 0)
+    else if (plan.schedule == 0 && (plan.bm == kSmallTile || plan.split_k > 1) &&
+             tuning(kKnobKernel) < 0)
         plan.kernel = kKernelFfma2x128;
     // Large grids: the operands whose stored rows run along K (A as given,
     // B^T) are first copied transposed into the workspace, so the product

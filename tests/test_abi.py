@@ -180,7 +180,8 @@ def test_plan_issue_form(lib, tune):
     assert plan(8192, 8192, 8192).kernel == 1            # A^T grid
     assert plan(2560, 1024, 2048).kernel == 1            # A^T + stream-K
     assert plan(1024, 1024, 1024).kernel == 1            # split-K, no pass
-    assert plan(2048, 2048, 64).kernel == 0              # unsplit grid, no pass
+    assert plan(2048, 2048, 64).kernel == 0              # unsplit 128-wide grid, no pass
+    assert plan(1023, 777, 513, lda=513, ldb=777, ldc=777).kernel == 1   # 64-wide tiles
     tune(kernel=0)
     assert plan(8192, 8192, 8192).kernel == 0
     assert plan(1024, 1024, 1024).kernel == 0

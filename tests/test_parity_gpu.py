@@ -206,7 +206,7 @@ def test_empty_shapes_are_no_ops(sg):
     assert bool((c == 3.0).all())
 
 
-@pytest.mark.parametrize("kernel,tile", [("0", "128"), ("1", "128"), ("0", "64")])
+@pytest.mark.parametrize("kernel,tile", [("0", "128"), ("1", "128"), ("0", "64"), ("1", "64")])
 @pytest.mark.parametrize("split", ["1", "2", "3", "7"])
 def test_forced_kernel_and_split(sg, tune, kernel, tile, split):
     tune(kernel=kernel)
@@ -300,8 +300,9 @@ def test_transposed_a_with_caller_workspace(sg, tune):
     assert e.value.status == 7
 
 
-def test_both_kernels_bit_identical(sg, tune):
-    tune(tile="128")
+@pytest.mark.parametrize("tile", ["128", "64"])
+def test_both_kernels_bit_identical(sg, tune, tile):
+    tune(tile=tile)
     outs = []
     for kernel in ("0", "1"):
         tune(kernel=kernel)
