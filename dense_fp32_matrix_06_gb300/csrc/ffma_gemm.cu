@@ -31,6 +31,7 @@ __global__ void transpose_kernel(const float *__restrict__ A, int64_t M, int64_t
                                  float *__restrict__ At, int64_t ldt, int64_t stride_a,
                                  int64_t stride_t) {
     __shared__ float tile[32][33];
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");   // as transpose64_kernel
     A += int64_t(blockIdx.z) * stride_a;    // batch z
     At += int64_t(blockIdx.z) * stride_t;
     const int64_t m0 = int64_t(blockIdx.y) * 32, k0 = int64_t(blockIdx.x) * 32;
@@ -56,6 +57,10 @@ __global__ void __launch_bounds__(256) transpose64_kernel(const float *__restric
                                                           float *__restrict__ At, int64_t ldt,
                                                           int64_t stride_a, int64_t stride_t) {
     __shared__ float tile[64][65];
+    // the product that reads A^T is launched as a programmatic dependent: its
+    // CTAs may be scheduled once every CTA of this grid has started (they wait
+    // for this grid's completion before reading)
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     A += int64_t(blockIdx.z) * stride_a;    // batch z
     At += int64_t(blockIdx.z) * stride_t;
     const int64_t m0 = int64_t(blockIdx.y) * 64, k0 = int64_t(blockIdx.x) * 64;

@@ -255,6 +255,11 @@ ffma_gemm_kernel(const GemmArgs p) {
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
+    // A^T plans follow the transpose pass as its programmatic dependent: wait
+    // until that grid has completed and its writes are visible (a no-op when
+    // the launch has no such dependency)
+    if constexpr (kTransA) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+
     // stream-K segment state (kSched = 1), advanced by thread 0 between two
     // barriers so it occupies no registers across the main loop
     __shared__ long long s_sk_it, s_sk_tile;
@@ -857,9 +862,12 @@ cudaError_t launch_partial_reduce(const ReduceArgs &r, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, partial_reduce_kernel<kTile, kVec, kEdge, kExt>, r);
 }
 
+// `pdl`: launch as a programmatic dependent of the previous kernel on the
+// stream (the transpose pass of an A^T plan; the kernel waits for it).
 template <int kTile, bool kPacked, bool kVec, bool kEdge, bool kSplit, bool kTransA,
           bool kTransB, bool kExt, int kBKT = kTile / 8, int kSched = 0>
-cudaError_t launch_variant(const GemmArgs &a, cudaStream_t stream, int64_t sk_grid = 0) {
+cudaError_t launch_variant(const GemmArgs &a, cudaStream_t stream, int64_t sk_grid = 0,
+                           bool pdl = false) {
     using TC = TileCfg<kTile, kBKT>;
     auto kernel = ffma_gemm_kernel<kTile, kPacked, kVec, kEdge, kSplit, kTransA, kTransB, kExt,
                                    kBKT, kSched>;
@@ -876,8 +884,21 @@ cudaError_t launch_variant(const GemmArgs &a, cudaStream_t stream, int64_t sk_gr
                                 : unsigned(a.tail_start * a.split_k +
                                            (tiles - a.tail_start) * a.tail_split),
                     1, 1);
-    kernel<<<grid, TC::kThreads, dyn, stream>>>(a);
-    {
+    if (pdl) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(TC::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = size_t(dyn);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a);
+        if (e != cudaSuccess) return e;
+    } else {
+        kernel<<<grid, TC::kThreads, dyn, stream>>>(a);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

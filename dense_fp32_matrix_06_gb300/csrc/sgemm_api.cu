@@ -625,7 +625,8 @@ SkArgs sk_args(const gemm_plan_t &plan, const GemmArgs &a, void *workspace) {
 
 sgemm_status run(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K, float alpha,
                  const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
-                 float *C, int64_t ldc, void *workspace, cudaStream_t stream) {
+                 float *C, int64_t ldc, void *workspace, cudaStream_t stream,
+                 int sms) {
     if (M == 0 || N == 0) return SGEMM_OK;
     cudaError_t e;
     if (K == 0 || alpha == 0.0f) {
@@ -673,18 +674,21 @@ sgemm_status run(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K, float
         a.A = at;
         a.lda = plan.a_t_ld;
         const bool packed = plan.kernel == kKernelFfma2x128;
+        // the product as a programmatic dependent of the transpose pass, where
+        // its grid has more CTAs than SMs (ffma_gemm_tn.cu)
+        const bool pdl = plan.grid_ctas > sms;
         if (plan.schedule == 1)
             e = packed ? launch_ffma_tn_wide_sk_packed(sk_gemm_args(plan, a, workspace),
                                                        plan.grid_ctas, plan.vec != 0,
-                                                       plan.edge != 0, stream)
+                                                       plan.edge != 0, pdl, stream)
                        : launch_ffma_tn_wide_sk(sk_gemm_args(plan, a, workspace), plan.grid_ctas,
-                                                plan.vec != 0, plan.edge != 0, false, stream);
+                                                plan.vec != 0, plan.edge != 0, false, pdl, stream);
         else if (plan.kernel == kKernelFfma16x8)
             e = launch_ffma16x8(a, plan.edge != 0, false, stream);
         else if (packed)
-            e = launch_ffma_tn_wide_packed(a, plan.vec != 0, plan.edge != 0, false, stream);
+            e = launch_ffma_tn_wide_packed(a, plan.vec != 0, plan.edge != 0, false, pdl, stream);
         else
-            e = launch_ffma_tn_wide(a, plan.vec != 0, plan.edge != 0, false, stream);
+            e = launch_ffma_tn_wide(a, plan.vec != 0, plan.edge != 0, false, pdl, stream);
         return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
     }
     if (plan.schedule == 1) {
@@ -856,7 +860,7 @@ sgemm_status sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
         }
         if (s != SGEMM_OK) return s;
     }
-    return run(plan, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, ws, st);
+    return run(plan, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, ws, st, sms);
 }
 
 sgemm_status sgemm_with_plan(const gemm_plan_t *plan, int64_t M, int64_t N, int64_t K,
@@ -874,10 +878,11 @@ sgemm_status sgemm_with_plan(const gemm_plan_t *plan, int64_t M, int64_t N, int6
         if (!workspace || workspace_bytes < plan->workspace_bytes) return SGEMM_ERR_WORKSPACE;
         if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SGEMM_ERR_INVALID_ARG;
     }
-    s = current_device(nullptr, nullptr);
+    int sms = 0;
+    s = current_device(nullptr, &sms);
     if (s != SGEMM_OK) return s;
     return run(*plan, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, workspace,
-               static_cast<cudaStream_t>(stream));
+               static_cast<cudaStream_t>(stream), sms);
 }
 
 const char *sgemm_status_string(sgemm_status status) {
@@ -965,7 +970,7 @@ extern "C" sgemm_status sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alp
         // The buffer keeps whatever the previous call left, which is fine:
         // every partial tile is written before it is read back.
     }
-    return run(plan, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, ws, st);
+    return run(plan, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, ws, st, sms);
 }
 
 // ---------------------------------------------------------------------------
@@ -1148,7 +1153,7 @@ extern "C" sgemm_status sgemm_ex(int32_t op_a, int32_t op_b, int64_t M, int64_t 
     if (plan.schedule == 1) {
         if (ta && !tb && plan.bm == 128)   // both operands direct: the split-K kernel's loop
             e = launch_ffma_tn_wide_sk(sk_gemm_args(plan, a, ws), plan.grid_ctas, plan.vec != 0,
-                                       plan.edge != 0, ext, st);
+                                       plan.edge != 0, ext, false, st);
         else
             e = launch_ffma_sk(sk_args(plan, a, ws), plan.bm, plan.bk, plan.stages,
                                plan.vec != 0, ta, tb, ext, st);
@@ -1176,8 +1181,10 @@ extern "C" sgemm_status sgemm_ex(int32_t op_a, int32_t op_b, int64_t M, int64_t 
         }
         e = plan.kernel == kKernelFfma16x8 ? launch_ffma16x8(a, plan.edge != 0, ext, st)
             : plan.kernel == kKernelFfma2x128
-                ? launch_ffma_tn_wide_packed(a, plan.vec != 0, plan.edge != 0, ext, st)
-                : launch_ffma_tn_wide(a, plan.vec != 0, plan.edge != 0, ext, st);
+                ? launch_ffma_tn_wide_packed(a, plan.vec != 0, plan.edge != 0, ext,
+                                             plan.grid_ctas > sms, st)
+                : launch_ffma_tn_wide(a, plan.vec != 0, plan.edge != 0, ext, plan.grid_ctas > sms,
+                                      st);
         return e == cudaSuccess ? SGEMM_OK : cuda_fail(e, SGEMM_ERR_LAUNCH);
     }
     e = launch_ffma(a, plan.kernel, plan.bm, plan.vec != 0, plan.edge != 0, ta, tb, st);

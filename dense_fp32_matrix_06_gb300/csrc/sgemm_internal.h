@@ -131,7 +131,8 @@ enum KernelId : int32_t {
 // `dp_rounds` rounds of whole-K tiles handed out round-robin (tile r*G + g
 // to CTA g), then the K slices of the remaining tiles, cut into G equal
 // contiguous runs over (tile, slice) order.  A tile whose slices several
-// CTAs share is summed in a fixed order by the last of them to finish.
+// CTAs share is summed in a fixed order by partial_reduce_kernel, launched
+// after the persistent grid.
 struct SkArgs {
     const float *A;
     const float *B;
@@ -190,12 +191,14 @@ cudaError_t launch_ffma_tt(const GemmArgs &a, int tile, bool vec, bool edge, cud
 // transposed copies); split-K allowed; `ext` compiles in batches, bias and
 // activation.
 constexpr int kWideBK = 32;
-cudaError_t launch_ffma_tn_wide(const GemmArgs &a, bool vec, bool edge, bool ext,
+// `pdl`: launch as a programmatic dependent of the previous kernel on the
+// stream (the transpose pass), for grids of more CTAs than SMs.
+cudaError_t launch_ffma_tn_wide(const GemmArgs &a, bool vec, bool edge, bool ext, bool pdl,
                                 cudaStream_t stream);
 // The same kernel as a persistent stream-K launch of `grid` CTAs (the
 // stream-K fields of `a` set).
 cudaError_t launch_ffma_tn_wide_sk(const GemmArgs &a, int64_t grid, bool vec, bool edge, bool ext,
-                                   cudaStream_t stream);
+                                   bool pdl, cudaStream_t stream);
 // The small-problem kernel (ffma_tiny.cu): 32 x 32 tiles, the whole K range
 // (at most kTinyMaxK) staged at once, K split across the CTA's 8 warps.
 constexpr int64_t kTinyMaxK = 256;
@@ -206,9 +209,9 @@ size_t tiny_smem_bytes(int64_t K);
 cudaError_t launch_ffma16x8(const GemmArgs &a, bool edge, bool ext, cudaStream_t stream);
 // The same two schedules with packed FMA issue (stream-K: plain products only).
 cudaError_t launch_ffma_tn_wide_packed(const GemmArgs &a, bool vec, bool edge, bool ext,
-                                       cudaStream_t stream);
+                                       bool pdl, cudaStream_t stream);
 cudaError_t launch_ffma_tn_wide_sk_packed(const GemmArgs &a, int64_t grid, bool vec, bool edge,
-                                          cudaStream_t stream);
+                                          bool pdl, cudaStream_t stream);
 // At_b = A_b^T (K x M, row stride ldt) for b < batch, with A_b = A +
 // b*stride_a and At_b = At + b*stride_t; M <= 65535 * 32, batch <= 65535.
 cudaError_t launch_transpose(const float *A, int64_t M, int64_t K, int64_t lda, float *At,
