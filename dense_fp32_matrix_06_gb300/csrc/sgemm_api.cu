@@ -366,7 +366,7 @@ size_t transpose_bytes(int64_t M, int64_t K, int64_t *ld) {
     return (size_t(K) * size_t(*ld) * sizeof(float) + 255) / 256 * 256;
 }
 
-// Workspace of a transposing plan: [counters][split-K partials][A^T].
+// Workspace of a transposing plan: [reserved block][partial tiles][A^T].
 size_t transpose_workspace(const gemm_plan_t &p, int64_t M, int64_t K, int64_t *ld,
                            size_t *at_offset) {
     const int64_t tiles = p.tiles_m * p.tiles_n;
@@ -1093,7 +1093,7 @@ extern "C" sgemm_status sgemm_ex(int32_t op_a, int32_t op_b, int64_t M, int64_t 
     // Large grids: the operands whose stored rows run along K (A as given,
     // B^T) are first copied transposed into the workspace, so the product
     // runs with both operands copied directly, in K slices of 32 -- what
-    // sgemm does for A.  Layout: [counters][split-K partials][A^T][B].
+    // sgemm does for A.  Layout: [reserved block][partial tiles][A^T][B].
     // (op T/N needs no copy, only the longer K slice.)
     const bool copy_a = !ta, copy_b = tb;
     const bool pre = ex_transpose_first(plan, M, N, K, batch, copy_a, copy_b, sms);
