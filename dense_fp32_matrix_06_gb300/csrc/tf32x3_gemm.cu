@@ -314,8 +314,8 @@ struct TcArgs {
     // of kb_per_split blocks, tiles [tail_start, tiles) into `tail_split`
     // ranges of tail_kb_per_split (only the last, partly filled wave of tiles
     // is cut when split == 1).  The ranges of a tile are consecutive CTAs.
-    // Split tiles only: partial slot of CTA x is x - part_base, counter of
-    // tile t is counters[t - cnt_base].
+    // Split tiles only: partial slot of CTA x is x - part_base; flag of tile
+    // t is counters[t - cnt_base] (set only by a range whose waits expired).
     int32_t split;
     int32_t kb_per_split;
     int32_t tail_start;
@@ -323,7 +323,7 @@ struct TcArgs {
     int32_t tail_kb_per_split;
     int32_t part_base;
     int32_t cnt_base;
-    unsigned *counters;    // split > 1: one ticket per tile, zero on entry and exit
+    unsigned *counters;    // split tiles: one failure flag per tile, zero on entry and exit
     float *partials;       // split > 1: tiles * split partial tiles of 128 x BN
 };
 
@@ -392,7 +392,6 @@ tf32x3_mma_kernel(const __grid_constant__ CUtensorMap map_a_hi,
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     __shared__ int s_mma_ok;
-    __shared__ unsigned s_ticket;
 
     // (tile, K range) of this CTA; grouped raster over 8 tile rows
     const TcWork work = tc_work(p);
@@ -528,10 +527,11 @@ tf32x3_mma_kernel(const __grid_constant__ CUtensorMap map_a_hi,
             }
         }
     } else {
-        // partial tile of this K range: slot blockIdx.x, row-major 128 x BN
+        // partial tile of this K range: slot blockIdx.x, row-major 128 x BN;
+        // tc_reduce_kernel sums the tile's ranges after this launch
         const size_t slot = size_t(kTcBM) * BN;
-        float *part = p.partials + size_t(work.slot_first) * slot;
-        float *mine = part + size_t(split_idx) * slot + size_t(warp * 32 + lane) * BN;
+        float *mine = p.partials + (size_t(work.slot_first) + size_t(split_idx)) * slot +
+                      size_t(warp * 32 + lane) * BN;
         if (__all_sync(0xffffffffu, clean)) {
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -547,42 +547,12 @@ tf32x3_mma_kernel(const __grid_constant__ CUtensorMap map_a_hi,
                     __stcg(reinterpret_cast<float4 *>(mine + c0 + 4 * q),
                            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
             }
-        }
-        __threadfence();
-        __syncthreads();
-        // ticket: +1 per finished range; a range whose waits expired adds
-        // 0x10001, so the tile still completes (and rearms) but is not stored
-        if (threadIdx.x == 0) {
-            const unsigned add = clean ? 1u : 0x10001u;
-            const unsigned now = atomicAdd(p.counters + work.cnt, add) + add;
-            s_ticket = now;
-            if ((now & 0xffffu) == unsigned(work.ns)) p.counters[work.cnt] = 0u;
-        }
-        __syncthreads();
-        const unsigned now = s_ticket;
-        if ((now & 0xffffu) == unsigned(work.ns) && (now >> 16) == 0u && row_ok) {
-            __threadfence();
-            const float *base = part + size_t(warp * 32 + lane) * BN;
-#pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                float v[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-                for (int sidx = 0; sidx < work.ns; ++sidx) {
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 x = __ldcg(reinterpret_cast<const float4 *>(
-                            base + size_t(sidx) * slot + c0 + 4 * q));
-                        v[4 * q] += x.x;
-                        v[4 * q + 1] += x.y;
-                        v[4 * q + 2] += x.z;
-                        v[4 * q + 3] += x.w;
-                    }
-                }
-                store32(c0, v);
-            }
+        } else if (threadIdx.x == 0) {
+            p.counters[work.cnt] = 1u;   // a wait expired: the tile is not stored
         }
     }
+    // the reduction launch may be scheduled once every CTA is here
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
     // ---- teardown ----
     tc_fence_before();
@@ -662,7 +632,6 @@ tf32x3_fused_kernel(const __grid_constant__ CUtensorMap map_a,
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     __shared__ int s_mma_ok;
-    __shared__ unsigned s_ticket;
 
     // (tile, K range) of this CTA; grouped raster over 8 tile rows
     const TcWork work = tc_work(p);
@@ -843,9 +812,11 @@ tf32x3_fused_kernel(const __grid_constant__ CUtensorMap map_a,
             }
         }
     } else {
+        // partial tile of this K range, row-major 128 x BN; tc_reduce_kernel
+        // sums the tile's ranges after this launch
         const size_t slot = size_t(kTcBM) * BN;
-        float *part = p.partials + size_t(work.slot_first) * slot;
-        float *mine = part + size_t(split_idx) * slot + size_t(lrow) * BN;
+        float *mine = p.partials + (size_t(work.slot_first) + size_t(split_idx)) * slot +
+                      size_t(lrow) * BN;
         if (__all_sync(0xffffffffu, clean)) {
 #pragma unroll 1
             for (int c0 = cbeg; c0 < cbeg + BN / 2; c0 += 32) {
@@ -861,40 +832,12 @@ tf32x3_fused_kernel(const __grid_constant__ CUtensorMap map_a,
                     __stcg(reinterpret_cast<float4 *>(mine + c0 + 4 * q),
                            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
             }
-        }
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const unsigned add = clean ? 1u : 0x10001u;
-            const unsigned now = atomicAdd(p.counters + work.cnt, add) + add;
-            s_ticket = now;
-            if ((now & 0xffffu) == unsigned(work.ns)) p.counters[work.cnt] = 0u;
-        }
-        __syncthreads();
-        const unsigned now = s_ticket;
-        if ((now & 0xffffu) == unsigned(work.ns) && (now >> 16) == 0u && row_ok) {
-            __threadfence();
-            const float *rowp = part + size_t(lrow) * BN;
-#pragma unroll 1
-            for (int c0 = cbeg; c0 < cbeg + BN / 2; c0 += 32) {
-                float v[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-                for (int sidx = 0; sidx < work.ns; ++sidx) {
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 x = __ldcg(reinterpret_cast<const float4 *>(
-                            rowp + size_t(sidx) * slot + c0 + 4 * q));
-                        v[4 * q] += x.x;
-                        v[4 * q + 1] += x.y;
-                        v[4 * q + 2] += x.z;
-                        v[4 * q + 3] += x.w;
-                    }
-                }
-                store32(c0, v);
-            }
+        } else if (threadIdx.x == 0) {
+            p.counters[work.cnt] = 1u;   // a wait expired: the tile is not stored
         }
     }
+    // the reduction launch may be scheduled once every CTA is here
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
     // ---- teardown ----
     tc_fence_before();
@@ -916,6 +859,113 @@ tf32x3_fused_kernel(const __grid_constant__ CUtensorMap map_a,
                      "r"(uint32_t(BN))
                      : "memory");
     }
+}
+
+// The second launch of a split plan: for every split tile, the sum of its K
+// ranges' partial tiles in ascending range order, then alpha and beta.
+// Launched as a programmatic dependent of the product grid (it waits for that
+// grid's completion before reading).  A tile one of whose ranges gave up a
+// bounded wait carries a flag: it is not stored (C stays untouched), and the
+// flag is cleared for the next call.  One CTA per tile, so the CTA that
+// clears the flag is the only one that reads it; each thread takes float4s
+// of the tile four at a time, all their partials' loads in flight together.
+__global__ void __launch_bounds__(256) tc_reduce_kernel(const TcArgs p, int bn) {
+    const int i_tile = int(blockIdx.x);                 // among the split tiles
+    int pid, ns;
+    if (p.split > 1) {
+        pid = i_tile;
+        ns = p.split;
+    } else {
+        pid = p.tail_start + i_tile;
+        ns = p.tail_split;
+    }
+    // the product kernels' grouped raster over 8 tile rows
+    const int per_group = 8 * p.tiles_n;
+    const int group = pid / per_group;
+    const int first_m = group * 8;
+    const int gm = min(p.tiles_m - first_m, 8);
+    const int in_group = pid - group * per_group;
+    const int64_t m0 = int64_t(first_m + in_group % gm) * kTcBM;
+    const int64_t n0 = int64_t(in_group / gm) * bn;
+
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    __shared__ unsigned s_flag;
+    unsigned *flag = p.counters + i_tile;
+    if (threadIdx.x == 0) s_flag = *flag;
+    __syncthreads();
+    if (s_flag != 0u) {
+        if (threadIdx.x == 0) *flag = 0u;
+        return;
+    }
+    const size_t slot = size_t(kTcBM) * bn;
+    const float *part = p.partials + size_t(i_tile) * size_t(ns) * slot;
+    const bool vec = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0) && (p.ldc % 4 == 0);
+    const int per_row = bn / 4;                          // float4 per tile row
+    const int total = kTcBM * per_row;                   // float4 per tile (a multiple of 1024)
+    for (int base = threadIdx.x; base < total; base += 4 * blockDim.x) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int sidx = 0; sidx < ns; ++sidx) {
+            float4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                x[u] = __ldcg(reinterpret_cast<const float4 *>(part + size_t(sidx) * slot) +
+                              base + u * blockDim.x);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                v[u].x += x[u].x;
+                v[u].y += x[u].y;
+                v[u].z += x[u].z;
+                v[u].w += x[u].w;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = base + u * blockDim.x;
+            const int64_t row = m0 + idx / per_row, col = n0 + (idx % per_row) * 4;
+            if (row >= p.M || col >= p.N) continue;
+            float o[4] = {p.alpha * v[u].x, p.alpha * v[u].y, p.alpha * v[u].z, p.alpha * v[u].w};
+            float *cp = p.C + row * p.ldc + col;
+            if (vec && col + 4 <= p.N) {
+                if (p.beta != 0.0f) {
+                    const float4 old = *reinterpret_cast<const float4 *>(cp);
+                    o[0] = fmaf(p.beta, old.x, o[0]);
+                    o[1] = fmaf(p.beta, old.y, o[1]);
+                    o[2] = fmaf(p.beta, old.z, o[2]);
+                    o[3] = fmaf(p.beta, old.w, o[3]);
+                }
+                *reinterpret_cast<float4 *>(cp) = make_float4(o[0], o[1], o[2], o[3]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (col + e < p.N) {
+                        float x = o[e];
+                        if (p.beta != 0.0f) x = fmaf(p.beta, cp[e], x);
+                        cp[e] = x;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Launches tc_reduce_kernel for a plan's split tiles (nothing without any).
+cudaError_t launch_tc_reduce(const TcArgs &a, int bn, cudaStream_t stream) {
+    const int64_t tiles = int64_t(a.tiles_m) * a.tiles_n;
+    const int64_t split_tiles = a.split > 1 ? tiles : (a.tail_split > 1 ? tiles - a.tail_start : 0);
+    if (split_tiles <= 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(split_tiles), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_reduce_kernel, a, bn);
 }
 
 // cuTensorMapEncodeTiled, looked up once through the runtime (no link-time
@@ -969,7 +1019,8 @@ cudaError_t launch_mma(const CUtensorMap &ah, const CUtensorMap &al, const CUten
     const unsigned grid = unsigned(int64_t(a.tail_start) * a.split +
                                    (tiles - a.tail_start) * a.tail_split);
     tf32x3_mma_kernel<BN, STAGES><<<grid, kTcThreads, L::kDynBytes, stream>>>(ah, al, bh, bl, a);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    return e == cudaSuccess ? launch_tc_reduce(a, BN, stream) : e;
 }
 
 template <int BN, int STAGES>
@@ -984,7 +1035,8 @@ cudaError_t launch_fused(const CUtensorMap &a, const CUtensorMap &bh, const CUte
     const unsigned grid = unsigned(int64_t(args.tail_start) * args.split +
                                    (tiles - args.tail_start) * args.tail_split);
     tf32x3_fused_kernel<BN, STAGES><<<grid, kFusedThreads, L::kDynBytes, stream>>>(a, bh, bl, args);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    return e == cudaSuccess ? launch_tc_reduce(args, BN, stream) : e;
 }
 
 }  // namespace
