@@ -26,11 +26,12 @@ constexpr int kSmallCtasPerSm = 8;
 // GB with 16, the same 65.9 TFLOP/s.
 constexpr int kGroupM = 16;
 
-// Workspace layout: [counter block: kCounterBytes][partial tiles][...].  The
-// 3xTF32 mode keeps its split-K tile counters in the block (fixed size, so a
-// buffer reused across plans never sees stale partial data where a counter
-// is expected); the FFMA kernels take no tickets and leave it untouched.
-// Split plans stay within kMaxSplitTiles split tiles either way.
+// Workspace layout: [flag block: kCounterBytes][partial tiles][...].  The
+// 3xTF32 mode keeps one flag per split tile in the block, set only by a K
+// range whose bounded wait expired and cleared by the reduction (fixed size,
+// so a buffer reused across plans never sees stale partial data where a
+// flag is expected); the FFMA kernels leave it untouched.  Split plans stay
+// within kMaxSplitTiles split tiles either way.
 constexpr size_t kCounterBytes = 16384;
 constexpr int64_t kMaxSplitTiles = kCounterBytes / sizeof(unsigned);
 constexpr int kMaxSplit = 32;

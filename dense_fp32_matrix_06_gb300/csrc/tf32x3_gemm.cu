@@ -333,7 +333,7 @@ struct TcWork {
     int sidx, ns;     // range index, ranges of the tile
     int kbps;         // K blocks per range
     int slot_first;   // partial slot of the tile's first range
-    int cnt;          // counter index
+    int cnt;          // flag index
 };
 
 __device__ __forceinline__ TcWork tc_work(const TcArgs &p) {
@@ -1190,7 +1190,7 @@ TcArgs make_args(float *C, int64_t ldc, int64_t M, int64_t N, int64_t K, float a
     a.tail_start = int32_t(plan.tail_start);
     a.tail_split = plan.tail_split > 1 ? plan.tail_split : 1;
     a.tail_kb_per_split = int32_t((nkb + a.tail_split - 1) / a.tail_split);
-    // partial slots / counters only for split tiles
+    // partial slots / flags only for split tiles
     a.part_base = a.split > 1 ? 0 : a.tail_start;
     a.cnt_base = a.split > 1 ? 0 : a.tail_start;
     a.counters = counters;

@@ -79,7 +79,8 @@ typedef enum {
 } sgemm_act;
 
 /* Size of the block at the start of every workspace that the 3xTF32 mode
- * keeps its tile counters in; the FFMA kernels leave it untouched. */
+ * keeps its per-tile failure flags in (zero on entry and left zero by every
+ * call); the FFMA kernels leave it untouched. */
 #define SGEMM_WORKSPACE_COUNTER_BYTES 16384
 
 /* A per-shape launch configuration chosen by gemm_plan.  Plain data: the
