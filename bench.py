@@ -646,9 +646,10 @@ def roofline_entry(flops: float, nbytes: float, seconds: float, peak_tflops: flo
 
 def run_configs(sg, device, stream, peak_tflops: float, probe_tflops: float | None):
     """Every configured workload: TFLOP/s of sgemm and sgemm_tf32x3 (inputs
-    resident, CUDA events, median; workloads under 200 MB get the L2 flushed
-    between repetitions) with each one's roofline fraction, and the CPU oracle
-    on a sample of the workload's rows.
+    resident, CUDA events, 5 warm-ups, then the median and minimum of 20-40
+    repetitions; workloads under 200 MB get the L2 flushed between
+    repetitions) with each one's roofline fraction, and the CPU oracle on a
+    sample of the workload's rows.
 
     FFMA roofline: the slower of the fp32 FMA peak (`peak_tflops`) and HBM
     bandwidth for the algorithmic bytes.  Tensor mode: the tf32 tensor peak
@@ -674,10 +675,10 @@ def run_configs(sg, device, stream, peak_tflops: float, probe_tflops: float | No
             def call():
                 fn(p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
                    C.data_ptr(), p.ldc, sh)
-            for _ in range(3):
+            for _ in range(5):
                 call()
             torch.cuda.synchronize(device)
-            reps = max(5, min(40, int(1e12 / p.flops)))
+            reps = max(20, min(40, int(1e12 / p.flops)))
             ts = []
             for _ in range(reps):
                 if small:
@@ -693,6 +694,7 @@ def run_configs(sg, device, stream, peak_tflops: float, probe_tflops: float | No
             med = ts[len(ts) // 2]
             res[mode] = round(p.flops / med / 1e12, 3)
             res[f"{mode}_ms"] = round(med * 1e3, 4)
+            res[f"{mode}_ms_min"] = round(ts[0] * 1e3, 4)
             if mode == "ffma":
                 r = roofline_entry(p.flops, nbytes, med, peak_tflops, bw)
                 res.update(r)
