@@ -52,6 +52,10 @@ __global__ void transpose_kernel(const float *__restrict__ A, int64_t M, int64_t
 // of 256 threads loads four float4 along k and stores four float4 along m.
 // The shared tile is padded by one float per row; the column reads of the
 // store phase then see at most two-way bank conflicts.
+// kVecLoad: A's rows start on 16 bytes (lda and stride_a multiples of 4, A
+// aligned), so each thread reads its 4 columns with one 128-bit load;
+// otherwise with 4 scalar loads (coalesced across the warp all the same).
+template <bool kVecLoad>
 __global__ void __launch_bounds__(256) transpose64_kernel(const float *__restrict__ A, int64_t M,
                                                           int64_t K, int64_t lda,
                                                           float *__restrict__ At, int64_t ldt,
@@ -72,7 +76,7 @@ __global__ void __launch_bounds__(256) transpose64_kernel(const float *__restric
         const int64_t m = m0 + r, k = k0 + c4;
         float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         if (m < M) {
-            if (k + 3 < K) {
+            if (kVecLoad && k + 3 < K) {
                 v = __ldg(reinterpret_cast<const float4 *>(A + m * lda + k));
             } else {
                 const float *src = A + m * lda;
@@ -185,13 +189,20 @@ cudaError_t launch_ffma(const GemmArgs &a, int kernel, int tile, bool vec, bool 
 cudaError_t launch_transpose(const float *A, int64_t M, int64_t K, int64_t lda, float *At,
                              int64_t ldt, cudaStream_t stream, int64_t batch, int64_t stride_a,
                              int64_t stride_t) {
-    const bool vec = (reinterpret_cast<uintptr_t>(A) & 15u) == 0 &&
-                     (reinterpret_cast<uintptr_t>(At) & 15u) == 0 && lda % 4 == 0 &&
-                     ldt % 4 == 0 && ldt >= (M + 3) / 4 * 4 && stride_a % 4 == 0 &&
-                     stride_t % 4 == 0;
-    if (vec) {
+    // the 64 x 64 kernel stores 128-bit rows of A^T; it reads A with 128-bit
+    // loads when A's rows allow, with scalar loads otherwise
+    const bool vec_store = (reinterpret_cast<uintptr_t>(At) & 15u) == 0 && ldt % 4 == 0 &&
+                           ldt >= (M + 3) / 4 * 4 && stride_t % 4 == 0;
+    const bool vec_load = (reinterpret_cast<uintptr_t>(A) & 15u) == 0 && lda % 4 == 0 &&
+                          stride_a % 4 == 0;
+    if (vec_store) {
         const dim3 grid(unsigned((K + 63) / 64), unsigned((M + 63) / 64), unsigned(batch));
-        transpose64_kernel<<<grid, 256, 0, stream>>>(A, M, K, lda, At, ldt, stride_a, stride_t);
+        if (vec_load)
+            transpose64_kernel<true><<<grid, 256, 0, stream>>>(A, M, K, lda, At, ldt, stride_a,
+                                                               stride_t);
+        else
+            transpose64_kernel<false><<<grid, 256, 0, stream>>>(A, M, K, lda, At, ldt, stride_a,
+                                                                stride_t);
     } else {
         const dim3 grid(unsigned((K + 31) / 32), unsigned((M + 31) / 32), unsigned(batch));
         transpose_kernel<<<grid, dim3(32, 8), 0, stream>>>(A, M, K, lda, At, ldt, stride_a,

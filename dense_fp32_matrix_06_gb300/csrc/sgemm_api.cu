@@ -480,20 +480,26 @@ void plan_tiny(gemm_plan_t &p, int64_t M, int64_t N, int64_t K) {
 sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                        int64_t ldc, const void *A, const void *B, const void *C,
                        int sms, gemm_plan_t *out, bool allow_transpose = true) {
-    const bool vec = lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0 && aligned16(A) &&
-                     aligned16(B) && aligned16(C);
+    // B and C decide whether a product after the A^T pass can take the vector
+    // path: the copy of A is written aligned whatever A's own alignment
+    const bool vec_bc = ldb % 4 == 0 && ldc % 4 == 0 && aligned16(B) && aligned16(C);
+    const bool vec = vec_bc && lda % 4 == 0 && aligned16(A);
     plan_core(M, N, K, 1, vec, sms, out);
     if (M > 0 && N > 0 && choose_tiny(M, N, K, sms)) {
         plan_tiny(*out, M, N, K);
         return SGEMM_OK;
     }
-    const int fam = (allow_transpose && M > 0 && N > 0 && K > 0)
-                        ? choose_transpose_a(*out, M, N, K, sms)
-                        : int(kTransposeNone);
+    int fam = kTransposeNone;
+    if (allow_transpose && M > 0 && N > 0 && K > 0 && vec_bc) {
+        gemm_plan_t probe = *out;   // the bands as if A were aligned too
+        probe.vec = 1;
+        fam = choose_transpose_a(probe, M, N, K, sms);
+    }
     if (fam != kTransposeNone) {
         // the product then runs with both operands copied by rows, in K slices of 32
         gemm_plan_t &q = *out;
         q.transpose_a = 1;
+        q.vec = 1;
         if (fam == kTransposeStreamK) {
             plan_stream_k(q, M, N, q.tiles_m * q.tiles_n, K, sms, true);
             q.kernel = tuning(kKnobKernel) == kKernelFfma128 ? kKernelFfma128 : kKernelFfma2x128;
@@ -753,8 +759,8 @@ bool plan_matches(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int64_t
         if (sk_tiles > 0 && (G > p.sk_iters || sk_tiles > kMaxSplitTiles ||
                              G > sk_tiles * kSkMaxContrib))
             return false;
-        if (p.vec && !(lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0 && aligned16(A) &&
-                       aligned16(B) && aligned16(C)))
+        if (p.vec && !(ldb % 4 == 0 && ldc % 4 == 0 && aligned16(B) && aligned16(C) &&
+                       (p.transpose_a || (lda % 4 == 0 && aligned16(A)))))
             return false;
         if (p.transpose_a) {
             if (t != 128 || !p.vec || M > int64_t(65535) * 32) return false;
@@ -782,8 +788,9 @@ bool plan_matches(const gemm_plan_t &p, int64_t M, int64_t N, int64_t K, int64_t
         return false;
     if (p.grid_ctas != p.tail_start * p.split_k + (tiles - p.tail_start) * p.tail_split)
         return false;
-    const bool vec_ok = lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0 && aligned16(A) &&
-                        aligned16(B) && aligned16(C);
+    // (a plan with the A^T pass reads the aligned copy of A, not A)
+    const bool vec_ok = ldb % 4 == 0 && ldc % 4 == 0 && aligned16(B) && aligned16(C) &&
+                        (p.transpose_a || (lda % 4 == 0 && aligned16(A)));
     if (p.vec && !vec_ok) return false;
     if (!p.edge) {
         if (!p.vec) return false;

@@ -132,7 +132,13 @@ def test_plan_transpose_choice(lib, tune):
     assert plan(2048, 2048, 64).transpose_a == 0          # K = 64 on under 8 waves
     assert plan(1024, 1024, 1024).transpose_a == 0        # 64 tiles, K = 1024
     assert plan(4096, 512, 4096).transpose_a == 0         # N < 768
-    assert plan(4096, 4096, 4096, A=4100).transpose_a == 0   # not vector-aligned
+    # A's own alignment does not matter (its copy is aligned); B's and C's do
+    q = plan(4096, 4096, 4096, A=4100)
+    assert q.transpose_a == 1 and q.vec == 1
+    q = plan(4096, 4096, 4095, lda=4095)
+    assert q.transpose_a == 1 and q.vec == 1 and q.a_t_ld == 4096
+    assert plan(4096, 4096, 4096, B=4100).transpose_a == 0
+    assert plan(4096, 4095, 4096, ldb=4095, ldc=4095).transpose_a == 0
     tune(transpose_a="0")
     q = plan(8192, 8192, 8192)
     assert q.transpose_a == 0 and q.workspace_bytes == 0 and q.bk == 16

@@ -340,6 +340,21 @@ def test_packed_issue_on_transposed_a_plans(sg, tune, M, N, K, lds, dist, knobs)
     assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
 
 
+@pytest.mark.parametrize("M,N,K,lda,a_offset,dist", [
+    (2304, 1024, 515, 515, 0, "uniform"),     # odd lda: A's rows not 16-byte aligned
+    (2304, 1024, 516, 516, 1, "int4"),        # A's pointer 4 bytes off
+    (1280, 2048, 2047, 2047, 1, "uniform"),   # both, and A^T + stream-K
+])
+def test_transposed_a_path_with_unaligned_a(sg, M, N, K, lda, a_offset, dist):
+    """Only B and C need 16-byte alignment for the A^T plans: A is copied into
+    an aligned A^T first (the scalar transpose kernel reads it)."""
+    p = workloads.make(M, N, K, dist=dist, seed=73, lda=lda, alpha=1.5 if dist == "int4" else 0.75,
+                       beta=0.5, c0_dist="int4" if dist == "int4" else "uniform")
+    plan = sg.gemm_plan_for_sms(p.M, p.N, p.K, p.lda, p.ldb, p.ldc, 4 * a_offset, 0, 0)
+    assert plan.transpose_a == 1 and plan.vec == 1
+    run_and_check(sg, p, exact=dist == "int4", a_offset=a_offset)
+
+
 def test_deterministic_run_to_run(sg):
     for name in ("long_k", "ragged", "gpt2_mlp_down"):
         p = workloads.workload(name)
