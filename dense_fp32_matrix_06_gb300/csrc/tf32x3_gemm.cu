@@ -1099,9 +1099,10 @@ Tf32x3Plan tf32x3_plan(int64_t M, int64_t N, int64_t K, int sms) {
         }
     }
     if (tiles <= kMaxSplitTiles && 2 * tiles <= sms) {
-        // at least 24 K blocks a range on 256-wide tiles, 16 on 128-wide
-        // ones (1024^3, 128-wide: 56.0 us unsplit, 47.8 in two ranges of 16)
-        int64_t sp = std::min<int64_t>(sms / tiles, nkb / (plan.bn == 128 ? 16 : 24));
+        // at least 24 K blocks a range on 256-wide tiles, 8 on 128-wide ones
+        // (1024^3, 128-wide: 56.0 us unsplit, 47.8 in two ranges of 16;
+        // 1023x777x513: 43.7 unsplit, 37.5 in two ranges of 9, 44.7 in three)
+        int64_t sp = std::min<int64_t>(sms / tiles, nkb / (plan.bn == 128 ? 8 : 24));
         sp = std::min<int64_t>(sp, 16);
         plan.split = sp > 1 ? int(sp) : 1;
         return plan;
