@@ -216,12 +216,40 @@ def cpu_baseline(p: workloads.Problem, target_s: float = 15.0) -> dict:
 # arms
 # --------------------------------------------------------------------------
 
+def code_tokens(text: str) -> str:
+    """C/C++ source with comments removed and whitespace runs collapsed (string
+    and character literals kept as written), so that a comment edit leaves it
+    unchanged and any edit of the code does not."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+            out.append(" ")
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_hash() -> str:
-    """Hash of the FFMA kernel's sources (traffic figures are tied to it)."""
+    """Hash of the FFMA kernel's code (traffic figures are tied to it);
+    comments and layout do not enter it."""
     h = hashlib.sha256()
     for path in KERNEL_SOURCES:
-        with open(path, "rb") as f:
-            h.update(f.read())
+        with open(path, encoding="utf-8") as f:
+            h.update(code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 

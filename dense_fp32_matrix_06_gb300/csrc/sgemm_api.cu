@@ -133,7 +133,10 @@ int choose_split(int64_t tiles, int64_t K, int sms, int64_t *k_per_split, int bk
 // default: measured on GB300 it gains nothing (8192^3: 59.26 TFLOP/s either
 // way; 4096^3: 56.35 with, 56.93 without), because with two CTAs per SM a
 // CTA left alone on its SM in the last wave already runs at close to the
-// whole SM's rate.
+// whole SM's rate.  Plans with the A^T pass never take it: tried there (the
+// last 144 of 8192^3's 4096 tiles in two K ranges), the split build of the
+// kernel ran every wave slower (8192^3 15.89 -> 16.31 ms, 4096^3 2091 ->
+// 2144 us).
 void choose_tail(int64_t tiles, int64_t K, int sms, int64_t *tail_start, int *tail_split,
                  int64_t *tail_kps) {
     const int64_t slots = int64_t(sms) * kCtasPerSm;

@@ -107,3 +107,18 @@ def test_per_workload_roofline_arithmetic():
     t = bench.roofline_entry(q.flops, bench.algorithmic_bytes(q), 50e-6, 316.0, 6800.0)
     assert t["bound"] == "hbm"
     assert t["frac"] == pytest.approx(bench.algorithmic_bytes(q) / 6800e9 / 50e-6, rel=1e-3)
+
+
+def test_traffic_hash_ignores_comments_not_code():
+    """The DRAM traffic figures are tied to the kernel's code: a comment or
+    layout edit keeps the hash, any change of a token outside comments, or
+    inside a string literal, changes it."""
+    src = 'int f(int x) { // twice\n  return 2 * x; /* done */ }\nconst char *s = "a // b";\n'
+    same = 'int f(int x) {\n    return 2 * x;   // doubled\n}\nconst char *s = "a // b";\n'
+    other = 'int f(int x) { return 3 * x; }\nconst char *s = "a // b";\n'
+    lit = 'int f(int x) { return 2 * x; }\nconst char *s = "a // c";\n'
+    assert bench.code_tokens(src) == bench.code_tokens(same)
+    assert bench.code_tokens(src) != bench.code_tokens(other)
+    assert bench.code_tokens(src) != bench.code_tokens(lit)
+    assert "twice" not in bench.code_tokens(src) and '"a // b"' in bench.code_tokens(src)
+    assert len(bench.source_hash()) == 16
