@@ -430,7 +430,7 @@ def run_e2e(sg, p, A, B, C, A_h, B_h, stream, device, dist, world, args):
     streams, so the upload of step i+1 and the download of step i-1 overlap
     the GEMM of step i."""
     import torch
-    e_steps = max(3, min(args.steps, args.e2e_steps))
+    e_steps = max(3, args.e2e_steps if args.e2e_steps > 0 else args.steps)
     up = torch.cuda.Stream(device)
     down = torch.cuda.Stream(device)
     bufs = [(A, B, C), (torch.empty_like(A), torch.empty_like(B), torch.empty_like(C))]
@@ -814,7 +814,8 @@ def parse(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="square8192", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=0,
+                    help="steps of the end-to-end leg (default: as many as --steps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
