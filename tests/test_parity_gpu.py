@@ -466,6 +466,53 @@ def test_large_workload_sampled(sg, name, dist):
         assert np.all(np.isfinite(C))
 
 
+@pytest.mark.parametrize("path", ["planned", "staged", "tf32x3"])
+def test_output_beyond_two_to_the_31_elements(sg, tune, path):
+    """A C of 131072 x 16400 = 2.15e9 elements (8.6 GB): row offsets past 2^31
+    in every epilogue, 132k output tiles, a ragged last tile column, K shorter
+    than one slice.  Integer inputs, so the sampled entries -- both sides of
+    the row where the offset crosses 2^31, the last row and column, and
+    random ones -- are bit-exact against the oracle.  'planned' takes the
+    A^T pass the planner picks here, 'staged' reads A as stored, 'tf32x3' is
+    the tensor-core mode."""
+    import torch
+    M, N, K = 131072, 16400, 24
+    assert M * N > 2**31
+    A, B = workloads.operands(M, N, K, dist="int4", seed=61)
+    if path == "staged":
+        tune(transpose_a=0)
+    plan = sg.gemm_plan(M, N, K, K, N, N, 0, 0, 0)
+    if path == "planned":
+        assert plan.transpose_a == 1
+    if path == "staged":
+        assert plan.transpose_a == 0
+    dev = torch.device("cuda", 0)
+    Ad = torch.from_numpy(A).to(dev)
+    Bd = torch.from_numpy(B).to(dev)
+    Cd = torch.full((M * N,), float("nan"), dtype=torch.float32, device=dev)
+    try:
+        st = torch.cuda.current_stream().cuda_stream
+        fn = sg.sgemm_tf32x3_ptr if path == "tf32x3" else sg.sgemm_ptr
+        fn(M, N, K, 1.0, Ad.data_ptr(), K, Bd.data_ptr(), N, 0.0, Cd.data_ptr(), N, st)
+        torch.cuda.synchronize()
+        cross = (2**31) // N                      # the row where i * N passes 2^31
+        rows = np.array([0, cross - 1, cross, cross + 1, M - 1], dtype=np.int64)
+        ii = np.repeat(rows, 6)
+        jj = np.tile(np.array([0, 1, 127, N // 2, N - 2, N - 1], dtype=np.int64), len(rows))
+        ri, rj = workloads.sample_indices(M, N, 4000, seed=62)
+        ii = np.concatenate([ii, ri])
+        jj = np.concatenate([jj, rj])
+        got = Cd[torch.from_numpy(ii * N + jj).to(dev)].cpu().numpy()
+        last = Cd[(M - 1) * N:].cpu().numpy()
+    finally:
+        del Cd
+        torch.cuda.empty_cache()
+    ref = oracle.sgemm_entries(M, N, K, 1.0, A, B, 0.0, None, ii, jj, lda=K, ldb=N)
+    assert np.array_equal(got, ref)
+    ref_last = oracle.sgemm_rows(M, N, K, 1.0, A, B, 0.0, None, np.array([M - 1]), lda=K, ldb=N)
+    assert np.array_equal(last, ref_last.ravel())
+
+
 def test_transposed_plan_falls_back_when_the_workspace_is_capped(sg, tune):
     """When the workspace for the transposed copy of A cannot be had (here a
     1 MiB cap stands in for a failed allocation), sgemm runs the plan that

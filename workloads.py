@@ -133,6 +133,17 @@ def make(M: int, N: int, K: int, *, dist: str = "uniform", seed: int = 0,
                    {"dist": dist, "seed": seed})
 
 
+def operands(M: int, N: int, K: int, *, dist: str = "int4", seed: int = 0,
+             lda: int | None = None, ldb: int | None = None):
+    """A (M x lda) and B (K x ldb) only, drawn as make() draws them, for shapes
+    whose C is too large to hold on the host (C0 is never read at beta = 0)."""
+    lda = max(K, 1) if lda is None else lda
+    ldb = max(N, 1) if ldb is None else ldb
+    rng = np.random.default_rng(seed)
+    fill = {"uniform": uniform_fill, "normal": normal_fill, "int4": int_fill}[dist](rng)
+    return _padded(fill, M, K, lda), _padded(fill, K, N, ldb)
+
+
 def workload(name: str, *, dist: str | None = None) -> Problem:
     """One of the named benchmark workloads (table in the module docstring)."""
     M, N, K, d, seed, alpha, beta, extra = WORKLOADS[name]
