@@ -250,11 +250,15 @@ sgemm_status sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
  * split and transposed into a library-owned workspace per call, and A is
  * split inside the kernel (or, when its layout does not allow TMA, in a
  * pre-pass into the same workspace) -- at most 8*(M+N)*ceil(K/4)*4 bytes per
- * (device, stream), grown with stream-ordered allocation.  Grids smaller than half the GPU are split along K (partials in
- * the same workspace).  M and N must be below 2^31 and K at most 2,097,120
- * (SGEMM_ERR_INVALID_ARG otherwise).  Every device-side
- * wait gives up after 1 s: the kernel then stores nothing to C and records
- * the event, which sgemm_device_status reports.
+ * (device, stream), grown with stream-ordered allocation.  Grids smaller
+ * than half the GPU are split along K (partials in the same workspace).  M
+ * and N must be below 2^31 and K at most 2,097,120 (SGEMM_ERR_INVALID_ARG
+ * otherwise).  Every device-side wait gives up after 1 s: the kernel then
+ * stores nothing to C and records the event, which sgemm_device_status
+ * reports.  Non-finite inputs: a NaN gives NaN where fp32 arithmetic would;
+ * an infinite input gives NaN where fp32 would give +-inf (the split cannot
+ * carry it: inf - inf in the low part, or inf * 0 against an operand exact in
+ * TF32).  sgemm follows IEEE fp32 throughout.
  */
 sgemm_status sgemm_tf32x3(int64_t M, int64_t N, int64_t K, float alpha,
                           const float *A, int64_t lda, const float *B, int64_t ldb,

@@ -8,6 +8,7 @@ Every test also checks that C's padding and the memory around C are untouched.
 """
 from __future__ import annotations
 
+import dataclasses
 import os
 
 import numpy as np
@@ -195,6 +196,57 @@ def test_alpha_zero_and_k_zero_scale_c(sg):
     d.run(sg)
     C, buf = d.result()
     assert np.array_equal(C, np.zeros((64, 64), np.float32))
+
+
+def with_non_finite(p):
+    """A copy of `p` with +inf, -inf and NaN planted in A and B (inside the
+    logical block): row 5 meets +inf, row 9 -inf, row 40 NaN, row 70 both
+    infinities (NaN in every column), column 7 a NaN of B."""
+    A = p.A.copy()
+    B = p.B.copy()
+    A[5, 17] = np.inf
+    A[9, 3] = -np.inf
+    A[40, 60] = np.nan
+    A[70, 10] = np.inf
+    A[70, p.K - 1] = -np.inf
+    B[10, :p.N] = np.abs(B[10, :p.N]) + 0.5       # so row 70's two infinite terms
+    B[p.K - 1, :p.N] = np.abs(B[p.K - 1, :p.N]) + 0.5   # have opposite signs everywhere
+    B[100, 7] = np.nan
+    return dataclasses.replace(p, A=A, B=B, name=p.name + "+nonfinite")
+
+
+def assert_same_specials(C, ref):
+    """NaN, +inf and -inf exactly where the oracle has them."""
+    assert np.array_equal(np.isnan(C), np.isnan(ref))
+    assert np.array_equal(np.isposinf(C), np.isposinf(ref))
+    assert np.array_equal(np.isneginf(C), np.isneginf(ref))
+
+
+@pytest.mark.parametrize("knobs", [{}, {"tile": 64, "split_k": 3}, {"split_k": 4},
+                                   {"transpose_a": 1, "tile": 128, "split_k": 1},
+                                   {"transpose_a": 1, "tile": 128, "split_k": 3},
+                                   {"schedule": 1}, {"schedule": 2}])
+def test_non_finite_inputs_propagate_as_in_ieee_fp32(sg, tune, knobs):
+    """IEEE semantics survive every path: a product with an infinity stays
+    infinite with its sign, +inf and -inf in one sum give NaN, and a NaN
+    spreads to its row or column -- the oracle (fp64 sums of the same
+    products) fixes where.  The finite entries keep the usual tolerance."""
+    tune(**knobs)
+    M, N, K = (200, 256, 256) if knobs.get("schedule") == 2 else (300, 260, 1000)
+    p = with_non_finite(workloads.make(M, N, K, seed=71, beta=0.5, c0_dist="uniform"))
+    d = DeviceProblem(p)
+    d.run(sg)
+    C, buf = d.result()
+    d.check_untouched(buf)
+    ref = oracle.problem(p)
+    assert_same_specials(C, ref)
+    assert np.isposinf(ref[5]).any() and np.isneginf(ref[9]).any()
+    assert np.isnan(ref[40]).all() and np.isnan(ref[70]).all() and np.isnan(ref[:, 7]).all()
+    fin = np.isfinite(ref)
+    A, B, C0 = logical(p)
+    den = K * float(np.nanmax(np.abs(np.where(np.isfinite(A), A, 0)))) * \
+        float(np.nanmax(np.abs(np.where(np.isfinite(B), B, 0)))) + 0.5 * float(np.abs(C0).max())
+    assert float(np.abs(C[fin].astype(np.float64) - ref[fin]).max()) / den <= TOL_FFMA
 
 
 def test_empty_shapes_are_no_ops(sg):

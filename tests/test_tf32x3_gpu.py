@@ -341,3 +341,39 @@ def test_narrow_tiles(sg, tune, M, N, K, dist, split, fuse):
     p = workloads.make(M, N, K, dist=dist, seed=M + K, alpha=1.5 if dist == "int4" else 0.75,
                        beta=0.5, c0_dist="int4" if dist == "int4" else "uniform")
     check(p, run(sg, p, c_offset=1), exact=dist == "int4")
+
+
+@pytest.mark.parametrize("fuse", ["1", "0"])
+def test_non_finite_inputs(sg, tune, fuse):
+    """The split cannot carry an infinity: x_hi = inf leaves x_lo = tf32(inf - inf)
+    = NaN, and even with x_lo = 0 the term x_hi * y_lo is inf * 0 wherever y is
+    exact in TF32.  So the tensor mode returns NaN where fp32 gives +-inf -- a
+    non-finite value, never a finite one -- and NaN exactly where fp32 gives
+    NaN; entries no special value reaches keep the mode's tolerance."""
+    import dataclasses
+    tune(tf32x3_fuse_a=fuse)
+    p = workloads.make(300, 260, 1000, seed=72, beta=0.5, c0_dist="uniform")
+    A = p.A.copy()
+    B = p.B.copy()
+    A[5, 17] = np.inf
+    A[9, 3] = -np.inf
+    A[40, 60] = np.nan
+    B[100, 7] = np.nan
+    p = dataclasses.replace(p, A=A, B=B)
+    C = run(sg, p)
+    ref = oracle.problem(p)
+    assert np.isinf(ref[5]).any() and np.isinf(ref[9]).any() and np.isnan(ref[40]).all()
+    assert np.all(np.isnan(C[np.isnan(ref)]))
+    assert not np.isfinite(C[np.isinf(ref)]).any()
+    fin = np.isfinite(ref)
+    assert np.isfinite(C[fin]).all()
+    keep = np.ones(p.M, bool)
+    keep[[5, 9, 40]] = False
+    cols = np.ones(p.N, bool)
+    cols[7] = False
+    sub = np.ix_(keep, cols)
+    Af = np.where(np.isfinite(A[:, :p.K]), A[:, :p.K], 0)
+    Bf = np.where(np.isfinite(B[:, :p.N]), B[:, :p.N], 0)
+    den = p.K * float(np.abs(Af).max()) * float(np.abs(Bf).max()) + 0.5 * float(
+        np.abs(p.C0[:, :p.N]).max())
+    assert float(np.abs(C[sub].astype(np.float64) - ref[sub]).max()) / den <= TOL_TF32X3
