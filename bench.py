@@ -469,6 +469,25 @@ def run_e2e(sg, p, A, B, C, A_h, B_h, stream, device, dist, world, args):
     warm.record(stream)
     run(2, warm)
     torch.cuda.synchronize(device)
+
+    # the pinned copies alone, one step's worth each, on their own streams:
+    # one untimed copy (the first after idle runs slow), then three timed
+    def copy_seconds(fn, on):
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(on):
+            fn()
+            c0.record(on)
+            for _ in range(3):
+                fn()
+            c1.record(on)
+        torch.cuda.synchronize(device)
+        return c0.elapsed_time(c1) / 3e3
+
+    Ad, Bd, Cd = bufs[0]
+    h2d_s = copy_seconds(lambda: (Ad.copy_(A_h, non_blocking=True),
+                                  Bd.copy_(B_h, non_blocking=True)), up)
+    d2h_s = copy_seconds(lambda: C_h[0].copy_(Cd, non_blocking=True), down)
     s0 = torch.cuda.Event(enable_timing=True)
     s1 = torch.cuda.Event(enable_timing=True)
     barrier(dist, device)
@@ -479,10 +498,14 @@ def run_e2e(sg, p, A, B, C, A_h, B_h, stream, device, dist, world, args):
     e_el = max_over_ranks(s0.elapsed_time(s1) / 1e3, dist, device)
     # the last step's result is the one on the host now; check it is finite
     finite = bool(torch.isfinite(C_h[(e_steps - 1) % 2][:, :p.N]).all())
+    h2d_bytes = int(p.A.nbytes + p.B.nbytes)
+    d2h_bytes = int(C_h[0].numel() * 4)
     return {"value": throughput(float(p.flops), e_steps, world, e_el), "unit": UNIT,
-            "h2d_bytes_per_step": int(p.A.nbytes + p.B.nbytes),
-            "d2h_bytes_per_step": int(C_h[0].numel() * 4), "steps": e_steps,
-            "result_finite": finite,
+            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+            "steps": e_steps, "result_finite": finite,
+            "h2d_gbs": round(h2d_bytes / h2d_s / 1e9, 1),
+            "d2h_gbs": round(d2h_bytes / d2h_s / 1e9, 1),
+            "copy_ms_per_step": round(max(h2d_s, d2h_s) * 1e3, 3),
             "pipelining": "two device buffer sets, three streams: the upload of step i+1 and "
                           "the download of step i-1 overlap the GEMM of step i"}
 
