@@ -266,11 +266,13 @@ bool choose_stream_k(int tile, int64_t tiles, int64_t K, int sms) {
 
 // `direct`: both operands reach the kernel by direct copies (op(A) = A^T and
 // op(B) = B), which lets a stream-K plan take the longer K slice.
+// `force_tile` / `force_split` (0: the planner's choice) serve the balance
+// rule below (choose_balanced_small).
 void plan_core(int64_t M, int64_t N, int64_t K, int64_t batch, bool vec, int sms,
-               gemm_plan_t *out, bool direct = false) {
+               gemm_plan_t *out, bool direct = false, int force_tile = 0, int force_split = 0) {
     gemm_plan_t p;
     std::memset(&p, 0, sizeof(p));
-    const int tile = choose_tile(M, N, K, batch, sms);
+    const int tile = force_tile ? force_tile : choose_tile(M, N, K, batch, sms);
     const int bk = tile / 8;
     const int cps = tile == kSmallTile ? kSmallCtasPerSm : kCtasPerSm;
     p.mode = SGEMM_MODE_FFMA;
@@ -288,6 +290,10 @@ void plan_core(int64_t M, int64_t N, int64_t K, int64_t batch, bool vec, int sms
     p.split_k = (M > 0 && N > 0 && K > 0 && batch > 0)
                     ? choose_split(tiles, K, sms, &kps, bk, cps)
                     : 1;
+    if (force_split > 1) {
+        p.split_k = force_split;
+        kps = K / force_split;
+    }
     if (p.split_k == 1) kps = ceil_div(K, bk) * bk;
     p.k_per_split = kps > 0 ? kps : bk;
     int tail_split = 1;
@@ -480,9 +486,9 @@ void plan_tiny(gemm_plan_t &p, int64_t M, int64_t N, int64_t K) {
     p.workspace_bytes = 0;
 }
 
-sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
-                       int64_t ldc, const void *A, const void *B, const void *C,
-                       int sms, gemm_plan_t *out, bool allow_transpose = true) {
+sgemm_status plan_impl_base(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                            int64_t ldc, const void *A, const void *B, const void *C,
+                            int sms, gemm_plan_t *out, bool allow_transpose) {
     // B and C decide whether a product after the A^T pass can take the vector
     // path: the copy of A is written aligned whatever A's own alignment
     const bool vec_bc = ldb % 4 == 0 && ldc % 4 == 0 && aligned16(B) && aligned16(C);
@@ -529,6 +535,54 @@ sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb
     gemm_plan_t &q = *out;
     if (q.schedule == 0 && (q.bm == kSmallTile || q.split_k > 1) && tuning(kKnobKernel) < 0)
         q.kernel = kKernelFfma2x128;
+    return SGEMM_OK;
+}
+
+// Split-K grids of 128-wide tiles that give every SM one CTA and some a
+// second (between sms and 1.75 sms CTAs) leave the SMs unevenly loaded: at
+// 1024^3, 64 tiles in four K ranges put two CTAs on 104 SMs and one on 48.
+// 64-wide tiles in enough exact K ranges (at least 128 deep) for about 13.5
+// CTAs a SM spread the same work evenly.  Measured on GB300 (microseconds,
+// L2 flushed, 128-wide plan / 64-wide): 1024^3 55.9 / 51.8 (8 ranges),
+// 1024x1024x2048 93.8 / 90.8 (8), 512x1024x2048 56.9 / 53.9 (16),
+// 1024x1024x4096 173.7 / 169.6 (8); grids already near two CTAs a SM keep
+// 128 (768x1024x1024, 288 CTAs: 44.6 against 45.7; 896x896x1536, 294 CTAs:
+// 55.9 against 62.1).  Returns the number of K ranges, 0 for no change.
+int choose_balanced_small(const gemm_plan_t &q, int64_t M, int64_t N, int64_t K, int sms) {
+    if (tuning(kKnobTile) >= 0 || tuning(kKnobSplit) >= 0 || tuning(kKnobSchedule) >= 0)
+        return 0;
+    if (q.bm != 128 || q.schedule != 0 || q.split_k < 2 || q.tail_split != 1) return 0;
+    if (q.grid_ctas <= sms || 4 * q.grid_ctas > 7 * int64_t(sms)) return 0;
+    const int64_t tiles64 = ceil_div(M, kSmallTile) * ceil_div(N, kSmallTile);
+    const int64_t target = int64_t(27) * sms / 2;   // about 13.5 CTAs a SM
+    int best = 0;
+    int64_t best_gap = 0;
+    for (int s = 2; s <= 16; ++s) {
+        if (K % (int64_t(8) * s) != 0 || K / s < 128) continue;   // exact ranges of 8-slices
+        const int64_t ctas = tiles64 * s;
+        if (ctas < int64_t(kSmallCtasPerSm) * sms) continue;      // at least one full wave
+        const int64_t gap = ctas > target ? ctas - target : target - ctas;
+        if (!best || gap < best_gap) {
+            best = s;
+            best_gap = gap;
+        }
+    }
+    return best;
+}
+
+sgemm_status plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                       int64_t ldc, const void *A, const void *B, const void *C,
+                       int sms, gemm_plan_t *out, bool allow_transpose = true) {
+    sgemm_status st = plan_impl_base(M, N, K, lda, ldb, ldc, A, B, C, sms, out, allow_transpose);
+    if (st != SGEMM_OK) return st;
+    // (measured on operands that all take the 16-byte path; others keep the plan)
+    const bool vec = ldb % 4 == 0 && ldc % 4 == 0 && aligned16(B) && aligned16(C) &&
+                     lda % 4 == 0 && aligned16(A);
+    const int s64 = vec ? choose_balanced_small(*out, M, N, K, sms) : 0;
+    if (s64 > 0) {
+        plan_core(M, N, K, 1, vec, sms, out, false, kSmallTile, s64);
+        if (tuning(kKnobKernel) < 0) out->kernel = kKernelFfma2x128;
+    }
     return SGEMM_OK;
 }
 

@@ -170,9 +170,12 @@ def test_plan_transpose_choice(lib, tune):
     (8192, 8192, 64, "grid"),          # 13 waves of K = 64
     (2048, 512, 4096, "none"),         # N < 768: the pass costs too much
 ])
-def test_plan_transpose_family_bands(lib, M, N, K, family):
+def test_plan_transpose_family_bands(lib, tune, M, N, K, family):
     """Below one wave, the pass over A and the schedule after it follow the
-    bands measured on GB300 (tile count as a fraction of a wave, and K)."""
+    bands measured on GB300 (tile count as a fraction of a wave, and K).  The
+    bands are a property of 128-wide plans: the tile knob pins that (and
+    leaves out the balance rule, tested below)."""
+    tune(tile=128)
     p = plan(M, N, K)
     got = "none" if not p.transpose_a else ("stream_k" if p.schedule == 1 else "grid")
     assert got == family
@@ -409,3 +412,35 @@ def test_stream_k_plan_round_trips_through_sgemm_with_plan_checks(lib, tune):
         rc = lib.sgemm_with_plan(ctypes.byref(q), 1024, 1024, 1024, 1.0, 4096, 1024, 4096,
                                  1024, 0.0, 4096, 1024, 4096, 1 << 30, None)
         assert rc == 1, field
+
+
+@pytest.mark.parametrize("M,N,K,bm,split", [
+    # 128-wide split grids of 256 CTAs (one CTA on 48 SMs, two on 104) move to
+    # 64-wide tiles in exact K ranges, about 13.5 CTAs a SM
+    (1024, 1024, 1024, 64, 8),
+    (512, 2048, 2048, 64, 8),      # (was the A^T pass in 4 ranges)
+    (1024, 512, 2048, 64, 16),
+    (896, 1536, 1024, 64, 8),      # 252 CTAs
+    (640, 2048, 1536, 64, 6),      # 240 CTAs; 6 ranges of 256 divide K exactly
+    # grids already near two CTAs a SM keep 128-wide tiles
+    (768, 1024, 1024, 128, 6),     # 288 CTAs
+    (896, 896, 1536, 128, 6),      # 294 CTAs
+])
+def test_plan_balanced_small_tiles(lib, M, N, K, bm, split):
+    p = plan(M, N, K)
+    assert (p.bm, p.split_k) == (bm, split)
+    if bm == 64:
+        assert p.transpose_a == 0 and p.schedule == 0 and p.edge == 0
+        assert p.kernel == 1                         # packed issue
+        assert p.k_per_split * split == K and p.k_per_split >= 128
+        assert p.grid_ctas == (M // 64) * (N // 64) * split
+
+
+def test_plan_balanced_small_tiles_needs_aligned_operands_and_no_knobs(lib, tune):
+    assert plan(1024, 1024, 1024).bm == 64
+    # A's rows not 16-byte aligned: the plan is the one measured for that case
+    assert plan(1024, 1024, 1024, lda=1025).bm == 128
+    tune(split_k=4)
+    assert plan(1024, 1024, 1024).bm == 128
+    tune(split_k=None, schedule=0)
+    assert plan(1024, 1024, 1024).bm == 128

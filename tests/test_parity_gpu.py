@@ -421,9 +421,12 @@ def test_deterministic_run_to_run(sg):
                 assert np.array_equal(C.view(np.uint32), first.view(np.uint32)), name
 
 
-def test_sgemm_with_plan_caller_workspace(sg):
+@pytest.mark.parametrize("name", ["long_k", "square1024ab"])
+def test_sgemm_with_plan_caller_workspace(sg, name):
+    """Caller-held workspace on a split plan: long_k (the A^T pass, then K
+    ranges) and 1024^3 (64-wide tiles in eight K ranges, the balance rule)."""
     torch = _torch()
-    p = workloads.workload("long_k")
+    p = workloads.workload(name)
     A = torch.from_numpy(p.A).cuda()
     B = torch.from_numpy(p.B).cuda()
     C = torch.empty((p.M, p.N), device="cuda")
@@ -432,12 +435,15 @@ def test_sgemm_with_plan_caller_workspace(sg):
     assert (plan.split_k > 1 or plan.sk_iters > 0) and plan.workspace_bytes > 0
     # the workspace needs no initialisation: start from garbage (NaN bytes)
     ws = torch.full((plan.workspace_bytes,), 0xFF, dtype=torch.uint8, device="cuda")
-    ref = oracle.problem(p)
+    if name == "square1024ab":
+        assert (plan.bm, plan.split_k, plan.transpose_a) == (64, 8, 0)
+    p0 = dataclasses.replace(p, alpha=1.0, beta=0.0)
+    ref = oracle.problem(p0)
     for _ in range(3):   # and it can be reused as it is left
         C.fill_(float("nan"))
         sg.sgemm_with_plan(plan, A, B, C, 1.0, 0.0, ws)
         torch.cuda.synchronize()
-        assert_parity(p, C.cpu().numpy(), ref, exact=False)
+        assert_parity(p0, C.cpu().numpy(), ref, exact=False)
     # the FFMA kernels leave the counter block (the 3xTF32 mode's) untouched
     assert bool((ws[:sg.WORKSPACE_COUNTER_BYTES] == 0xFF).all())
     with pytest.raises(sg.SgemmError) as e:
