@@ -183,11 +183,13 @@ int choose_tile(int64_t M, int64_t N, int64_t K, int64_t batch, int sms) {
     return 128;
 }
 
-// Kernel the planner names: the scalar-FMA kernel unless the tuning knob
-// kKnobKernel (0 = scalar, 1 = packed) asks otherwise; it exists for sweeps.
-// Measured on GB300 at 8192^3: scalar 59.0 TFLOP/s, packed 54.0 (a packed FMA
-// holds the FMA pipe for two cycles, so it saves issue slots but not pipe
-// time, and its broadcast operand pairs push the kernel past 128 registers).
+// Issue form plan_core names: scalar FMAs unless the tuning knob kKnobKernel
+// (0 = scalar, 1 = packed) asks otherwise.  plan_impl then moves the plans
+// where packed issue measured faster to it (the direct-copy product after the
+// A^T pass, split-K and 64-wide plans; see make_wide and plan_impl_base).
+// Unsplit grids that stage A through registers stay scalar: there the
+// broadcast operand pairs of the packed form push the kernel past 128
+// registers (8192^3 with A staged: scalar 59.0 TFLOP/s, packed 54.0).
 int32_t default_kernel() {
     const int k = tuning(kKnobKernel);
     if (k == kKernelFfma128 || k == kKernelFfma2x128) return k;   // (2: direct-copy plans only)
