@@ -169,7 +169,10 @@ size_t split_workspace(int64_t tiles, int split_k, int64_t tail_start, int tail_
 // under half the SMs while K is too short (<= 768) for split-K to make up
 // for it; 128 otherwise.  Measured on GB300 (TFLOP/s, 64 against 128): 256^3
 // 1.33 / 1.14, 1023x777x513 17.8 / 15.7, but 1024^3 28.9 / 31.5,
-// 1024x768x3072 37.8 / 41.9, 1024x1024x16384 40.6 / 47.0.
+// 1024x768x3072 37.8 / 41.9, 1024x1024x16384 40.6 / 47.0 (with the split the
+// cost model picks for each).  Split grids of 128-wide tiles that load the
+// SMs unevenly are replanned afterwards (choose_balanced_small: 1024^3 then
+// runs 64-wide tiles in eight exact K ranges).
 // The tuning knob kKnobTile (64/128) overrides the choice for sweeps.
 int choose_tile(int64_t M, int64_t N, int64_t K, int64_t batch, int sms) {
     {
