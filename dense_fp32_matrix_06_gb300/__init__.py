@@ -40,6 +40,7 @@ WORKSPACE_COUNTER_BYTES = 16384
 EXPORTED_SYMBOLS = (
     "gemm_plan",
     "gemm_plan_for_sms",
+    "gemm_plan_check",
     "sgemm",
     "sgemm_with_plan",
     "sgemm_status_string",
@@ -155,6 +156,9 @@ def load_library() -> ctypes.CDLL:
         lib.gemm_plan_for_sms.argtypes = [_i64, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _vp,
                                           ctypes.c_int32, ctypes.POINTER(GemmPlan)]
         lib.gemm_plan_for_sms.restype = ctypes.c_int
+        lib.gemm_plan_check.argtypes = [ctypes.POINTER(GemmPlan), _i64, _i64, _i64, _i64, _i64,
+                                        _i64, _vp, _vp, _vp]
+        lib.gemm_plan_check.restype = ctypes.c_int
         lib.sgemm.argtypes = [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _vp]
         lib.sgemm.restype = ctypes.c_int
         lib.sgemm_with_plan.argtypes = [ctypes.POINTER(GemmPlan), _i64, _i64, _i64, _f32, _vp,
@@ -230,6 +234,14 @@ def gemm_plan_for_sms(M: int, N: int, K: int, lda: int, ldb: int, ldc: int, A: i
                                             C or None, sm_count, ctypes.byref(plan)),
            "gemm_plan_for_sms")
     return plan
+
+
+def gemm_plan_check(plan: GemmPlan, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
+                    A: int = 0, B: int = 0, C: int = 0) -> bool:
+    """gemm_plan_check(): whether sgemm_with_plan would accept `plan` for these
+    sizes and pointers' alignment (no device needed)."""
+    return load_library().gemm_plan_check(ctypes.byref(plan), M, N, K, lda, ldb, ldc,
+                                          A or None, B or None, C or None) == 0
 
 
 def sgemm_ptr(M: int, N: int, K: int, alpha: float, A: int, lda: int, B: int, ldb: int,

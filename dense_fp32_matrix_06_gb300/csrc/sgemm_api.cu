@@ -900,6 +900,16 @@ sgemm_status gemm_plan_for_sms(int64_t M, int64_t N, int64_t K, int64_t lda, int
     return plan_impl(M, N, K, lda, ldb, ldc, A, B, C, sm_count, out);
 }
 
+sgemm_status gemm_plan_check(const gemm_plan_t *plan, int64_t M, int64_t N, int64_t K,
+                             int64_t lda, int64_t ldb, int64_t ldc, const void *A,
+                             const void *B, const void *C) {
+    if (!plan) return SGEMM_ERR_INVALID_ARG;
+    const sgemm_status s = check_sizes(M, N, K, lda, ldb, ldc);
+    if (s != SGEMM_OK) return s;
+    return plan_matches(*plan, M, N, K, lda, ldb, ldc, A, B, C) ? SGEMM_OK
+                                                                : SGEMM_ERR_INVALID_ARG;
+}
+
 sgemm_status sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
                    int64_t lda, const float *B, int64_t ldb, float beta, float *C,
                    int64_t ldc, void *stream) {

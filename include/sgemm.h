@@ -191,6 +191,19 @@ sgemm_status sgemm_with_plan(const gemm_plan_t *plan, int64_t M, int64_t N, int6
                              int64_t ldc, void *workspace, size_t workspace_bytes,
                              void *stream);
 
+/*
+ * gemm_plan_check -- the check sgemm_with_plan applies to its plan, without a
+ * device: whether `plan` is one this library can run for these sizes and
+ * these pointers' alignment (A, B, C may be NULL, which counts as aligned).
+ * Every plan gemm_plan or gemm_plan_for_sms returns passes it for the same
+ * arguments; a plan edited by hand may not.
+ * Returns SGEMM_OK, or SGEMM_ERR_INVALID_ARG (bad sizes, plan == NULL, or a
+ * plan that does not match).
+ */
+sgemm_status gemm_plan_check(const gemm_plan_t *plan, int64_t M, int64_t N, int64_t K,
+                             int64_t lda, int64_t ldb, int64_t ldc, const void *A,
+                             const void *B, const void *C);
+
 /* Capacity of the fixed scratch buffer sgemm_noalloc uses: 64 MiB per device. */
 #define SGEMM_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 

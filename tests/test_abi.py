@@ -444,3 +444,49 @@ def test_plan_balanced_small_tiles_needs_aligned_operands_and_no_knobs(lib, tune
     assert plan(1024, 1024, 1024).bm == 128
     tune(split_k=None, schedule=0)
     assert plan(1024, 1024, 1024).bm == 128
+
+
+def _plan_grid():
+    shapes = []
+    for M in (1, 7, 64, 100, 256, 513, 1024, 1536, 2048, 4096, 8192):
+        for N in (1, 64, 200, 768, 1024, 2304, 8192):
+            for K in (1, 16, 64, 100, 256, 300, 768, 1024, 2047, 4096, 16384):
+                shapes.append((M, N, K))
+    return shapes
+
+
+@pytest.mark.parametrize("sms", [152, 132, 80, 8])
+def test_every_planner_output_passes_the_plan_check(lib, sms):
+    """The planner and the check sgemm_with_plan applies must agree: every plan
+    gemm_plan_for_sms returns, over 847 shapes, three layouts (tight, padded,
+    unaligned leading dimensions), a misaligned A and four GPU sizes, passes
+    gemm_plan_check for the same arguments."""
+    bad = []
+    for (M, N, K) in _plan_grid():
+        for lda, ldb, ldc, a in ((K, N, N, 0), (K + 4, N + 8, N + 4, 0),
+                                 (K + 1, N + 3, N + 1, 0), (K, N, N, 4)):
+            p = sg.gemm_plan_for_sms(M, N, K, lda, ldb, ldc, a, 0, 0, sm_count=sms)
+            if not sg.gemm_plan_check(p, M, N, K, lda, ldb, ldc, a, 0, 0):
+                bad.append((M, N, K, lda, ldb, ldc, a))
+    assert not bad, f"{len(bad)} planner outputs rejected, e.g. {bad[:5]}"
+
+
+def test_plan_check_rejects_edited_plans(lib):
+    M = N = K = 2048
+    base = plan(M, N, K)
+    assert sg.gemm_plan_check(base, M, N, K, K, N, N)
+    edits = {
+        "split_k": base.split_k + 1, "grid_ctas": base.grid_ctas + 1,
+        "workspace_bytes": base.workspace_bytes - 1, "bm": 96, "bk": base.bk * 2,
+        "stages": 4, "tiles_m": base.tiles_m + 1, "kernel": 7, "schedule": 5,
+    }
+    for field, value in edits.items():
+        q = sg.GemmPlan.from_buffer_copy(base)
+        setattr(q, field, value)
+        assert not sg.gemm_plan_check(q, M, N, K, K, N, N), field
+    # the same plan for other sizes, or for unaligned B and C
+    assert not sg.gemm_plan_check(base, M + 128, N, K, K, N, N)
+    assert not sg.gemm_plan_check(base, M, N, K, K, N + 1, N + 1)
+    # edge-free plans need whole tiles
+    assert base.edge == 0
+    assert not sg.gemm_plan_check(base, M - 1, N, K, K, N, N)
