@@ -122,3 +122,15 @@ def test_traffic_hash_ignores_comments_not_code():
     assert bench.code_tokens(src) != bench.code_tokens(lit)
     assert "twice" not in bench.code_tokens(src) and '"a // b"' in bench.code_tokens(src)
     assert len(bench.source_hash()) == 16
+
+
+@pytest.mark.parametrize("dist", ["uniform", "normal", "int4"])
+def test_operands_draw_what_make_draws(dist):
+    """workloads.operands (A and B alone, for outputs too large to hold on the
+    host) draws the same seeded values, padding included, as workloads.make."""
+    import numpy as np
+    import workloads
+    p = workloads.make(37, 53, 29, dist=dist, seed=9, lda=31, ldb=57)
+    A, B = workloads.operands(37, 53, 29, dist=dist, seed=9, lda=31, ldb=57)
+    assert A.dtype == np.float32 and B.dtype == np.float32
+    assert np.array_equal(A, p.A) and np.array_equal(B, p.B)
