@@ -49,6 +49,10 @@ def test_build_targets_sm103a_only():
     flags = _build.ARCH_FLAGS
     assert flags == ["-gencode", "arch=compute_103a,code=sm_103a"]
     assert "--use_fast_math" not in _build.NVCC_FLAGS
+    # subnormals are kept (no flush to zero, IEEE division and square root),
+    # so results follow the IEEE oracle at the bottom of the range too
+    for f in ("-ftz=true", "--ftz=true", "-prec-div=false", "-prec-sqrt=false", "-fmad=false"):
+        assert f not in _build.NVCC_FLAGS
 
 
 def test_status_strings(lib):

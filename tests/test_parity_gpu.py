@@ -249,6 +249,33 @@ def test_non_finite_inputs_propagate_as_in_ieee_fp32(sg, tune, knobs):
     assert float(np.abs(C[fin].astype(np.float64) - ref[fin]).max()) / den <= TOL_FFMA
 
 
+@pytest.mark.parametrize("M,N,K,knobs", [
+    (2048, 1024, 512, {}),                  # the A^T pass, then the grid
+    (300, 260, 1000, {}),                   # 64-wide tiles, split K, reduction launch
+    (256, 256, 256, {}),                    # the small-problem kernel
+    (1024, 1024, 1024, {"transpose_a": 0, "tile": 128, "split_k": 4}),   # staged A, split
+])
+def test_subnormal_products_are_not_flushed(sg, tune, M, N, K, knobs):
+    """Operands of magnitude up to 1e-19: every product is below the smallest
+    normal float (1.18e-38), so a build that flushed subnormals to zero would
+    turn each step's result into 0.  IEEE arithmetic keeps the usual
+    tolerance against the oracle (its rounding of subnormal partial sums is
+    absolute, 7e-46, far below K * max|A| * max|B|)."""
+    tune(**knobs)
+    p = workloads.make(M, N, K, seed=81)
+    p = dataclasses.replace(p, A=(p.A * np.float32(1e-19)).astype(np.float32),
+                            B=(p.B * np.float32(1e-19)).astype(np.float32))
+    d = DeviceProblem(p)
+    d.run(sg)
+    C, buf = d.result()
+    d.check_untouched(buf)
+    ref = oracle.problem(p)
+    A, B, _ = logical(p)
+    den = K * float(np.abs(A).max()) * float(np.abs(B).max())
+    assert np.abs(ref).max() > 1e-37                  # the results themselves are not tiny
+    assert float(np.abs(C.astype(np.float64) - ref).max()) / den <= TOL_FFMA
+
+
 def test_empty_shapes_are_no_ops(sg):
     torch = _torch()
     c = torch.full((4, 4), 3.0, device="cuda")
