@@ -494,3 +494,35 @@ def test_plan_check_rejects_edited_plans(lib):
     # edge-free plans need whole tiles
     assert base.edge == 0
     assert not sg.gemm_plan_check(base, M - 1, N, K, K, N, N)
+
+
+def test_balance_rule_invariants_over_the_grid(lib, tune):
+    """Wherever the planner's 128-wide plan is an unevenly loaded split grid
+    (between sms and 1.75 sms CTAs, operands aligned) and the balance rule
+    takes it, the replacement is 64-wide tiles in exact K ranges of at least
+    128, at least one full wave of small CTAs; everywhere else the plan is the
+    one the planner makes with the rule left out (the tile knob at 128 leaves
+    it out, so compare only shapes whose plan is 128-wide either way)."""
+    sms = 152
+    changed = 0
+    for (M, N, K) in _plan_grid():
+        p = plan(M, N, K, sms=sms)
+        if p.bm != 64 or p.split_k < 2 or p.schedule != 0:
+            continue
+        # 64-wide by the tile choice itself (padding >= 40 %, or a small grid with
+        # K <= 768), not by the rule
+        tiles128 = -(-M // 128) * -(-N // 128)
+        if M * N < 0.6 * tiles128 * 128 * 128 or (2 * tiles128 < sms and K <= 768):
+            continue
+        tune(tile=128)
+        base = plan(M, N, K, sms=sms)
+        tune(tile=None)
+        if base.bm != 128 or base.split_k < 2 or base.schedule != 0 or base.tail_split != 1:
+            continue
+        if not (sms < base.grid_ctas <= 1.75 * sms):
+            continue
+        changed += 1
+        assert K % (8 * p.split_k) == 0 and p.k_per_split == K // p.split_k >= 128
+        assert p.grid_ctas >= 8 * sms and p.transpose_a == 0 and p.kernel == 1
+        assert p.edge == (0 if M % 64 == 0 and N % 64 == 0 else 1)
+    assert changed >= 10
